@@ -1,0 +1,191 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention, forward and backward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code, header, table or helper with the CUDA path.
+
+What it computes.  The article "Revolutionizing Web-Based AI: How a Plain
+JavaScript Prototype Paved the Way for High-Performance WebGPU Flash
+Attention 2" (section "Translating to WGSL and Optimizing Passes") describes a
+blocked forward pass that keeps an online-softmax state and never stores the
+N x N attention matrix, and a backward pass that recomputes the attention
+weights from Q, K and the saved log-sum-exp.  Both are exact reorganisations
+of plain softmax attention, so the oracle is that plain definition written out
+in fp64, one (batch, head) at a time, with the N x N score matrix
+materialised:
+
+    S   = scale * Q K^T                 (S[i, j] = -inf where j > i if causal)
+    LSE = m + ln sum_j exp(S[:, j] - m),  m = max_j S[:, j]   (natural log)
+    P   = exp(S - LSE)                  (each row sums to 1)
+    O   = P V
+    D   = rowsum(dO * O)
+    dV  = P^T dO
+    dP  = dO V^T
+    dS  = P * (dP - D)
+    dQ  = scale * dS K
+    dK  = scale * dS^T Q
+
+Readings where the pages are silent (each is stated again where it is used):
+  * causal means key j is visible to query i iff j <= i (N_q = N_k);
+  * LSE is the natural-log log-sum-exp of the *scaled*, masked scores;
+  * a row with no visible key (impossible for N_q = N_k causal) has O = 0,
+    LSE = -inf and zero gradients;
+  * inputs are the bf16 values the GPU receives, widened exactly to fp64, and
+    the scale is the fp32 value the GPU receives, widened to fp64.
+
+Every function here is pinned by tests/test_oracle_pins.py against closed
+forms, invariants, central finite differences, a brute-force scalar loop and
+torch's fp64 CPU attention + autograd.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "as_f64", "fp32_scale", "scores", "apply_causal_mask", "row_logsumexp",
+    "attn_fwd_head", "attn_bwd_head", "attn_fwd", "attn_bwd", "attn_rows",
+]
+
+
+def as_f64(x) -> np.ndarray:
+    """Widen a torch tensor (any float dtype, incl. bf16) or array to fp64 numpy."""
+    if hasattr(x, "detach"):
+        import torch
+        return x.detach().to(device="cpu", dtype=torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def fp32_scale(scale: float) -> float:
+    """The softmax scale exactly as an fp32 argument carries it, widened to fp64."""
+    return float(np.float32(scale))
+
+
+def scores(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """S = scale * Q K^T for one head: q [Nq, d], k [Nk, d] -> [Nq, Nk]."""
+    return scale * (q @ k.T)
+
+
+def apply_causal_mask(S: np.ndarray) -> np.ndarray:
+    """Set S[i, j] = -inf where key j lies after query i (j > i)."""
+    nq, nk = S.shape
+    i = np.arange(nq)[:, None]
+    j = np.arange(nk)[None, :]
+    return np.where(j > i, -np.inf, S)
+
+
+def row_logsumexp(S: np.ndarray) -> np.ndarray:
+    """ln sum_j exp(S[i, j]) per row, shifted by the row max for stability.
+
+    A row whose entries are all -inf gets -inf.
+    """
+    m = S.max(axis=1)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    s = np.exp(S - m_safe[:, None]).sum(axis=1)
+    with np.errstate(divide="ignore"):
+        return np.where(finite, m_safe + np.log(s), -np.inf)
+
+
+def _probabilities(S: np.ndarray, lse: np.ndarray) -> np.ndarray:
+    """P = exp(S - LSE); rows with LSE = -inf (nothing visible) are all zero."""
+    finite = np.isfinite(lse)
+    P = np.exp(S - np.where(finite, lse, 0.0)[:, None])
+    return np.where(finite[:, None], P, 0.0)
+
+
+def attn_fwd_head(q, k, v, scale: float, causal: bool):
+    """Forward pass for one head.  Returns (O [N, d], LSE [N], P [N, N])."""
+    S = scores(q, k, scale)
+    if causal:
+        S = apply_causal_mask(S)
+    lse = row_logsumexp(S)
+    P = _probabilities(S, lse)
+    O = P @ v
+    return O, lse, P
+
+
+def attn_bwd_head(q, k, v, dO, scale: float, causal: bool):
+    """Forward + backward for one head, gradients of L = sum(O * dO).
+
+    Returns a dict with O, LSE, D, dQ, dK, dV (fp64).
+    """
+    O, lse, P = attn_fwd_head(q, k, v, scale, causal)
+    D = (dO * O).sum(axis=1)
+    dV = P.T @ dO
+    dP = dO @ v.T
+    dS = P * (dP - D[:, None])
+    dQ = scale * (dS @ k)
+    dK = scale * (dS.T @ q)
+    return {"O": O, "LSE": lse, "D": D, "dQ": dQ, "dK": dK, "dV": dV}
+
+
+def attn_fwd(q, k, v, scale: float, causal: bool):
+    """Forward over [B, H, N, d] inputs.  Returns (O [B,H,N,d], LSE [B,H,N]) in fp64."""
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    s = fp32_scale(scale)
+    B, H, N, d = q.shape
+    O = np.empty((B, H, N, d))
+    L = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            O[b, h], L[b, h], _ = attn_fwd_head(q[b, h], k[b, h], v[b, h], s, causal)
+    return O, L
+
+
+def attn_bwd(q, k, v, dO, scale: float, causal: bool, heads=None):
+    """Forward + backward over [B, H, N, d] inputs, fp64.
+
+    ``heads`` optionally restricts the work to a list of (b, h) pairs; entries
+    of the returned arrays for other heads are NaN.  Returns a dict with
+    O, LSE, D, dQ, dK, dV.
+    """
+    q, k, v, dO = as_f64(q), as_f64(k), as_f64(v), as_f64(dO)
+    s = fp32_scale(scale)
+    B, H, N, d = q.shape
+    out = {
+        "O": np.full((B, H, N, d), np.nan), "LSE": np.full((B, H, N), np.nan),
+        "D": np.full((B, H, N), np.nan), "dQ": np.full((B, H, N, d), np.nan),
+        "dK": np.full((B, H, N, d), np.nan), "dV": np.full((B, H, N, d), np.nan),
+    }
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads:
+        r = attn_bwd_head(q[b, h], k[b, h], v[b, h], dO[b, h], s, causal)
+        for key, val in r.items():
+            out[key][b, h] = val
+    return out
+
+
+def attn_rows(q, k, v, dO, scale: float, causal: bool, rows):
+    """O, LSE, D and dQ at a chosen set of query rows, for every (b, h).
+
+    Each query row's outputs depend only on that row of Q and dO and on all
+    of K and V, so this is the same definition as ``attn_bwd`` restricted to
+    the rows in ``rows`` (a 1-D integer array).  Returns a dict of arrays
+    shaped [B, H, len(rows)(, d)].
+    """
+    q, k, v, dO = as_f64(q), as_f64(k), as_f64(v), as_f64(dO)
+    s = fp32_scale(scale)
+    rows = np.asarray(rows, dtype=np.int64)
+    B, H, N, d = q.shape
+    R = len(rows)
+    out = {"O": np.empty((B, H, R, d)), "LSE": np.empty((B, H, R)),
+           "D": np.empty((B, H, R)), "dQ": np.empty((B, H, R, d))}
+    cols = np.arange(N)[None, :]
+    for b in range(B):
+        for h in range(H):
+            S = scores(q[b, h][rows], k[b, h], s)                  # [R, N]
+            if causal:
+                S = np.where(cols > rows[:, None], -np.inf, S)
+            lse = row_logsumexp(S)
+            P = _probabilities(S, lse)
+            O = P @ v[b, h]
+            Dr = (dO[b, h][rows] * O).sum(axis=1)
+            dP = dO[b, h][rows] @ v[b, h].T
+            dS = P * (dP - Dr[:, None])
+            out["O"][b, h] = O
+            out["LSE"][b, h] = lse
+            out["D"][b, h] = Dr
+            out["dQ"][b, h] = s * (dS @ k[b, h])
+    return out

@@ -1,0 +1,324 @@
+"""Pins for the fp64 oracle, independent of the oracle itself (CPU only).
+
+The pages print no worked numerical example of attention, so the oracle is
+pinned by what the mathematics fixes: a hand-derived closed form
+(tests/golden/hand_cases.json), the N = 1 case, uniform keys (mean of V),
+row/gradient invariants, central finite differences of L = sum(O * dO), an
+independent brute-force scalar loop, and torch's fp64 CPU attention with
+autograd.  ``test_planted_mistakes_are_caught`` plants plausible mistakes in
+a copy of the oracle and checks that at least one pin fails for each.
+"""
+import inspect
+import json
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import attention as oa
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+
+
+# ---------------------------------------------------------------------------
+# Pins written against an implementation with attn_bwd_head's signature, so
+# they can be run on the oracle and on mutated copies of it.
+# ---------------------------------------------------------------------------
+
+def _rand(n, d, seed, scale=1.0):
+    r = np.random.Generator(np.random.PCG64(seed))
+    return [scale * r.standard_normal((n, d)) for _ in range(4)]
+
+
+def pin_hand_case(impl):
+    g = json.load(open(GOLDEN))
+    x = {k: np.array(v, dtype=np.float64) for k, v in g["inputs"].items() if k != "scale"}
+    for mode in ("noncausal", "causal"):
+        r = impl(x["q"], x["k"], x["v"], x["dO"], g["inputs"]["scale"], mode == "causal")
+        for key, want in g[mode].items():
+            np.testing.assert_allclose(r[key], np.array(want), rtol=0, atol=1e-12,
+                                       err_msg=f"{mode} {key}")
+
+
+def pin_single_key(impl):
+    # N = 1: the only key has weight 1, so O = V_0, LSE = s q.k, dV = dO, dQ = dK = 0.
+    for causal in (False, True):
+        for d in (1, 3, 16):
+            q, k, v, dO = _rand(1, d, 11 + d)
+            s = 0.37
+            r = impl(q, k, v, dO, s, causal)
+            np.testing.assert_allclose(r["O"], v, atol=1e-14)
+            np.testing.assert_allclose(r["LSE"], [s * float(q[0] @ k[0])], atol=1e-14)
+            np.testing.assert_allclose(r["dV"], dO, atol=1e-14)
+            np.testing.assert_allclose(r["dQ"], 0, atol=1e-14)
+            np.testing.assert_allclose(r["dK"], 0, atol=1e-14)
+
+
+def pin_uniform_keys(impl):
+    # All K rows equal: every visible key gets the same weight, so O_i is the
+    # mean of the visible V rows, LSE_i = s q_i.k + ln(#visible) and dQ = 0.
+    N, d, s = 9, 5, 0.4
+    q, _, v, dO = _rand(N, d, 21)
+    krow = np.random.Generator(np.random.PCG64(22)).standard_normal(d)
+    k = np.tile(krow, (N, 1))
+    for causal in (False, True):
+        r = impl(q, k, v, dO, s, causal)
+        for i in range(N):
+            vis = i + 1 if causal else N
+            np.testing.assert_allclose(r["O"][i], v[:vis].mean(axis=0), atol=1e-12)
+            np.testing.assert_allclose(r["LSE"][i], s * q[i] @ krow + math.log(vis), atol=1e-12)
+        np.testing.assert_allclose(r["dQ"], 0, atol=1e-12)
+
+
+def pin_zero_query(impl):
+    # Q = 0 makes every score 0: uniform weights regardless of K.
+    N, d, s = 7, 3, 0.9
+    _, k, v, dO = _rand(N, d, 31)
+    q = np.zeros((N, d))
+    for causal in (False, True):
+        r = impl(q, k, v, dO, s, causal)
+        for i in range(N):
+            vis = i + 1 if causal else N
+            np.testing.assert_allclose(r["O"][i], v[:vis].mean(axis=0), atol=1e-12)
+            np.testing.assert_allclose(r["LSE"][i], math.log(vis), atol=1e-12)
+
+
+def pin_gradient_invariants(impl):
+    # Rows of P sum to 1 => rows of dS sum to 0 => sum_j dK_j = 0 and
+    # sum_j dV_j = sum_i dO_i.
+    N, d, s = 13, 6, 0.5
+    q, k, v, dO = _rand(N, d, 41)
+    for causal in (False, True):
+        r = impl(q, k, v, dO, s, causal)
+        np.testing.assert_allclose(r["dK"].sum(axis=0), 0, atol=1e-12)
+        np.testing.assert_allclose(r["dV"].sum(axis=0), dO.sum(axis=0), atol=1e-12)
+
+
+def pin_shift_invariance(impl):
+    # K -> K + 1 c^T leaves O unchanged and shifts LSE_i by s q_i.c;
+    # V -> V + 1 c^T shifts O by c.
+    N, d, s = 10, 4, 0.6
+    q, k, v, dO = _rand(N, d, 51)
+    c = np.random.Generator(np.random.PCG64(52)).standard_normal(d)
+    for causal in (False, True):
+        r0 = impl(q, k, v, dO, s, causal)
+        r1 = impl(q, k + c, v, dO, s, causal)
+        np.testing.assert_allclose(r1["O"], r0["O"], atol=1e-12)
+        np.testing.assert_allclose(r1["LSE"], r0["LSE"] + s * (q @ c), atol=1e-12)
+        r2 = impl(q, k, v + c, dO, s, causal)
+        np.testing.assert_allclose(r2["O"], r0["O"] + c, atol=1e-12)
+
+
+def pin_key_permutation(impl):
+    # Non-causal attention is invariant to a joint permutation of K and V rows,
+    # and dK, dV permute with them.
+    N, d, s = 11, 4, 0.7
+    q, k, v, dO = _rand(N, d, 61)
+    perm = np.random.Generator(np.random.PCG64(62)).permutation(N)
+    r0 = impl(q, k, v, dO, s, False)
+    r1 = impl(q, k[perm], v[perm], dO, s, False)
+    np.testing.assert_allclose(r1["O"], r0["O"], atol=1e-12)
+    np.testing.assert_allclose(r1["dQ"], r0["dQ"], atol=1e-12)
+    np.testing.assert_allclose(r1["dK"], r0["dK"][perm], atol=1e-12)
+    np.testing.assert_allclose(r1["dV"], r0["dV"][perm], atol=1e-12)
+
+
+def pin_finite_differences(impl):
+    # Central differences of L = sum(O * dO) against the analytic gradients.
+    h = 1e-6
+    for causal in (False, True):
+        for (N, d, seed) in ((5, 3, 71), (8, 4, 72), (2, 1, 73)):
+            q, k, v, dO = _rand(N, d, seed)
+            s = 0.8
+            r = impl(q, k, v, dO, s, causal)
+
+            def loss(qq, kk, vv):
+                return float((impl(qq, kk, vv, dO, s, causal)["O"] * dO).sum())
+
+            for name, grad in (("q", r["dQ"]), ("k", r["dK"]), ("v", r["dV"])):
+                fd = np.zeros_like(grad)
+                for idx in np.ndindex(*grad.shape):
+                    args = {"q": q.copy(), "k": k.copy(), "v": v.copy()}
+                    args[name][idx] += h
+                    lp = loss(args["q"], args["k"], args["v"])
+                    args[name][idx] -= 2 * h
+                    lm = loss(args["q"], args["k"], args["v"])
+                    fd[idx] = (lp - lm) / (2 * h)
+                err = np.abs(fd - grad).max() / max(1.0, np.abs(grad).max())
+                assert err < 1e-7, (name, causal, N, d, err)
+
+
+def _brute_force(q, k, v, dO, s, causal):
+    """Scalar-loop attention written independently of the oracle (pure Python)."""
+    N, d = len(q), len(q[0])
+    O = [[0.0] * d for _ in range(N)]
+    LSE = [0.0] * N
+    P = [[0.0] * N for _ in range(N)]
+    for i in range(N):
+        vis = [j for j in range(N) if (not causal or j <= i)]
+        logits = {j: s * sum(q[i][c] * k[j][c] for c in range(d)) for j in vis}
+        top = max(logits.values())
+        tot = sum(math.exp(x - top) for x in logits.values())
+        LSE[i] = top + math.log(tot)
+        for j in vis:
+            P[i][j] = math.exp(logits[j] - LSE[i])
+        for c in range(d):
+            O[i][c] = sum(P[i][j] * v[j][c] for j in vis)
+    dQ = [[0.0] * d for _ in range(N)]
+    dK = [[0.0] * d for _ in range(N)]
+    dV = [[0.0] * d for _ in range(N)]
+    for i in range(N):
+        # dL/dlogit_ij = p_ij * dO_i . (v_j - O_i)
+        for j in range(N):
+            if P[i][j] == 0.0:
+                continue
+            g = P[i][j] * sum(dO[i][c] * (v[j][c] - O[i][c]) for c in range(d))
+            for c in range(d):
+                dQ[i][c] += s * g * k[j][c]
+                dK[j][c] += s * g * q[i][c]
+                dV[j][c] += P[i][j] * dO[i][c]
+    return {"O": np.array(O), "LSE": np.array(LSE), "dQ": np.array(dQ),
+            "dK": np.array(dK), "dV": np.array(dV)}
+
+
+def pin_brute_force(impl):
+    N, d, s = 12, 5, 0.45
+    q, k, v, dO = _rand(N, d, 81, scale=1.5)
+    for causal in (False, True):
+        want = _brute_force(q.tolist(), k.tolist(), v.tolist(), dO.tolist(), s, causal)
+        got = impl(q, k, v, dO, s, causal)
+        for key in want:
+            np.testing.assert_allclose(got[key], want[key], rtol=1e-11, atol=1e-12, err_msg=key)
+
+
+def pin_torch_sdpa(impl):
+    # Library special case: torch fp64 CPU attention + autograd.
+    N, d, s = 17, 8, 0.3
+    q, k, v, dO = _rand(N, d, 91)
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+        o = torch.nn.functional.scaled_dot_product_attention(
+            tq[None, None], tk[None, None], tv[None, None], is_causal=causal, scale=s)[0, 0]
+        (o * torch.tensor(dO)).sum().backward()
+        logits = s * (torch.tensor(q) @ torch.tensor(k).T)
+        if causal:
+            logits = logits.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+        lse = torch.logsumexp(logits, dim=1)
+        r = impl(q, k, v, dO, s, causal)
+        np.testing.assert_allclose(r["O"], o.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(r["LSE"], lse.numpy(), atol=1e-12)
+        np.testing.assert_allclose(r["dQ"], tq.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(r["dK"], tk.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(r["dV"], tv.grad.numpy(), atol=1e-12)
+
+
+PINS = [pin_hand_case, pin_single_key, pin_uniform_keys, pin_zero_query,
+        pin_gradient_invariants, pin_shift_invariance, pin_key_permutation,
+        pin_finite_differences, pin_brute_force, pin_torch_sdpa]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_head_pins(pin):
+    pin(oracle.attn_bwd_head)
+
+
+# ---------------------------------------------------------------------------
+# Batched entry points agree with the per-head function and with each other.
+# ---------------------------------------------------------------------------
+
+def test_batched_matches_per_head_and_rows():
+    w = workloads.WORKLOADS["tiny"]
+    x = workloads.workload_inputs(w)
+    for causal in (True, False):
+        full = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dO"], w.scale, causal)
+        O, L = oracle.attn_fwd(x["q"], x["k"], x["v"], w.scale, causal)
+        np.testing.assert_array_equal(O, full["O"])
+        np.testing.assert_array_equal(L, full["LSE"])
+        rows = workloads.sample_rows(w.N, 9, 5)
+        rr = oracle.attn_rows(x["q"], x["k"], x["v"], x["dO"], w.scale, causal, rows)
+        for key in ("O", "LSE", "D", "dQ"):
+            np.testing.assert_allclose(rr[key], full[key][:, :, rows], rtol=1e-12, atol=1e-12)
+
+
+def test_tiny_workload_against_brute_force_and_probability_rows():
+    # The tiny workload end to end (bf16 inputs widened to fp64) against the
+    # scalar loop, plus: every probability row sums to one.
+    w = workloads.WORKLOADS["tiny"]
+    x = workloads.workload_inputs(w)
+    q, k, v, dO = (oracle.as_f64(x[n])[0, 0][:24, :8] for n in ("q", "k", "v", "dO"))
+    s = oracle.fp32_scale(w.scale)
+    for causal in (True, False):
+        want = _brute_force(q.tolist(), k.tolist(), v.tolist(), dO.tolist(), s, causal)
+        got = oracle.attn_bwd_head(q, k, v, dO, s, causal)
+        for key in want:
+            np.testing.assert_allclose(got[key], want[key], rtol=1e-11, atol=1e-12)
+        _, _, P = oracle.attn_fwd_head(q, k, v, s, causal)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+        if causal:
+            assert np.all(np.triu(P, 1) == 0)
+
+
+def test_lse_matches_library_logsumexp_large_logits():
+    # Large logits (the stress workload's x3 scaling and beyond): the stable
+    # LSE equals scipy's logsumexp and never overflows.
+    from scipy.special import logsumexp
+    r = np.random.Generator(np.random.PCG64(3))
+    S = 40.0 * r.standard_normal((16, 33))
+    np.testing.assert_allclose(oa.row_logsumexp(S), logsumexp(S, axis=1), rtol=0, atol=1e-12)
+    S[3, :] = -np.inf
+    assert oa.row_logsumexp(S)[3] == -np.inf
+
+
+def test_fp32_scale_is_what_the_gpu_receives():
+    assert oracle.fp32_scale(1 / math.sqrt(128)) == float(np.float32(1 / math.sqrt(128)))
+    assert oracle.fp32_scale(0.1) != 0.1
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: each mutant of the oracle must fail at least one pin.
+# ---------------------------------------------------------------------------
+
+MUTANTS = {
+    "dropped_D_term": ("dS = P * (dP - D[:, None])", "dS = P * dP"),
+    "flipped_dS_sign": ("dS = P * (dP - D[:, None])", "dS = P * (D[:, None] - dP)"),
+    "transposed_dK": ("dK = scale * (dS.T @ q)", "dK = scale * (dS @ q)"),
+    "dQ_missing_scale": ("dQ = scale * (dS @ k)", "dQ = dS @ k"),
+    "dV_not_transposed": ("dV = P.T @ dO", "dV = P @ dO"),
+    "D_from_dO_only": ("D = (dO * O).sum(axis=1)", "D = dO.sum(axis=1)"),
+    "dP_wrong_operand": ("dP = dO @ v.T", "dP = dO @ k.T"),
+}
+
+FWD_MUTANTS = {
+    "mask_hides_diagonal": ("np.where(j > i, -np.inf, S)", "np.where(j >= i, -np.inf, S)"),
+    "mask_off_by_one_late": ("np.where(j > i, -np.inf, S)", "np.where(j > i + 1, -np.inf, S)"),
+    "scale_applied_twice": ("return scale * (q @ k.T)", "return scale * scale * (q @ k.T)"),
+    "lse_in_base_2": ("m_safe + np.log(s)", "m_safe + np.log2(s)"),
+    "lse_without_max": ("m_safe + np.log(s)", "np.log(s)"),
+}
+
+
+def _mutant_module(src_fn_names, old, new):
+    """Copy oracle.attention into a fresh module with one textual mistake planted."""
+    src = inspect.getsource(oa)
+    assert src.count(old) == 1, f"mutation target not unique: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS) + sorted(FWD_MUTANTS))
+def test_planted_mistakes_are_caught(name):
+    old, new = MUTANTS.get(name) or FWD_MUTANTS[name]
+    mod = _mutant_module(None, old, new)
+    failed = []
+    for pin in PINS:
+        try:
+            pin(mod.attn_bwd_head)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught planted mistake {name}"
