@@ -1,0 +1,107 @@
+/*
+ * fa2.h - C ABI of the GB300 (sm_103a) FlashAttention-2 library.
+ *
+ * Operation.  Exact scaled-dot-product attention, forward and backward, as
+ * described by the article "Revolutionizing Web-Based AI: How a Plain
+ * JavaScript Prototype Paved the Way for High-Performance WebGPU Flash
+ * Attention 2", section "Translating to WGSL and Optimizing Passes":
+ *   - forward: per (batch, head, query tile), walk K and V in blocks with an
+ *     online softmax (running max m, running sum l) and never store the
+ *     N x N score matrix;
+ *   - backward: recompute the attention weights tile by tile from the saved
+ *     Q, K and the per-row log-sum-exp (LSE).
+ * With S = scale * Q K^T (S[i][j] = -inf for j > i when causal):
+ *   LSE_i = ln sum_j exp(S_ij)          O = softmax(S) V
+ *   D_i = sum_c dO_ic O_ic              dS = P * (dO V^T - D)
+ *   dQ = scale dS K   dK = scale dS^T Q   dV = P^T dO,  P = exp(S - LSE).
+ *
+ * Layout.  q, k, v, o, dO, dq, dk, dv: bf16 (raw 16-bit storage), row-major
+ * contiguous [B, H, N, d].  lse: fp32 [B, H, N], natural log of the scaled,
+ * masked scores.  Queries and keys have the same length N.  causal != 0
+ * means key j is visible to query i iff j <= i.
+ *
+ * Pointers.  Every tensor pointer is a DEVICE pointer on the current CUDA
+ * device.  bf16 tensors must be 16-byte aligned; lse 4-byte aligned.
+ * Outputs must not overlap inputs or each other.  The caller owns all
+ * memory; the library keeps no state except one-time kernel attributes.
+ *
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ * Calls only enqueue work and return; results are valid once the stream
+ * has been synchronised.
+ *
+ * Errors.  Every argument is checked before anything is enqueued; on a bad
+ * argument nothing is launched and a nonzero fa2_status is returned.  No
+ * entry point aborts, traps or prints.  Kernels bound every internal wait
+ * (2 s); a wait that runs out sets a device status word that
+ * fa2_device_status() reads.
+ */
+#ifndef FA2_GB300_H
+#define FA2_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA2_OK = 0,
+  FA2_ERR_NULL = 1,      /* a required pointer is NULL                      */
+  FA2_ERR_SHAPE = 2,     /* B, H or N < 1, or a size beyond the index range */
+  FA2_ERR_HEADDIM = 3,   /* d not in {16, 32, 64, 128}                      */
+  FA2_ERR_ALIGN = 4,     /* a pointer is not aligned as stated above        */
+  FA2_ERR_SCALE = 5,     /* scale not finite or not > 0                     */
+  FA2_ERR_ALLOC = 6,     /* stream-ordered workspace allocation failed      */
+  FA2_ERR_CUDA = 7,      /* a CUDA runtime / driver call or launch failed   */
+  FA2_ERR_WORKSPACE = 8, /* caller workspace NULL, too small or misaligned  */
+  FA2_ERR_ALIAS = 9      /* an output overlaps an input or another output   */
+} fa2_status;
+
+/*
+ * Forward pass.  Writes o [B,H,N,d] bf16 and lse [B,H,N] fp32.
+ * Source: the article's forward-pass bullet (blocked K/V walk, online
+ * softmax state, no stored score matrix) and backward-pass bullet (the
+ * saved log-sum-exp).  One kernel launch.
+ */
+int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+            float scale, int causal, void* stream);
+
+/*
+ * Backward pass for L with dL/dO = dO.  Reads q, k, v, the forward's o and
+ * lse and dO; writes dq, dk, dv [B,H,N,d] bf16.  Source: the article's
+ * backward-pass bullet (recompute P from Q, K and LSE) plus the standard
+ * D = rowsum(dO * O) identity.  Enqueues three kernels (D preprocess, main,
+ * dQ convert).  Scratch (fa2_bwd_workspace_bytes bytes) is obtained with
+ * cudaMallocAsync and released with cudaFreeAsync on `stream`.
+ */
+int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+            void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/* Bytes of device scratch fa2_bwd needs: D (fp32 [B,H,N]) and the fp32 dQ
+ * accumulator [B,H,N,d], each 256-byte aligned.  0 on invalid sizes. */
+size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* fa2_bwd with caller-provided scratch: `workspace` is a device pointer,
+ * 256-byte aligned, of at least fa2_bwd_workspace_bytes(B,H,N,d) bytes,
+ * owned by the caller and not used by anything else until the stream has
+ * passed this call.  Allocates nothing. */
+int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* fa2_status_string(int status);
+
+/* Read (and if `reset` != 0, clear) the kernels' device status word on the
+ * current device: 0 = every wait completed, 1 = some wait timed out.
+ * Synchronous with respect to the device. Returns an fa2_status. */
+int fa2_device_status(int* value, int reset);
+
+/* ABI version of this header (major * 100 + minor). */
+int fa2_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_GB300_H */

@@ -1,0 +1,128 @@
+"""The C-ABI library loads, exports every entry point include/fa2.h declares,
+and rejects bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tiled_exact_attention_fa2_gb300 as fa2
+from tiled_exact_attention_fa2_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa2.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa2_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa2_fwd", "fa2_bwd", "fa2_bwd_workspace_bytes", "fa2_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_symbol():
+    for name in declared_functions():
+        assert name in fa2._SIGNATURES, name
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert fa2.fa2_status_string(s)
+    assert fa2.fa2_status_string(0) == "ok"
+    assert "unknown" in fa2.fa2_status_string(12345)
+    assert fa2.fa2_abi_version() == 100
+
+
+def test_workspace_bytes(lib):
+    # D (fp32 per row) + dQ accumulator (fp32 per element), 256-byte rounded
+    assert fa2.fa2_bwd_workspace_bytes(2, 16, 4096, 128) == 2 * 16 * 4096 * 4 + 2 * 16 * 4096 * 128 * 4
+    assert fa2.fa2_bwd_workspace_bytes(1, 1, 1, 16) == 256 + 256
+    assert fa2.fa2_bwd_workspace_bytes(0, 1, 1, 16) == 0
+    assert fa2.fa2_bwd_workspace_bytes(1, 1, 1, 48) == 0
+
+
+A = 1 << 20  # a fake, 16-byte aligned "device" address; never dereferenced
+
+
+def fwd(lib, q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, B=1, H=1, N=128, d=64, scale=0.125, causal=1):
+    return lib.fa2_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, None)
+
+
+def bwd(lib, ptrs=None, B=1, H=1, N=128, d=64, scale=0.125):
+    p = ptrs or [A * (i + 1) for i in range(9)]
+    return lib.fa2_bwd(*p, B, H, N, d, scale, 1, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert fwd(lib, q=None) == 1
+    assert fwd(lib, lse=None) == 1
+    assert fwd(lib, B=0) == 2
+    assert fwd(lib, N=0) == 2
+    assert fwd(lib, H=-1) == 2
+    for d in (0, 8, 48, 96, 256):
+        assert fwd(lib, d=d) == 3
+    assert fwd(lib, q=A + 8) == 4
+    assert fwd(lib, o=4 * A + 2) == 4
+    assert fwd(lib, lse=5 * A + 2) == 4
+    for s in (0.0, -0.1, float("inf"), float("nan")):
+        assert fwd(lib, scale=s) == 5
+    assert fwd(lib, o=A) == 9            # o aliases q
+    assert fwd(lib, lse=3 * A + 64) == 9  # lse inside v
+    assert lib.fa2_fwd(A, 2 * A, 3 * A, 4 * A, 5 * A, 1, 1, (1 << 30) + 1, 64, 0.1, 1, None) == 2
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    p = [A * (i + 1) for i in range(9)]
+    for i in range(9):
+        q = list(p)
+        q[i] = None
+        assert bwd(lib, q) == 1
+    assert bwd(lib, B=0) == 2
+    assert bwd(lib, d=24) == 3
+    q = list(p)
+    q[6] = 7 * A + 4  # dq misaligned
+    assert bwd(lib, q) == 4
+    assert bwd(lib, scale=float("nan")) == 5
+    q = list(p)
+    q[7] = q[6]  # dk == dq
+    assert bwd(lib, q) == 9
+    q = list(p)
+    q[8] = q[0]  # dv == q
+    assert bwd(lib, q) == 9
+
+
+def test_bwd_ws_rejects_bad_workspace(lib):
+    p = [A * (i + 1) for i in range(9)]
+    need = fa2.fa2_bwd_workspace_bytes(1, 1, 128, 64)
+    ws = 64 * A
+    assert lib.fa2_bwd_ws(*p, 1, 1, 128, 64, 0.125, 1, None, need, None) == 8
+    assert lib.fa2_bwd_ws(*p, 1, 1, 128, 64, 0.125, 1, ws, need - 1, None) == 8
+    assert lib.fa2_bwd_ws(*p, 1, 1, 128, 64, 0.125, 1, ws + 16, need, None) == 8
+
+
+def test_device_status_null(lib):
+    assert lib.fa2_device_status(None, 0) == 1
+
+
+def test_python_binding_checks_metadata():
+    import torch
+    q = torch.zeros(1, 1, 4, 16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa2.fa2_fwd(q, q, q)  # CPU tensors are refused before any call
+    with pytest.raises(ValueError):
+        fa2.fa2_fwd(q.float(), q, q)

@@ -1,0 +1,200 @@
+"""GB300 (sm_103a) FlashAttention-2: thin Python binding of the C ABI in include/fa2.h.
+
+Every step of the computation runs in the CUDA kernels of
+``libfa2_gb300.so``; this module only checks tensor metadata, allocates
+outputs with torch and passes raw pointers, sizes and the current CUDA stream.
+There is no fallback: if the shared library is missing, every call raises.
+
+Build the library with ``python -c "import __graft_entry__ as g; g.build()"``
+(or ``python tiled_exact_attention_fa2_gb300/_build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "FA2Error", "load_library", "fa2_fwd", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
+    "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
+    "FA2_OK",
+]
+
+FA2_OK = 0
+_LIB: Optional[ctypes.CDLL] = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "fa2_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_bwd_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "fa2_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa2_status_string": (ctypes.c_char_p, [_i]),
+    "fa2_device_status": (_i, [ctypes.POINTER(_i), _i]),
+    "fa2_abi_version": (_i, []),
+}
+
+
+class FA2Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed with status {status}: {fa2_status_string(status)}")
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libfa2_gb300.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{os.path.basename(path)} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == _build.LIB_PATH:
+        _LIB = lib
+    return lib
+
+
+def fa2_status_string(status: int) -> str:
+    return load_library().fa2_status_string(int(status)).decode()
+
+
+def fa2_abi_version() -> int:
+    return load_library().fa2_abi_version()
+
+
+def fa2_device_status(reset: bool = False) -> int:
+    """Device status word of the kernels (0 = every internal wait completed)."""
+    v = _i(0)
+    rc = load_library().fa2_device_status(ctypes.byref(v), 1 if reset else 0)
+    if rc != FA2_OK:
+        raise FA2Error("fa2_device_status", rc)
+    return v.value
+
+
+def fa2_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return load_library().fa2_bwd_workspace_bytes(B, H, N, d)
+
+
+def _shape(t: torch.Tensor, name: str):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, N, d], got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return tuple(t.shape)
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _scale(scale, d):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def fa2_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, scale: Optional[float] = None, causal: bool = True,
+            stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O [B,H,N,d] bf16 and LSE [B,H,N] fp32 of softmax(scale Q K^T) V."""
+    lib = load_library()
+    B, H, N, d = _shape(q, "q")
+    if _shape(k, "k") != (B, H, N, d) or _shape(v, "v") != (B, H, N, d):
+        raise ValueError("q, k and v must have the same shape")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    _shape(o, "o")
+    rc = lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                     _scale(scale, d), 1 if causal else 0, _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_fwd", rc)
+    return o, lse
+
+
+def _bwd_common(q, k, v, o, dO, lse, dq, dk, dv):
+    B, H, N, d = _shape(q, "q")
+    for name, t in (("k", k), ("v", v), ("o", o), ("dO", dO)):
+        if _shape(t, name) != (B, H, N, d):
+            raise ValueError(f"{name} must have q's shape")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _shape(t, name)
+    return (B, H, N, d), dq, dk, dv
+
+
+def fa2_bwd(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optional[float] = None,
+            causal: bool = True, stream=None):
+    """dQ, dK, dV (bf16) of L with dL/dO = dO; scratch is allocated stream-ordered inside the library."""
+    lib = load_library()
+    (B, H, N, d), dq, dk, dv = _bwd_common(q, k, v, o, dO, lse, dq, dk, dv)
+    rc = lib.fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, _scale(scale, d),
+                     1 if causal else 0, _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd", rc)
+    return dq, dk, dv
+
+
+def fa2_bwd_ws(q, k, v, o, dO, lse, workspace: torch.Tensor, dq=None, dk=None, dv=None,
+               scale: Optional[float] = None, causal: bool = True, stream=None):
+    """fa2_bwd with caller-owned scratch (a CUDA byte tensor of fa2_bwd_workspace_bytes bytes)."""
+    lib = load_library()
+    (B, H, N, d), dq, dk, dv = _bwd_common(q, k, v, o, dO, lse, dq, dk, dv)
+    rc = lib.fa2_bwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, _scale(scale, d),
+                        1 if causal else 0, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_ws", rc)
+    return dq, dk, dv
+
+
+def attention_step_from_host(host: dict, dev: dict, causal: bool = True, scale: Optional[float] = None,
+                             stream=None) -> dict:
+    """One forward + backward pass starting from pinned host tensors.
+
+    ``host`` holds pinned CPU bf16 tensors q, k, v, dO and pinned outputs
+    o, lse, dq, dk, dv; ``dev`` holds device buffers of the same names.
+    Copies the inputs host->device, runs fa2_fwd and fa2_bwd, copies every
+    result device->host, all on one stream (asynchronously; synchronise the
+    stream before reading ``host``).
+    """
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        for name in ("q", "k", "v", "dO"):
+            dev[name].copy_(host[name], non_blocking=True)
+        fa2_fwd(dev["q"], dev["k"], dev["v"], dev["o"], dev["lse"], scale, causal, s)
+        fa2_bwd(dev["q"], dev["k"], dev["v"], dev["o"], dev["dO"], dev["lse"], dev["dq"], dev["dk"], dev["dv"],
+                scale, causal, s)
+        for name in ("o", "lse", "dq", "dk", "dv"):
+            host[name].copy_(dev[name], non_blocking=True)
+    return host

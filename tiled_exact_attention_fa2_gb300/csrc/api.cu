@@ -1,0 +1,228 @@
+// C-ABI entry points declared in include/fa2.h: argument validation, TMA
+// descriptor construction and kernel dispatch.  Host code only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "fa2.h"
+#include "launch.h"
+
+namespace fa2 {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled comes from the driver; fetching it through the
+// runtime keeps the library free of a link-time libcuda dependency.
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+constexpr int kRowsPerTile = 128;
+
+// [B*H, N, d] bf16 view, box = [1, 128 rows, min(d, 64) columns], swizzle
+// width = box row width.  Rows past N in a head read as zero.
+bool make_tmap(CUtensorMap* out, const void* base, int BH, int N, int d) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const int box_cols = d >= 64 ? 64 : d;
+  const CUtensorMapSwizzle swz = d >= 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), kRowsPerTile, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+Range range_of(const void* p, size_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return {lo, lo + bytes};
+}
+
+int check_sizes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA2_ERR_SHAPE;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long tiles = (static_cast<long long>(N) + kRowsPerTile - 1) / kRowsPerTile;
+  // grid = tiles * B * H CTAs (32-bit); TMA dims < 2^32; row indices in int.
+  if (BH > 0x7fffffffLL || tiles * BH > 0x7fffffffLL || N > (1 << 30)) return FA2_ERR_SHAPE;
+  return FA2_OK;
+}
+
+int check_scale(float scale) { return (std::isfinite(scale) && scale > 0.f) ? FA2_OK : FA2_ERR_SCALE; }
+
+constexpr size_t kWsAlign = 256;
+size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+size_t workspace_bytes(int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
+}
+
+int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA2_ERR_NULL;
+  if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (int rc = check_scale(scale)) return rc;
+  const void* bf[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void* p : bf)
+    if (!aligned(p, 16)) return FA2_ERR_ALIGN;
+  if (!aligned(lse, 4)) return FA2_ERR_ALIGN;
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  const Range outs[] = {range_of(dq, tb), range_of(dk, tb), range_of(dv, tb)};
+  const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(o, tb), range_of(dO, tb),
+                       range_of(lse, lb)};
+  for (int a = 0; a < 3; ++a) {
+    for (const Range& r : ins)
+      if (overlap(outs[a], r)) return FA2_ERR_ALIAS;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlap(outs[a], outs[b])) return FA2_ERR_ALIAS;
+  }
+  return FA2_OK;
+}
+
+int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+            void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* ws, cudaStream_t st) {
+  const int BH = B * H;
+  TmapSet tm;
+  if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, BH, N, d) || !make_tmap(&tm.v, v, BH, N, d) ||
+      !make_tmap(&tm.dO, dO, BH, N, d))
+    return FA2_ERR_CUDA;
+  const size_t rows = static_cast<size_t>(BH) * N;
+  float* Dvec = static_cast<float*>(ws);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(rows * sizeof(float)));
+  return launch_bwd(tm, o, dO, lse, dq, dk, dv, Dvec, dq_acc, BH, N, d, scale, causal != 0, st) == 0
+             ? FA2_OK
+             : FA2_ERR_CUDA;
+}
+
+}  // namespace
+
+int ensure_max_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return 0;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return -1;
+  done.insert({kernel, dev});
+  return 0;
+}
+
+}  // namespace fa2
+
+using namespace fa2;
+
+extern "C" {
+
+int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+            float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
+  if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (int rc = check_scale(scale)) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA2_ERR_ALIGN;
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  const Range ro = range_of(o, tb), rl = range_of(lse, lb);
+  const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb)};
+  for (const Range& r : ins)
+    if (overlap(ro, r) || overlap(rl, r)) return FA2_ERR_ALIAS;
+  if (overlap(ro, rl)) return FA2_ERR_ALIAS;
+
+  const int BH = B * H;
+  TmapSet tm;
+  if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, BH, N, d) || !make_tmap(&tm.v, v, BH, N, d))
+    return FA2_ERR_CUDA;
+  return launch_fwd(tm, o, lse, BH, N, d, scale, causal != 0, static_cast<cudaStream_t>(stream)) == 0
+             ? FA2_OK
+             : FA2_ERR_CUDA;
+}
+
+size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d) != FA2_OK) return 0;
+  return workspace_bytes(B, H, N, d);
+}
+
+int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+               void* workspace, size_t workspace_bytes_given, void* stream) {
+  if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale)) return rc;
+  if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < workspace_bytes(B, H, N, d))
+    return FA2_ERR_WORKSPACE;
+  return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                 static_cast<cudaStream_t>(stream));
+}
+
+int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+            void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* stream) {
+  if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale)) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = workspace_bytes(B, H, N, d);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess || !ws) {
+    cudaGetLastError();
+    return FA2_ERR_ALLOC;
+  }
+  const int rc = run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, st);
+  if (cudaFreeAsync(ws, st) != cudaSuccess) return FA2_ERR_CUDA;
+  return rc;
+}
+
+const char* fa2_status_string(int status) {
+  switch (status) {
+    case FA2_OK: return "ok";
+    case FA2_ERR_NULL: return "a required pointer is NULL";
+    case FA2_ERR_SHAPE: return "B, H or N < 1 or beyond the supported index range";
+    case FA2_ERR_HEADDIM: return "head dim must be 16, 32, 64 or 128";
+    case FA2_ERR_ALIGN: return "pointer misaligned (bf16 tensors need 16 bytes, lse 4)";
+    case FA2_ERR_SCALE: return "scale must be finite and > 0";
+    case FA2_ERR_ALLOC: return "stream-ordered workspace allocation failed";
+    case FA2_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case FA2_ERR_WORKSPACE: return "workspace NULL, too small or not 256-byte aligned";
+    case FA2_ERR_ALIAS: return "an output overlaps an input or another output";
+    default: return "unknown fa2 status";
+  }
+}
+
+int fa2_device_status(int* value, int reset) {
+  if (!value) return FA2_ERR_NULL;
+  int a = 0, b = 0;
+  if (read_fwd_status(&a, reset != 0) != 0 || read_bwd_status(&b, reset != 0) != 0) return FA2_ERR_CUDA;
+  *value = a > b ? a : b;
+  return FA2_OK;
+}
+
+int fa2_abi_version(void) { return 100; }
+
+}  // extern "C"

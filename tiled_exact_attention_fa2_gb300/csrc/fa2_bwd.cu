@@ -1,0 +1,536 @@
+// FlashAttention-2 backward on sm_103a.
+//
+// Method: "Revolutionizing Web-Based AI: How a Plain JavaScript Prototype
+// Paved the Way for High-Performance WebGPU Flash Attention 2", section
+// "Translating to WGSL and Optimizing Passes" (backward-pass bullet): the
+// attention weights are recomputed tile by tile from the saved Q, K and the
+// per-row log-sum-exp instead of being read back from a stored matrix.  The
+// same article's section "Numerical Stability and Loss Drift" names atomic
+// reductions as a rounding source; dQ here is such a reduction (fp32 atomics
+// into a zeroed accumulator), the only step whose summation order varies
+// between runs.
+//
+// Three kernels, enqueued in this order on the caller's stream:
+//   1. preprocess: D = rowsum(dO * O) (fp32) and zero the fp32 dQ accumulator
+//      (HBM-bound, 16-byte coalesced loads).
+//   2. main: one CTA per (128-row key/value tile, head); loops over the query
+//      tiles that can see it (all of them, or those at or after the diagonal
+//      when causal):
+//         S^T  = K Q_i^T                   (TMEM)
+//         P^T  = exp(scale S^T - LSE_i)    (registers -> bf16 smem)
+//         dP^T = V dO_i^T                  (TMEM)
+//         dV  += P^T dO_i                  (TMEM accumulator)
+//         dS^T = P^T * (dP^T - D_i)        (registers -> bf16 smem)
+//         dK  += dS^T Q_i                  (TMEM accumulator)
+//         dQ_i = dS K                      (TMEM) -> fp32 atomics into dQacc
+//      then writes dK * scale and dV as bf16.
+//   3. convert: dQ = bf16(scale * dQacc).
+//
+// Warp roles of the main kernel (192 threads): warps 0-3 compute (thread t
+// owns key row t of the tile for P/dS and query row t for the dQ drain),
+// warp 4 TMA producer, warp 5 MMA issuer and TMEM owner.
+// TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK after dV;
+// dQ gets its own D columns after dK when they fit (D <= 64) and otherwise
+// reuses the S^T columns, which are free once P^T has been read out.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "tiles.cuh"
+
+namespace fa2 {
+
+__device__ int g_bwd_status;
+
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.44269504088896341f;
+
+enum BwdBar {
+  kBarKV = 0,
+  kBarQFull = 1,     // +stage (2)
+  kBarQEmpty = 3,    // +stage
+  kBarDoFull = 5,    // +stage
+  kBarDoEmpty = 7,   // +stage
+  kBarSFull = 9,
+  kBarDpFull = 10,
+  kBarPFull = 11,
+  kBarDsFull = 12,
+  kBarDqFull = 13,
+  kBarDqDrained = 14,
+  kBarPsEmpty = 15,
+  kBarAccFull = 16,
+  kBarDrain = 17,
+  kBarRowStats = 18,  // +buffer (2): LSE_i / D_i staged in shared memory
+  kNumBwdBars = 20,
+};
+
+template <int D>
+struct BwdCfg {
+  using T = HeadDim<D>;
+  static constexpr int kStages = D == 128 ? 1 : 2;  // Q / dO ring depth
+  // TMEM regions start on 32-column boundaries.
+  static constexpr int kCols = D < 32 ? 32 : D;
+  static constexpr bool kDqAliasesS = 256 + 3 * kCols > 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + kCols;
+  static constexpr uint32_t kColDQ = kDqAliasesS ? 0 : 256 + 2 * kCols;
+  // shared memory
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + T::kTileBytes;
+  static constexpr int kQ = kV + T::kTileBytes;
+  static constexpr int kDo = kQ + kStages * T::kTileBytes;
+  static constexpr int kPt = kDo + kStages * T::kTileBytes;
+  static constexpr int kDSt = kPt + Square::kTileBytes;
+  static constexpr int kLse = kDSt + Square::kTileBytes;  // [2][128] fp32, pre-multiplied by log2 e
+  static constexpr int kDv = kLse + 2 * 128 * 4;          // [2][128] fp32
+  static constexpr int kBars = kDv + 2 * 128 * 4;
+  static constexpr int kTmemSlot = kBars + kNumBwdBars * 8;
+  static constexpr int kUsed = kTmemSlot + 16;
+  static constexpr int kBytes = (kUsed + 1024) > 116 * 1024 ? (kUsed + 1024) : 116 * 1024;
+  static_assert(kUsed + 1024 <= 232448, "backward tile does not fit in shared memory");
+};
+
+// ---------------------------------------------------------------- preprocess
+// D[row] = sum_c dO[row, c] * O[row, c]; also zero the dQ accumulator.
+template <int D>
+__global__ void __launch_bounds__(256) fa2_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                                 const __nv_bfloat16* __restrict__ dO,
+                                                                 float* __restrict__ Dvec,
+                                                                 float* __restrict__ dq_acc, long long rows) {
+  constexpr int kTpr = D / 8;  // threads per row, 16 bytes each
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / kTpr;
+  const int sub = threadIdx.x % kTpr;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + row * D) + sub);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(pa[e]);
+      const float2 fb = __bfloat1622float2(pb[e]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) Dvec[row] = acc;
+
+  // Zero dQacc (rows * D fp32) with 16-byte stores, grid-stride.
+  const long long n4 = rows * D / 4;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+    acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ---------------------------------------------------------------- dQ convert
+__global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __restrict__ dq_acc,
+                                                             __nv_bfloat16* __restrict__ dq, long long n8,
+                                                             float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(dq_acc) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(dq_acc) + 2 * i + 1);
+    reinterpret_cast<uint4*>(dq)[i] =
+        make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                   pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+  }
+}
+
+// ---------------------------------------------------------------- main
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const float* __restrict__ lse, const float* __restrict__ Dvec, float* __restrict__ dq_acc,
+                   __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, float scale,
+                   float scale_log2) {
+  using T = HeadDim<D>;
+  using C = BwdCfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
+  float* sLse = reinterpret_cast<float*>(smem + C::kLse);
+  float* sDv = reinterpret_cast<float*>(smem + C::kDv);
+  const uint32_t sK = smem_u32(smem + C::kK);
+  const uint32_t sV = smem_u32(smem + C::kV);
+  const uint32_t sQ = smem_u32(smem + C::kQ);
+  const uint32_t sDo = smem_u32(smem + C::kDo);
+  const uint32_t sPt = smem_u32(smem + C::kPt);
+  const uint32_t sDSt = smem_u32(smem + C::kDSt);
+  int* status = &g_bwd_status;
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int num_tiles = (N + kTileRows - 1) / kTileRows;
+  const int bh = blockIdx.x % BH;
+  const int jt = blockIdx.x / BH;  // key/value tile; causal work shrinks with jt, so heavy tiles go first
+  const int kv0 = jt * kTileRows;
+  const int i_begin = CAUSAL ? jt : 0;
+  const int n_q = num_tiles - i_begin;
+
+  if (threadIdx.x == kBwdThreads - 64) {
+    mbar_init(&bars[kBarKV], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kBarQFull + s], 1);
+      mbar_init(&bars[kBarQEmpty + s], 1);
+      mbar_init(&bars[kBarDoFull + s], 1);
+      mbar_init(&bars[kBarDoEmpty + s], 1);
+    }
+    mbar_init(&bars[kBarSFull], 1);
+    mbar_init(&bars[kBarDpFull], 1);
+    mbar_init(&bars[kBarPFull], 4);
+    mbar_init(&bars[kBarDsFull], 4);
+    mbar_init(&bars[kBarDqFull], 1);
+    mbar_init(&bars[kBarDqDrained], 4);
+    mbar_init(&bars[kBarPsEmpty], 1);
+    mbar_init(&bars[kBarAccFull], 1);
+    mbar_init(&bars[kBarDrain], 1);
+    mbar_init(&bars[kBarRowStats], 128);
+    mbar_init(&bars[kBarRowStats + 1], 128);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      int last_q[2] = {-1, -1}, last_do[2] = {-1, -1};
+      mbar_arrive_expect_tx(&bars[kBarKV], 2 * T::kTileBytes);
+      for (int b = 0; b < T::kNumBoxes; ++b) {
+        tma_load_3d(smem + C::kK + b * T::kBoxBytes, &tm_k, &bars[kBarKV], b * T::kBoxCols, kv0, bh);
+        tma_load_3d(smem + C::kV + b * T::kBoxBytes, &tm_v, &bars[kBarKV], b * T::kBoxCols, kv0, bh);
+      }
+#pragma unroll 1
+      for (int it = 0; it < n_q; ++it) {
+        const int st = it % S, u = it / S;
+        const int q0 = (i_begin + it) * kTileRows;
+        if (it >= S && !mbar_wait(&bars[kBarDoEmpty + st], (u - 1) & 1, status)) break;
+        mbar_arrive_expect_tx(&bars[kBarDoFull + st], T::kTileBytes);
+        for (int b = 0; b < T::kNumBoxes; ++b)
+          tma_load_3d(smem + C::kDo + st * T::kTileBytes + b * T::kBoxBytes, &tm_do, &bars[kBarDoFull + st],
+                      b * T::kBoxCols, q0, bh);
+        last_do[st] = it;
+        if (it >= S && !mbar_wait(&bars[kBarQEmpty + st], (u - 1) & 1, status)) break;
+        mbar_arrive_expect_tx(&bars[kBarQFull + st], T::kTileBytes);
+        for (int b = 0; b < T::kNumBoxes; ++b)
+          tma_load_3d(smem + C::kQ + st * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQFull + st],
+                      b * T::kBoxCols, q0, bh);
+        last_q[st] = it;
+      }
+      mbar_wait(&bars[kBarKV], 0, status);
+      for (int s = 0; s < S; ++s) {
+        if (last_q[s] >= 0) mbar_wait(&bars[kBarQFull + s], (last_q[s] / S) & 1, status);
+        if (last_do[s] >= 0) mbar_wait(&bars[kBarDoFull + s], (last_do[s] / S) & 1, status);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdSq = make_idesc_bf16(128, 128, false, false);  // K x Q^T, V x dO^T
+      constexpr uint32_t kIdKV = make_idesc_bf16(128, D, false, true);     // P^T x dO, dS^T x Q
+      constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, true, true);      // dS x K
+      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDV = tmem + C::kColDV,
+                     tDK = tmem + C::kColDK, tDQ = tmem + C::kColDQ;
+      bool ok = mbar_wait(&bars[kBarKV], 0, status);
+#pragma unroll 1
+      for (int it = 0; ok && it < n_q; ++it) {
+        const int st = it % S, u = it / S;
+        const uint32_t q_s = sQ + st * T::kTileBytes, do_s = sDo + st * T::kTileBytes;
+        if (!(ok = mbar_wait(&bars[kBarQFull + st], u & 1, status))) break;
+        if (C::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bars[kBarDqDrained], (it - 1) & 1, status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tS, T::kmajor_desc(sK, kk), T::kmajor_desc(q_s, kk), kIdSq, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kBarSFull]);
+        if (!(ok = mbar_wait(&bars[kBarDoFull + st], u & 1, status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tDP, T::kmajor_desc(sV, kk), T::kmajor_desc(do_s, kk), kIdSq, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kBarDpFull]);
+        if (!(ok = mbar_wait(&bars[kBarPFull], it & 1, status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_bf16_ss(tDV, Square::kmajor_desc(sPt, kk), T::mnmajor_desc(do_s, kk), kIdKV,
+                      (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarDoEmpty + st]);
+        if (!(ok = mbar_wait(&bars[kBarDsFull], it & 1, status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_bf16_ss(tDK, Square::kmajor_desc(sDSt, kk), T::mnmajor_desc(q_s, kk), kIdKV,
+                      (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarQEmpty + st]);
+        if (!C::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bars[kBarDqDrained], (it - 1) & 1, status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_bf16_ss(tDQ, Square::mnmajor_desc(sDSt, kk), T::mnmajor_desc(sK, kk), kIdDQ, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kBarDqFull]);
+        mma_commit(&bars[kBarPsEmpty]);
+      }
+      if (ok) mma_commit(&bars[kBarAccFull]);
+      mma_commit(&bars[kBarDrain]);
+      mbar_wait(&bars[kBarDrain], 0, status);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int t = threadIdx.x;  // TMEM lane; key row kv0 + t; query row q0 + t in the dQ drain
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int kv_row = kv0 + t;
+    bool ok = true;
+#pragma unroll 1
+    for (int it = 0; it < n_q; ++it) {
+      const int i = i_begin + it;
+      const int q0 = i * kTileRows;
+      const int b = it & 1;
+      {
+        const int q = q0 + t;
+        const bool in = q < N;
+        sLse[b * 128 + t] = in ? lse[static_cast<size_t>(bh) * N + q] * kLog2e : INFINITY;
+        sDv[b * 128 + t] = in ? Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
+      }
+      // Every compute thread has staged its entry; a buffer is rewritten two
+      // iterations later, after all four warps have passed the dS hand-off.
+      mbar_arrive(&bars[kBarRowStats + b]);
+      if (!(ok = mbar_wait(&bars[kBarRowStats + b], (it >> 1) & 1, status))) break;
+      const float* lse2 = sLse + b * 128;
+      const float* dvec = sDv + b * 128;
+
+      // P^T = 2^(scale log2e S^T - log2e LSE), masked.
+      if (!(ok = mbar_wait(&bars[kBarSFull], it & 1, status))) break;
+      tc_fence_after();
+      float p[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + C::kColS + c * 32, p[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) p[c][e] = ex2_approx(fmaf(p[c][e], scale_log2, -lse2[c * 32 + e]));
+      if (kv_row >= N) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) p[c][e] = 0.f;
+      } else if (CAUSAL && i == jt) {
+        // key kv_row is visible to query q0 + col iff kv_row <= q0 + col
+        const int first = kv_row - q0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < first) p[c][e] = 0.f;
+      }
+      if (it >= 1 && !(ok = mbar_wait(&bars[kBarPsEmpty], (it - 1) & 1, status))) break;
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
+        const float* v = &p[c16 >> 2][(c16 & 3) * 8];
+        store_square_chunk(sPt, t, c16, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarPFull]);
+
+      // dS^T = P^T * (dP^T - D)
+      if (!(ok = mbar_wait(&bars[kBarDpFull], it & 1, status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float dp[32];
+        tmem_ld32(tmem + lane_base + C::kColDP + c * 32, dp);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          float ds[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) ds[x] = p[c][e + x] * (dp[e + x] - dvec[c * 32 + e + x]);
+          store_square_chunk(sDSt, t, c * 4 + e / 8, pack_bf16x2(ds[0], ds[1]), pack_bf16x2(ds[2], ds[3]),
+                             pack_bf16x2(ds[4], ds[5]), pack_bf16x2(ds[6], ds[7]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDsFull]);
+
+      // dQ_i partial (query row q0 + t) -> fp32 atomics.
+      if (!(ok = mbar_wait(&bars[kBarDqFull], it & 1, status))) break;
+      tc_fence_after();
+      {
+        const int q = q0 + t;
+        float* dst = dq_acc + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
+        if constexpr (D >= 32) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float g[32];
+            tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
+            tmem_wait_ld();
+            if (q < N) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
+            }
+          }
+        } else {
+          float g[16];
+          tmem_ld16(tmem + lane_base + C::kColDQ, g);
+          tmem_wait_ld();
+          if (q < N) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              atomicAdd(reinterpret_cast<float4*>(dst + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && mbar_wait(&bars[kBarAccFull], 0, status)) {
+      tc_fence_after();
+      const bool valid = kv_row < N;
+      const size_t off = (static_cast<size_t>(bh) * N + (valid ? kv_row : 0)) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+        const float mul = which == 0 ? 1.f : scale;
+        uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + off);
+        if constexpr (D >= 32) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float g[32];
+            tmem_ld32(tmem + lane_base + col + c * 32, g);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[c * 4 + q] = make_uint4(pack_bf16x2(g[8 * q + 0] * mul, g[8 * q + 1] * mul),
+                                            pack_bf16x2(g[8 * q + 2] * mul, g[8 * q + 3] * mul),
+                                            pack_bf16x2(g[8 * q + 4] * mul, g[8 * q + 5] * mul),
+                                            pack_bf16x2(g[8 * q + 6] * mul, g[8 * q + 7] * mul));
+            }
+          }
+        } else {
+          float g[16];
+          tmem_ld16(tmem + lane_base + col, g);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              dst[q] = make_uint4(pack_bf16x2(g[8 * q + 0] * mul, g[8 * q + 1] * mul),
+                                  pack_bf16x2(g[8 * q + 2] * mul, g[8 * q + 3] * mul),
+                                  pack_bf16x2(g[8 * q + 4] * mul, g[8 * q + 5] * mul),
+                                  pack_bf16x2(g[8 * q + 6] * mul, g[8 * q + 7] * mul));
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+int launch_preprocess_t(const void* o, const void* dO, float* Dvec, float* dq_acc, long long rows,
+                        cudaStream_t stream) {
+  constexpr int kTpr = D / 8;
+  const long long threads = rows * kTpr;
+  const long long blocks = (threads + 255) / 256;
+  fa2_bwd_preprocess_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, rows);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <int D, bool CAUSAL>
+int launch_bwd_main_t(const TmapSet& tm, const float* lse, const float* Dvec, float* dq_acc, void* dk, void* dv,
+                      int BH, int N, float scale, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  auto kern = fa2_bwd_kernel<D, CAUSAL>;
+  if (ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes) != 0) return -1;
+  const int num_tiles = (N + kTileRows - 1) / kTileRows;
+  const dim3 grid(static_cast<unsigned>(num_tiles) * static_cast<unsigned>(BH));
+  kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, lse, Dvec, dq_acc,
+                                                  static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+                                                  BH, N, scale, scale * kLog2e);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_dq_convert(const float* dq_acc, void* dq, long long elems, float scale, cudaStream_t stream) {
+  const long long n8 = elems / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  fa2_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_bwd(const TmapSet& tm, const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv,
+               float* Dvec, float* dq_acc, int BH, int N, int d, float scale, bool causal, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(BH) * N;
+  int rc = -1;
+  switch (d) {
+    case 16: rc = launch_preprocess_t<16>(o, dO, Dvec, dq_acc, rows, stream); break;
+    case 32: rc = launch_preprocess_t<32>(o, dO, Dvec, dq_acc, rows, stream); break;
+    case 64: rc = launch_preprocess_t<64>(o, dO, Dvec, dq_acc, rows, stream); break;
+    case 128: rc = launch_preprocess_t<128>(o, dO, Dvec, dq_acc, rows, stream); break;
+    default: return -1;
+  }
+  if (rc != 0) return rc;
+  switch (d) {
+    case 16: rc = causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                         : launch_bwd_main_t<16, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
+    case 32: rc = causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                         : launch_bwd_main_t<32, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
+    case 64: rc = causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                         : launch_bwd_main_t<64, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
+    case 128: rc = causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                          : launch_bwd_main_t<128, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
+  }
+  if (rc != 0) return rc;
+  return launch_dq_convert(dq_acc, dq, rows * d, scale, stream);
+}
+
+int read_bwd_status(int* value, bool reset) {
+  if (cudaMemcpyFromSymbol(value, g_bwd_status, sizeof(int)) != cudaSuccess) return -1;
+  if (reset) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return 0;
+}
+
+}  // namespace fa2

@@ -1,0 +1,25 @@
+// Internal interface between the C-ABI entry points (api.cu) and the kernel
+// translation units.  Not part of the public header.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa2 {
+
+// TMA descriptors of the [B*H, N, d] bf16 views of the operands.
+struct TmapSet {
+  CUtensorMap q, k, v, dO;
+};
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+int ensure_max_smem(const void* kernel, int bytes);
+
+int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, float scale, bool causal,
+               cudaStream_t stream);
+int launch_bwd(const TmapSet& tm, const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv,
+               float* Dvec, float* dq_acc, int BH, int N, int d, float scale, bool causal, cudaStream_t stream);
+
+int read_fwd_status(int* value, bool reset);
+int read_bwd_status(int* value, bool reset);
+
+}  // namespace fa2
