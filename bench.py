@@ -1,0 +1,357 @@
+#!/usr/bin/env python
+"""Throughput of the FA2 hot path (forward + backward) on GB300.
+
+One step = fa2_fwd followed by the three backward stages (D preprocess, main
+recompute kernel, dQ convert) on one batch of synthetic inputs already
+resident in HBM.  Default workload: the long-sequence configuration
+B=1, H=32, N=16384, d=128, causal (Q, K, V, dO are 134 MB each, so the
+inputs of a step exceed the 129 MB L2 and no flush is needed).
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are weak-scaled:
+every rank runs its own batch of the same shape; no data-path collective.
+``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+_CORES = len(os.sched_getaffinity(0))
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "causal bf16 FA2 fwd / bwd TFLOPS and % of GB300 dense bf16 peak (1 GPU)"
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture of the same kernel build on this workload; None when no capture of
+# the current kernel exists.  The profile summary under profiles/ names the
+# command that produced the figure.
+DOMINANT_KERNEL_TRAFFIC = {}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained": p["bf16_tflops_sustained"],
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle legs
+def _oracle_sample(w, causal: bool, n_prefix: int):
+    """fp64 oracle forward + backward on the first n_prefix rows of head (0, 0).
+
+    Returns (flops counted as FA2 work, seconds)."""
+    import oracle
+    x = workloads.make_inputs(1, 1, n_prefix, w.d, seed=w.seed, qk_mult=w.qk_mult)
+    t0 = time.perf_counter()
+    oracle.attn_bwd(x["q"], x["k"], x["v"], x["dO"], w.scale, causal)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * n_prefix * n_prefix * w.d * (0.5 if causal else 1.0)
+    return flops, dt
+
+
+def _choose_prefix(w, causal, budget_s: float) -> int:
+    """Largest head prefix (multiple of 1024, <= N) whose oracle run fits budget_s."""
+    base = min(2048, w.N)
+    _, t = _oracle_sample(w, causal, base)
+    n = base
+    while n * 2 <= w.N and t * ((n * 2) / base) ** 2 <= budget_s:
+        n *= 2
+    for cand in range(n, min(w.N, 2 * n) + 1, 1024):
+        if t * (cand / base) ** 2 <= budget_s:
+            n = cand
+    return min(n, w.N)
+
+
+def cpu_baseline(w, causal):
+    n = _choose_prefix(w, causal, budget_s=20.0)
+    flops, dt = _oracle_sample(w, causal, n)
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": _CORES, "kind": "oracle",
+            "sample": f"fp64 numpy oracle fwd+bwd on one head (b=0,h=0) of the {w.name} workload, "
+                      f"first {n} of {w.N} rows{' (causal prefix)' if causal else ''}; {dt:.1f} s; "
+                      f"BLAS threads {_CORES}"}
+
+
+def run_reference(args, w, causal):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = _choose_prefix(w, causal, budget)
+    for _ in range(args.warmup):
+        _oracle_sample(w, causal, n)
+    tot_flops, tot_t = 0.0, 0.0
+    for _ in range(args.steps):
+        f, t = _oracle_sample(w, causal, n)
+        tot_flops += f
+        tot_t += t
+    value = tot_flops / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} "
+                               f"{'causal' if causal else 'non-causal'} (oracle on a head prefix per step)",
+                   "sample_rows": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": _CORES, "kind": "oracle",
+                         "sample": f"per step: fp64 oracle fwd+bwd on the first {n} rows of head (0,0)"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args, w, causal):
+    world, rank, local = _dist()
+    import tiled_exact_attention_fa2_gb300 as fa2
+    from tiled_exact_attention_fa2_gb300 import _build
+    _build.build()
+    fa2.load_library()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    x = workloads.make_inputs(B, H, N, d, seed=w.seed + rank, qk_mult=w.qk_mult)
+    g = {k: t.to(dev) for k, t in x.items()}
+    o = torch.empty_like(g["q"])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+    Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq_acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    scale = w.scale
+    fwd_flops, bwd_flops = w.fwd_flops(causal), w.bwd_flops(causal)
+
+    n_ev = args.steps + args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_ev)]
+
+    def step(i):
+        e = ev[i]
+        e[0].record(stream)
+        fa2.fa2_fwd(g["q"], g["k"], g["v"], o, lse, scale, causal, stream)
+        fa2.fa2_bwd_stages(g["q"], g["k"], g["v"], o, g["dO"], lse, Dvec, dq_acc, dq, dk, dv, scale, causal,
+                           stream, hook=lambda j: e[j + 1].record(stream))
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert fa2.fa2_device_status(reset=True) == 0
+    sampler = ClockSampler(local)
+    _barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.warmup, n_ev):
+        step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    clocks = sampler.stop()
+    status = fa2.fa2_device_status(reset=True)
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = _max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    timed = ev[args.warmup:]
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in timed)
+    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in timed)
+    main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in timed)
+    conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in timed)
+    bwd_ms = pre_ms + main_ms + conv_ms
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: x[k].pin_memory() for k in ("q", "k", "v", "dO")}
+        host.update({k: torch.empty_like(host["q"]).pin_memory() for k in ("o", "dq", "dk", "dv")})
+        host["lse"] = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        devb = dict(g, o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+        for _ in range(max(1, args.warmup)):
+            fa2.attention_step_from_host(host, devb, causal, scale, stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fa2.attention_step_from_host(host, devb, causal, scale, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = _max_over_ranks(a.elapsed_time(b), world) / args.steps
+        h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "dO"))
+        d2h = sum(host[k].numel() * host[k].element_size() for k in ("o", "lse", "dq", "dk", "dv"))
+        e2e = {"value": world * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    peaks = _peaks()
+    value = world * (fwd_flops + bwd_flops) / (ms_step * 1e-3) / 1e12
+    fwd_tf = fwd_flops / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    main_tf = bwd_flops / (main_ms * 1e-3) / 1e12
+    dominant = "fa2_bwd_kernel" if main_ms >= fwd_ms else "fa2_fwd_kernel"
+    dom_ms, dom_tf = (main_ms, main_tf) if dominant == "fa2_bwd_kernel" else (fwd_ms, fwd_tf)
+    pre_bytes = 2 * B * H * N * d * 2 + B * H * N * 4 + B * H * N * d * 4  # O, dO read; D written; dQacc zeroed
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'}",
+                   "B": B, "H": H, "N": N, "d": d, "causal": causal, "parallelism": f"weak x{world} (heads)",
+                   "l2": "inputs larger than L2 (Q, K, V, dO 134 MB each), no flush"},
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "pct_of_peak_burst": 100 * fwd_tf / peaks["bf16_tflops"],
+                "pct_of_peak_sustained": 100 * fwd_tf / peaks["bf16_tflops_sustained"]},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "pct_of_peak_burst": 100 * bwd_tf / peaks["bf16_tflops"],
+                "pct_of_peak_sustained": 100 * bwd_tf / peaks["bf16_tflops_sustained"],
+                "preprocess_ms": pre_ms, "main_ms": main_ms, "dq_convert_ms": conv_ms,
+                "preprocess_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9},
+        "roofline": {"kernel": dominant, "bound": "tensor", "achieved": dom_tf,
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": dom_tf / peaks["bf16_tflops_sustained"],
+                     "traffic": DOMINANT_KERNEL_TRAFFIC.get((dominant, w.name, causal)),
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
+                     "frac_of_burst": dom_tf / peaks["bf16_tflops"]},
+        "gpu_launches": 4 * args.steps,
+        "device_status": status,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, causal)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--noncausal", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    w = workloads.WORKLOADS[args.workload]
+    causal = not args.noncausal
+    if args.impl == "reference":
+        return run_reference(args, w, causal)
+    return run_gpu(args, w, causal)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -89,6 +89,30 @@ int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const
                void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The three stages fa2_bwd / fa2_bwd_ws enqueue, exposed separately so that a
+ * caller can time, reorder or overlap them.  Running the three in this order
+ * on one stream is exactly fa2_bwd_ws.
+ *
+ * fa2_bwd_preprocess: Dvec[r] = sum_c dO[r,c] * o[r,c] (fp32 [B,H,N]) and
+ *   dq_acc (fp32 [B,H,N,d], 16-byte aligned) set to zero.  The D identity is
+ *   the standard FA2 backward identity (the pages do not state it).
+ * fa2_bwd_main: recomputes P from q, k and lse tile by tile (the article's
+ *   backward-pass bullet), writes dk and dv (bf16) and ADDS the unscaled
+ *   dS K into dq_acc with fp32 atomics (the order of that sum varies from run
+ *   to run; the article's "Numerical Stability and Loss Drift" section notes
+ *   atomic reductions as a rounding source).
+ * fa2_bwd_dq_convert: dq = bf16(scale * dq_acc).
+ * Same pointer, alignment and error rules as above; Dvec and dq_acc are
+ * device pointers owned by the caller.
+ */
+int fa2_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H, int N, int d,
+                       void* stream);
+int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
+                 float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                 void* stream);
+int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* fa2_status_string(int status);
 

@@ -22,6 +22,7 @@ from . import _build
 __all__ = [
     "FA2Error", "load_library", "fa2_fwd", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
     "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
+    "fa2_bwd_stages",
     "FA2_OK",
 ]
 
@@ -41,6 +42,9 @@ _SIGNATURES = {
     "fa2_status_string": (ctypes.c_char_p, [_i]),
     "fa2_device_status": (_i, [ctypes.POINTER(_i), _i]),
     "fa2_abi_version": (_i, []),
+    "fa2_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "fa2_bwd_main": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
 }
 
 
@@ -175,6 +179,33 @@ def fa2_bwd_ws(q, k, v, o, dO, lse, workspace: torch.Tensor, dq=None, dk=None, d
                         _stream(stream, q.device))
     if rc != FA2_OK:
         raise FA2Error("fa2_bwd_ws", rc)
+    return dq, dk, dv
+
+
+def fa2_bwd_stages(q, k, v, o, dO, lse, Dvec, dq_acc, dq, dk, dv, scale: Optional[float] = None,
+                   causal: bool = True, stream=None, hook=None):
+    """fa2_bwd_ws as its three C-ABI stages; ``hook(i)`` is called before stage i
+    (0: preprocess, 1: main, 2: dQ convert) and with i = 3 after the last, so a
+    caller can record CUDA events between them."""
+    lib = load_library()
+    (B, H, N, d), dq, dk, dv = _bwd_common(q, k, v, o, dO, lse, dq, dk, dv)
+    sc, st = _scale(scale, d), _stream(stream, q.device)
+    hook = hook or (lambda i: None)
+    hook(0)
+    rc = lib.fa2_bwd_preprocess(o.data_ptr(), dO.data_ptr(), Dvec.data_ptr(), dq_acc.data_ptr(), B, H, N, d, st)
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_preprocess", rc)
+    hook(1)
+    rc = lib.fa2_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                          Dvec.data_ptr(), dq_acc.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, sc,
+                          1 if causal else 0, st)
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_main", rc)
+    hook(2)
+    rc = lib.fa2_bwd_dq_convert(dq_acc.data_ptr(), dq.data_ptr(), B, H, N, d, sc, st)
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_dq_convert", rc)
+    hook(3)
     return dq, dk, dv
 
 

@@ -110,19 +110,25 @@ int validate_bwd(const void* q, const void* k, const void* v, const void* o, con
   return FA2_OK;
 }
 
+int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const void* dO, int BH, int N, int d) {
+  return (make_tmap(&tm->q, q, BH, N, d) && make_tmap(&tm->k, k, BH, N, d) && make_tmap(&tm->v, v, BH, N, d) &&
+          make_tmap(&tm->dO, dO, BH, N, d))
+             ? FA2_OK
+             : FA2_ERR_CUDA;
+}
+
 int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
             void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* ws, cudaStream_t st) {
   const int BH = B * H;
   TmapSet tm;
-  if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, BH, N, d) || !make_tmap(&tm.v, v, BH, N, d) ||
-      !make_tmap(&tm.dO, dO, BH, N, d))
-    return FA2_ERR_CUDA;
+  if (int rc = make_tmaps(&tm, q, k, v, dO, BH, N, d)) return rc;
   const size_t rows = static_cast<size_t>(BH) * N;
   float* Dvec = static_cast<float*>(ws);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(rows * sizeof(float)));
-  return launch_bwd(tm, o, dO, lse, dq, dk, dv, Dvec, dq_acc, BH, N, d, scale, causal != 0, st) == 0
-             ? FA2_OK
-             : FA2_ERR_CUDA;
+  if (launch_bwd_preprocess(o, dO, Dvec, dq_acc, BH, N, d, st) != 0) return FA2_ERR_CUDA;
+  if (launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, BH, N, d, scale, causal != 0, st) != 0) return FA2_ERR_CUDA;
+  if (launch_bwd_dq_convert(dq_acc, dq, BH, N, d, scale, st) != 0) return FA2_ERR_CUDA;
+  return FA2_OK;
 }
 
 }  // namespace
@@ -197,6 +203,64 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const vo
   const int rc = run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, st);
   if (cudaFreeAsync(ws, st) != cudaSuccess) return FA2_ERR_CUDA;
   return rc;
+}
+
+int fa2_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H, int N, int d,
+                       void* stream) {
+  if (!o || !dO || !Dvec || !dq_acc) return FA2_ERR_NULL;
+  if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (!aligned(o, 16) || !aligned(dO, 16) || !aligned(Dvec, 4) || !aligned(dq_acc, 16)) return FA2_ERR_ALIGN;
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const Range rd = range_of(Dvec, static_cast<size_t>(B) * H * N * 4);
+  const Range ra = range_of(dq_acc, static_cast<size_t>(B) * H * N * d * 4);
+  const Range ins[] = {range_of(o, tb), range_of(dO, tb)};
+  for (const Range& r : ins)
+    if (overlap(rd, r) || overlap(ra, r)) return FA2_ERR_ALIAS;
+  if (overlap(rd, ra)) return FA2_ERR_ALIAS;
+  return launch_bwd_preprocess(o, dO, Dvec, dq_acc, B * H, N, d, static_cast<cudaStream_t>(stream)) == 0
+             ? FA2_OK
+             : FA2_ERR_CUDA;
+}
+
+int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
+                 float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                 void* stream) {
+  if (!q || !k || !v || !dO || !lse || !Dvec || !dq_acc || !dk || !dv) return FA2_ERR_NULL;
+  if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (int rc = check_scale(scale)) return rc;
+  const void* bf[] = {q, k, v, dO, dk, dv};
+  for (const void* p : bf)
+    if (!aligned(p, 16)) return FA2_ERR_ALIGN;
+  if (!aligned(lse, 4) || !aligned(Dvec, 4) || !aligned(dq_acc, 16)) return FA2_ERR_ALIGN;
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  const Range outs[] = {range_of(dk, tb), range_of(dv, tb), range_of(dq_acc, tb * 2)};
+  const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(dO, tb), range_of(lse, lb),
+                       range_of(Dvec, lb)};
+  for (int a = 0; a < 3; ++a) {
+    for (const Range& r : ins)
+      if (overlap(outs[a], r)) return FA2_ERR_ALIAS;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlap(outs[a], outs[b])) return FA2_ERR_ALIAS;
+  }
+  TmapSet tm;
+  if (int rc = make_tmaps(&tm, q, k, v, dO, B * H, N, d)) return rc;
+  return launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, B * H, N, d, scale, causal != 0,
+                         static_cast<cudaStream_t>(stream)) == 0
+             ? FA2_OK
+             : FA2_ERR_CUDA;
+}
+
+int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale, void* stream) {
+  if (!dq_acc || !dq) return FA2_ERR_NULL;
+  if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (int rc = check_scale(scale)) return rc;
+  if (!aligned(dq_acc, 16) || !aligned(dq, 16)) return FA2_ERR_ALIGN;
+  const size_t n = static_cast<size_t>(B) * H * N * d;
+  if (overlap(range_of(dq_acc, n * 4), range_of(dq, n * 2))) return FA2_ERR_ALIAS;
+  return launch_bwd_dq_convert(dq_acc, dq, B * H, N, d, scale, static_cast<cudaStream_t>(stream)) == 0
+             ? FA2_OK
+             : FA2_ERR_CUDA;
 }
 
 const char* fa2_status_string(int status) {

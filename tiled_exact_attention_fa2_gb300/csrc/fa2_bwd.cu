@@ -498,30 +498,35 @@ int launch_dq_convert(const float* dq_acc, void* dq, long long elems, float scal
 
 }  // namespace
 
-int launch_bwd(const TmapSet& tm, const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv,
-               float* Dvec, float* dq_acc, int BH, int N, int d, float scale, bool causal, cudaStream_t stream) {
+int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int BH, int N, int d,
+                          cudaStream_t stream) {
   const long long rows = static_cast<long long>(BH) * N;
-  int rc = -1;
   switch (d) {
-    case 16: rc = launch_preprocess_t<16>(o, dO, Dvec, dq_acc, rows, stream); break;
-    case 32: rc = launch_preprocess_t<32>(o, dO, Dvec, dq_acc, rows, stream); break;
-    case 64: rc = launch_preprocess_t<64>(o, dO, Dvec, dq_acc, rows, stream); break;
-    case 128: rc = launch_preprocess_t<128>(o, dO, Dvec, dq_acc, rows, stream); break;
+    case 16: return launch_preprocess_t<16>(o, dO, Dvec, dq_acc, rows, stream);
+    case 32: return launch_preprocess_t<32>(o, dO, Dvec, dq_acc, rows, stream);
+    case 64: return launch_preprocess_t<64>(o, dO, Dvec, dq_acc, rows, stream);
+    case 128: return launch_preprocess_t<128>(o, dO, Dvec, dq_acc, rows, stream);
     default: return -1;
   }
-  if (rc != 0) return rc;
+}
+
+int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, float* dq_acc, void* dk, void* dv, int BH,
+                    int N, int d, float scale, bool causal, cudaStream_t stream) {
   switch (d) {
-    case 16: rc = causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                         : launch_bwd_main_t<16, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
-    case 32: rc = causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                         : launch_bwd_main_t<32, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
-    case 64: rc = causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                         : launch_bwd_main_t<64, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
-    case 128: rc = causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                          : launch_bwd_main_t<128, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream); break;
+    case 16: return causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                           : launch_bwd_main_t<16, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
+    case 32: return causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                           : launch_bwd_main_t<32, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
+    case 64: return causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                           : launch_bwd_main_t<64, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
+    case 128: return causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
+                            : launch_bwd_main_t<128, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
+    default: return -1;
   }
-  if (rc != 0) return rc;
-  return launch_dq_convert(dq_acc, dq, rows * d, scale, stream);
+}
+
+int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, float scale, cudaStream_t stream) {
+  return launch_dq_convert(dq_acc, dq, static_cast<long long>(BH) * N * d, scale, stream);
 }
 
 int read_bwd_status(int* value, bool reset) {

@@ -16,8 +16,11 @@ int ensure_max_smem(const void* kernel, int bytes);
 
 int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, float scale, bool causal,
                cudaStream_t stream);
-int launch_bwd(const TmapSet& tm, const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv,
-               float* Dvec, float* dq_acc, int BH, int N, int d, float scale, bool causal, cudaStream_t stream);
+int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int BH, int N, int d,
+                          cudaStream_t stream);
+int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, float* dq_acc, void* dk, void* dv, int BH,
+                    int N, int d, float scale, bool causal, cudaStream_t stream);
+int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, float scale, cudaStream_t stream);
 
 int read_fwd_status(int* value, bool reset);
 int read_bwd_status(int* value, bool reset);
