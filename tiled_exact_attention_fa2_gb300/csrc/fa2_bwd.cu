@@ -45,7 +45,7 @@ __device__ int g_bwd_status;
 
 namespace {
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.44269504088896341f;
 
@@ -55,42 +55,47 @@ enum BwdBar {
   kBarQEmpty = 3,    // +stage
   kBarDoFull = 5,    // +stage
   kBarDoEmpty = 7,   // +stage
-  kBarSFull = 9,
-  kBarDpFull = 10,
-  kBarPFull = 11,
-  kBarDsFull = 12,
-  kBarDqFull = 13,
-  kBarDqDrained = 14,
-  kBarPsEmpty = 15,
-  kBarAccFull = 16,
-  kBarDrain = 17,
-  kBarRowStats = 18,  // +buffer (2): LSE_i / D_i staged in shared memory
-  kNumBwdBars = 20,
+  kBarSFull = 9,     // S^T in TMEM
+  kBarDpFull = 10,   // dP^T in TMEM
+  kBarPFull = 11,    // P^T in shared memory (4 warp arrivals)
+  kBarPtEmpty = 12,  // P^T shared memory free again (dV MMA done)
+  kBarDsFull = 13,   // dS^T in shared memory, dP^T read out (4 warp arrivals)
+  kBarDsEmpty = 14,  // dS^T shared memory free again (dK, dQ MMAs done)
+  kBarDqFull = 15,   // dQ_i in TMEM
+  kBarDqDrained = 16,  // dQ_i read out of TMEM (4 warp arrivals)
+  kBarAccFull = 17,  // dK, dV complete
+  kBarDrain = 18,
+  kBarRowStats = 19,  // +buffer (2): LSE_i / D_i staged in shared memory (128 arrivals)
+  kNumBwdBars = 21,
 };
 
 template <int D>
 struct BwdCfg {
   using T = HeadDim<D>;
-  static constexpr int kStages = D == 128 ? 1 : 2;  // Q / dO ring depth
-  // TMEM regions start on 32-column boundaries.
+  static constexpr int kQStages = 2;
+  static constexpr int kDoStages = D == 128 ? 1 : 2;  // shared memory is full at D = 128
+  // TMEM: S^T [0,128), dP^T [128,256) (dQ_i reuses these columns once dS^T
+  // is formed), dV and dK after them on 32-column boundaries.
   static constexpr int kCols = D < 32 ? 32 : D;
-  static constexpr bool kDqAliasesS = 256 + 3 * kCols > 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + kCols;
-  static constexpr uint32_t kColDQ = kDqAliasesS ? 0 : 256 + 2 * kCols;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 256 + kCols;
   // shared memory
   static constexpr int kK = 0;
   static constexpr int kV = kK + T::kTileBytes;
   static constexpr int kQ = kV + T::kTileBytes;
-  static constexpr int kDo = kQ + kStages * T::kTileBytes;
-  static constexpr int kPt = kDo + kStages * T::kTileBytes;
+  static constexpr int kDo = kQ + kQStages * T::kTileBytes;
+  static constexpr int kPt = kDo + kDoStages * T::kTileBytes;
   static constexpr int kDSt = kPt + Square::kTileBytes;
   static constexpr int kLse = kDSt + Square::kTileBytes;  // [2][128] fp32, pre-multiplied by log2 e
   static constexpr int kDv = kLse + 2 * 128 * 4;          // [2][128] fp32
   static constexpr int kBars = kDv + 2 * 128 * 4;
   static constexpr int kTmemSlot = kBars + kNumBwdBars * 8;
   static constexpr int kUsed = kTmemSlot + 16;
-  static constexpr int kBytes = (kUsed + 1024) > 116 * 1024 ? (kUsed + 1024) : 116 * 1024;
-  static_assert(kUsed + 1024 <= 232448, "backward tile does not fit in shared memory");
+  // Request 1 KB of slack to round the base up to 1024 bytes when it fits;
+  // otherwise the kernel requires (and checks) an aligned base.
+  static constexpr int kMaxSmem = 232448;
+  static constexpr int kBytes = kUsed + 1024 <= kMaxSmem ? (kUsed + 1024 > 116 * 1024 ? kUsed + 1024 : 116 * 1024)
+                                                         : kUsed;
+  static_assert(kUsed <= kMaxSmem, "backward tile does not fit in shared memory");
 };
 
 // ---------------------------------------------------------------- preprocess
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __rest
 
 // ---------------------------------------------------------------- main
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __maxnreg__(200)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const float* __restrict__ lse, const float* __restrict__ Dvec, float* __restrict__ dq_acc,
@@ -153,9 +158,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    float scale_log2) {
   using T = HeadDim<D>;
   using C = BwdCfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int SQ = C::kQStages, SD = C::kDoStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int* status = &g_bwd_status;
+  if (smem + C::kUsed > smem_raw + C::kBytes) {  // base not 1024-aligned and no slack requested
+    if (threadIdx.x == 0) atomicCAS(status, kDevOk, kDevSmemMisaligned);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
   float* sLse = reinterpret_cast<float*>(smem + C::kLse);
@@ -166,7 +176,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sDo = smem_u32(smem + C::kDo);
   const uint32_t sPt = smem_u32(smem + C::kPt);
   const uint32_t sDSt = smem_u32(smem + C::kDSt);
-  int* status = &g_bwd_status;
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -177,28 +186,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int i_begin = CAUSAL ? jt : 0;
   const int n_q = num_tiles - i_begin;
 
-  if (threadIdx.x == kBwdThreads - 64) {
+  if (threadIdx.x == 8 * 32) {
     mbar_init(&bars[kBarKV], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kBarQFull + s], 1);
       mbar_init(&bars[kBarQEmpty + s], 1);
       mbar_init(&bars[kBarDoFull + s], 1);
       mbar_init(&bars[kBarDoEmpty + s], 1);
+      mbar_init(&bars[kBarRowStats + s], 128);
     }
     mbar_init(&bars[kBarSFull], 1);
     mbar_init(&bars[kBarDpFull], 1);
     mbar_init(&bars[kBarPFull], 4);
+    mbar_init(&bars[kBarPtEmpty], 1);
     mbar_init(&bars[kBarDsFull], 4);
+    mbar_init(&bars[kBarDsEmpty], 1);
     mbar_init(&bars[kBarDqFull], 1);
     mbar_init(&bars[kBarDqDrained], 4);
-    mbar_init(&bars[kBarPsEmpty], 1);
     mbar_init(&bars[kBarAccFull], 1);
     mbar_init(&bars[kBarDrain], 1);
-    mbar_init(&bars[kBarRowStats], 128);
-    mbar_init(&bars[kBarRowStats + 1], 128);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -222,82 +231,92 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
 #pragma unroll 1
       for (int it = 0; it < n_q; ++it) {
-        const int st = it % S, u = it / S;
         const int q0 = (i_begin + it) * kTileRows;
-        if (it >= S && !mbar_wait(&bars[kBarDoEmpty + st], (u - 1) & 1, status)) break;
-        mbar_arrive_expect_tx(&bars[kBarDoFull + st], T::kTileBytes);
-        for (int b = 0; b < T::kNumBoxes; ++b)
-          tma_load_3d(smem + C::kDo + st * T::kTileBytes + b * T::kBoxBytes, &tm_do, &bars[kBarDoFull + st],
-                      b * T::kBoxCols, q0, bh);
-        last_do[st] = it;
-        if (it >= S && !mbar_wait(&bars[kBarQEmpty + st], (u - 1) & 1, status)) break;
-        mbar_arrive_expect_tx(&bars[kBarQFull + st], T::kTileBytes);
-        for (int b = 0; b < T::kNumBoxes; ++b)
-          tma_load_3d(smem + C::kQ + st * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQFull + st],
-                      b * T::kBoxCols, q0, bh);
-        last_q[st] = it;
+        {
+          const int st = it % SQ, u = it / SQ;
+          if (it >= SQ && !mbar_wait(&bars[kBarQEmpty + st], (u - 1) & 1, status)) break;
+          mbar_arrive_expect_tx(&bars[kBarQFull + st], T::kTileBytes);
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_load_3d(smem + C::kQ + st * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQFull + st],
+                        b * T::kBoxCols, q0, bh);
+          last_q[st] = it;
+        }
+        {
+          const int st = it % SD, u = it / SD;
+          if (it >= SD && !mbar_wait(&bars[kBarDoEmpty + st], (u - 1) & 1, status)) break;
+          mbar_arrive_expect_tx(&bars[kBarDoFull + st], T::kTileBytes);
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_load_3d(smem + C::kDo + st * T::kTileBytes + b * T::kBoxBytes, &tm_do, &bars[kBarDoFull + st],
+                        b * T::kBoxCols, q0, bh);
+          last_do[st] = it;
+        }
       }
+      // Never leave the CTA with a TMA write still landing in shared memory.
       mbar_wait(&bars[kBarKV], 0, status);
-      for (int s = 0; s < S; ++s) {
-        if (last_q[s] >= 0) mbar_wait(&bars[kBarQFull + s], (last_q[s] / S) & 1, status);
-        if (last_do[s] >= 0) mbar_wait(&bars[kBarDoFull + s], (last_do[s] / S) & 1, status);
+      for (int s = 0; s < 2; ++s) {
+        if (last_q[s] >= 0) mbar_wait(&bars[kBarQFull + s], (last_q[s] / SQ) & 1, status);
+        if (last_do[s] >= 0) mbar_wait(&bars[kBarDoFull + s], (last_do[s] / SD) & 1, status);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdSq = make_idesc_bf16(128, 128, false, false);  // K x Q^T, V x dO^T
       constexpr uint32_t kIdKV = make_idesc_bf16(128, D, false, true);     // P^T x dO, dS^T x Q
       constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, true, true);      // dS x K
-      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDV = tmem + C::kColDV,
-                     tDK = tmem + C::kColDK, tDQ = tmem + C::kColDQ;
+      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ,
+                     tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
       bool ok = mbar_wait(&bars[kBarKV], 0, status);
 #pragma unroll 1
       for (int it = 0; ok && it < n_q; ++it) {
-        const int st = it % S, u = it / S;
-        const uint32_t q_s = sQ + st * T::kTileBytes, do_s = sDo + st * T::kTileBytes;
-        if (!(ok = mbar_wait(&bars[kBarQFull + st], u & 1, status))) break;
-        if (C::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bars[kBarDqDrained], (it - 1) & 1, status))) break;
+        const int qs = it % SQ, qu = it / SQ, ds = it % SD, du = it / SD;
+        const uint32_t q_s = sQ + qs * T::kTileBytes, do_s = sDo + ds * T::kTileBytes;
+        // S^T = K Q_i^T.  The S^T columns are free: the compute warps read
+        // S^T(i-1) before they signalled P(i-1).
+        if (!(ok = mbar_wait(&bars[kBarQFull + qs], qu & 1, status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ss(tS, T::kmajor_desc(sK, kk), T::kmajor_desc(q_s, kk), kIdSq, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarSFull]);
-        if (!(ok = mbar_wait(&bars[kBarDoFull + st], u & 1, status))) break;
+        // dP^T = V dO_i^T into the columns dQ(i-1) occupied.
+        if (!(ok = mbar_wait(&bars[kBarDoFull + ds], du & 1, status))) break;
+        if (it >= 1 && !(ok = mbar_wait(&bars[kBarDqDrained], (it - 1) & 1, status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ss(tDP, T::kmajor_desc(sV, kk), T::kmajor_desc(do_s, kk), kIdSq, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarDpFull]);
+        // dV += P^T dO_i
         if (!(ok = mbar_wait(&bars[kBarPFull], it & 1, status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
           mma_bf16_ss(tDV, Square::kmajor_desc(sPt, kk), T::mnmajor_desc(do_s, kk), kIdKV,
                       (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarDoEmpty + st]);
+        mma_commit(&bars[kBarDoEmpty + ds]);
+        mma_commit(&bars[kBarPtEmpty]);
+        // dK += dS^T Q_i ; dQ_i = dS K (dS read as the MN-major view of dS^T)
         if (!(ok = mbar_wait(&bars[kBarDsFull], it & 1, status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
           mma_bf16_ss(tDK, Square::kmajor_desc(sDSt, kk), T::mnmajor_desc(q_s, kk), kIdKV,
                       (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarQEmpty + st]);
-        if (!C::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bars[kBarDqDrained], (it - 1) & 1, status))) break;
-        tc_fence_after();
+        mma_commit(&bars[kBarQEmpty + qs]);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
           mma_bf16_ss(tDQ, Square::mnmajor_desc(sDSt, kk), T::mnmajor_desc(sK, kk), kIdDQ, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarDqFull]);
-        mma_commit(&bars[kBarPsEmpty]);
+        mma_commit(&bars[kBarDsEmpty]);
       }
       if (ok) mma_commit(&bars[kBarAccFull]);
       mma_commit(&bars[kBarDrain]);
       mbar_wait(&bars[kBarDrain], 0, status);
     }
-  } else {
-    // ------------------------------------------------------------ compute
-    const int t = threadIdx.x;  // TMEM lane; key row kv0 + t; query row q0 + t in the dQ drain
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P / dS warps
+    const int t = threadIdx.x;  // TMEM lane = key row kv0 + t
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int kv_row = kv0 + t;
     bool ok = true;
@@ -319,38 +338,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* lse2 = sLse + b * 128;
       const float* dvec = sDv + b * 128;
 
-      // P^T = 2^(scale log2e S^T - log2e LSE), masked.
+      // P^T = 2^(scale log2e S^T - log2e LSE), masked, kept as packed bf16.
       if (!(ok = mbar_wait(&bars[kBarSFull], it & 1, status))) break;
       tc_fence_after();
-      float p[4][32];
+      uint32_t pk[64];
+      const bool row_dead = kv_row >= N;
+      const int first = (CAUSAL && i == jt) ? kv_row - q0 : 0;  // queries q0 + c with c < first cannot see this key
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + C::kColS + c * 32, p[c]);
-      tmem_wait_ld();
+      for (int c = 0; c < 4; ++c) {
+        float sv[32];
+        tmem_ld32(tmem + lane_base + C::kColS + c * 32, sv);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) p[c][e] = ex2_approx(fmaf(p[c][e], scale_log2, -lse2[c * 32 + e]));
-      if (kv_row >= N) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) p[c][e] = 0.f;
-      } else if (CAUSAL && i == jt) {
-        // key kv_row is visible to query q0 + col iff kv_row <= q0 + col
-        const int first = kv_row - q0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < first) p[c][e] = 0.f;
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = ex2_approx(fmaf(sv[e], scale_log2, -lse2[c * 32 + e]));
+          float p1 = ex2_approx(fmaf(sv[e + 1], scale_log2, -lse2[c * 32 + e + 1]));
+          if (row_dead || c * 32 + e < first) p0 = 0.f;
+          if (row_dead || c * 32 + e + 1 < first) p1 = 0.f;
+          pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+        }
       }
-      if (it >= 1 && !(ok = mbar_wait(&bars[kBarPsEmpty], (it - 1) & 1, status))) break;
+      if (it >= 1 && !(ok = mbar_wait(&bars[kBarPtEmpty], (it - 1) & 1, status))) break;
 #pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        const float* v = &p[c16 >> 2][(c16 & 3) * 8];
-        store_square_chunk(sPt, t, c16, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-      }
+      for (int c16 = 0; c16 < 16; ++c16)
+        store_square_chunk(sPt, t, c16, pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -358,6 +369,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
       // dS^T = P^T * (dP^T - D)
       if (!(ok = mbar_wait(&bars[kBarDpFull], it & 1, status))) break;
+      if (it >= 1 && !(ok = mbar_wait(&bars[kBarDsEmpty], (it - 1) & 1, status))) break;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -366,54 +378,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
-          float ds[8];
+          uint32_t w[4];
 #pragma unroll
-          for (int x = 0; x < 8; ++x) ds[x] = p[c][e + x] * (dp[e + x] - dvec[c * 32 + e + x]);
-          store_square_chunk(sDSt, t, c * 4 + e / 8, pack_bf16x2(ds[0], ds[1]), pack_bf16x2(ds[2], ds[3]),
-                             pack_bf16x2(ds[4], ds[5]), pack_bf16x2(ds[6], ds[7]));
+          for (int x = 0; x < 4; ++x) {
+            const float2 pp = unpack_bf16x2(pk[c * 16 + (e + 2 * x) / 2]);
+            const int col = c * 32 + e + 2 * x;
+            w[x] = pack_bf16x2(pp.x * (dp[e + 2 * x] - dvec[col]), pp.y * (dp[e + 2 * x + 1] - dvec[col + 1]));
+          }
+          store_square_chunk(sDSt, t, c * 4 + e / 8, w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarDsFull]);
-
-      // dQ_i partial (query row q0 + t) -> fp32 atomics.
+    }
+    tc_fence_before();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ drain + epilogue warps
+    const int t = threadIdx.x - 128;  // TMEM lane: query row q0 + t (dQ), key row kv0 + t (dK, dV)
+    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    bool ok = true;
+#pragma unroll 1
+    for (int it = 0; it < n_q; ++it) {
+      const int q = (i_begin + it) * kTileRows + t;
       if (!(ok = mbar_wait(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
-      {
-        const int q = q0 + t;
-        float* dst = dq_acc + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
-        if constexpr (D >= 32) {
+      float* dst = dq_acc + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
+      if constexpr (D >= 32) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float g[32];
-            tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
-            tmem_wait_ld();
-            if (q < N) {
-#pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
-            }
-          }
-        } else {
-          float g[16];
-          tmem_ld16(tmem + lane_base + C::kColDQ, g);
+        for (int c = 0; c < D / 32; ++c) {
+          float g[32];
+          tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
           tmem_wait_ld();
+          if (c == D / 32 - 1) {  // every dQ column is in registers: release the TMEM columns early
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+          }
           if (q < N) {
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
+            for (int e = 0; e < 32; e += 4)
+              atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
           }
         }
+      } else {
+        float g[16];
+        tmem_ld16(tmem + lane_base + C::kColDQ, g);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+        if (q < N) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            atomicAdd(reinterpret_cast<float4*>(dst + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
     }
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue: dV, dK * scale -> bf16
     if (ok && mbar_wait(&bars[kBarAccFull], 0, status)) {
       tc_fence_after();
+      const int kv_row = kv0 + t;
       const bool valid = kv_row < N;
       const size_t off = (static_cast<size_t>(bh) * N + (valid ? kv_row : 0)) * D;
 #pragma unroll
@@ -455,7 +481,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -20,6 +20,7 @@ namespace fa2 {
 enum DeviceStatus : int {
   kDevOk = 0,
   kDevWaitTimeout = 1,
+  kDevSmemMisaligned = 2,
 };
 
 // ---------------------------------------------------------------- generic
@@ -259,6 +260,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&v);
+  return __bfloat1622float2(b);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
