@@ -121,6 +121,11 @@ const char* fa2_status_string(int status);
  * Synchronous with respect to the device. Returns an fa2_status. */
 int fa2_device_status(int* value, int reset);
 
+/* Text describing the last CUDA failure (FA2_ERR_CUDA / FA2_ERR_ALLOC) an
+ * entry point saw on the calling host thread: "where: cudaErrorName (text)".
+ * Empty if none.  Valid until the next failing call on the same thread. */
+const char* fa2_last_error_detail(void);
+
 /* ABI version of this header (major * 100 + minor). */
 int fa2_abi_version(void);
 

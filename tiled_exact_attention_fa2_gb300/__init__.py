@@ -45,13 +45,16 @@ _SIGNATURES = {
     "fa2_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "fa2_bwd_main": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "fa2_last_error_detail": (ctypes.c_char_p, []),
 }
 
 
 class FA2Error(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} failed with status {status}: {fa2_status_string(status)}")
+        detail = load_library().fa2_last_error_detail().decode() if status in (6, 7) else ""
+        super().__init__(f"{fn} failed with status {status}: {fa2_status_string(status)}"
+                         + (f" [{detail}]" if detail else ""))
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

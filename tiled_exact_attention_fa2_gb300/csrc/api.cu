@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -54,6 +55,16 @@ bool make_tmap(CUtensorMap* out, const void* base, int BH, int N, int d) {
   return enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Text of the last CUDA failure seen by an entry point on this host thread.
+thread_local char g_last_error[256] = "";
+
+int cuda_fail(int cuda_code, const char* where) {
+  const cudaError_t e = static_cast<cudaError_t>(cuda_code);
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return FA2_ERR_CUDA;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -114,7 +125,7 @@ int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const v
   return (make_tmap(&tm->q, q, BH, N, d) && make_tmap(&tm->k, k, BH, N, d) && make_tmap(&tm->v, v, BH, N, d) &&
           make_tmap(&tm->dO, dO, BH, N, d))
              ? FA2_OK
-             : FA2_ERR_CUDA;
+             : cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
 }
 
 int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
@@ -125,9 +136,10 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
   const size_t rows = static_cast<size_t>(BH) * N;
   float* Dvec = static_cast<float*>(ws);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(rows * sizeof(float)));
-  if (launch_bwd_preprocess(o, dO, Dvec, dq_acc, BH, N, d, st) != 0) return FA2_ERR_CUDA;
-  if (launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, BH, N, d, scale, causal != 0, st) != 0) return FA2_ERR_CUDA;
-  if (launch_bwd_dq_convert(dq_acc, dq, BH, N, d, scale, st) != 0) return FA2_ERR_CUDA;
+  if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, BH, N, d, st)) return cuda_fail(e, "bwd preprocess launch");
+  if (int e = launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, BH, N, d, scale, causal != 0, st))
+    return cuda_fail(e, "bwd main launch");
+  if (int e = launch_bwd_dq_convert(dq_acc, dq, BH, N, d, scale, st)) return cuda_fail(e, "dq convert launch");
   return FA2_OK;
 }
 
@@ -137,10 +149,11 @@ int ensure_max_smem(const void* kernel, int bytes) {
   static std::mutex mu;
   static std::set<std::pair<const void*, int>> done;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaError_t e = cudaGetDevice(&dev)) return static_cast<int>(e);
   std::lock_guard<std::mutex> lock(mu);
   if (done.count({kernel, dev})) return 0;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return -1;
+  if (cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))
+    return static_cast<int>(e);
   done.insert({kernel, dev});
   return 0;
 }
@@ -169,10 +182,10 @@ int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   const int BH = B * H;
   TmapSet tm;
   if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, BH, N, d) || !make_tmap(&tm.v, v, BH, N, d))
-    return FA2_ERR_CUDA;
-  return launch_fwd(tm, o, lse, BH, N, d, scale, causal != 0, static_cast<cudaStream_t>(stream)) == 0
-             ? FA2_OK
-             : FA2_ERR_CUDA;
+    return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
+  if (int e = launch_fwd(tm, o, lse, BH, N, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
+    return cuda_fail(e, "fwd launch");
+  return FA2_OK;
 }
 
 size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -196,12 +209,13 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const vo
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = workspace_bytes(B, H, N, d);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess || !ws) {
+  if (cudaError_t e = cudaMallocAsync(&ws, bytes, st)) {
     cudaGetLastError();
+    cuda_fail(static_cast<int>(e), "cudaMallocAsync");
     return FA2_ERR_ALLOC;
   }
   const int rc = run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, st);
-  if (cudaFreeAsync(ws, st) != cudaSuccess) return FA2_ERR_CUDA;
+  if (cudaError_t e = cudaFreeAsync(ws, st)) return cuda_fail(static_cast<int>(e), "cudaFreeAsync");
   return rc;
 }
 
@@ -217,9 +231,9 @@ int fa2_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc
   for (const Range& r : ins)
     if (overlap(rd, r) || overlap(ra, r)) return FA2_ERR_ALIAS;
   if (overlap(rd, ra)) return FA2_ERR_ALIAS;
-  return launch_bwd_preprocess(o, dO, Dvec, dq_acc, B * H, N, d, static_cast<cudaStream_t>(stream)) == 0
-             ? FA2_OK
-             : FA2_ERR_CUDA;
+  if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, B * H, N, d, static_cast<cudaStream_t>(stream)))
+    return cuda_fail(e, "bwd preprocess launch");
+  return FA2_OK;
 }
 
 int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
@@ -245,10 +259,10 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
   }
   TmapSet tm;
   if (int rc = make_tmaps(&tm, q, k, v, dO, B * H, N, d)) return rc;
-  return launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, B * H, N, d, scale, causal != 0,
-                         static_cast<cudaStream_t>(stream)) == 0
-             ? FA2_OK
-             : FA2_ERR_CUDA;
+  if (int e = launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, B * H, N, d, scale, causal != 0,
+                              static_cast<cudaStream_t>(stream)))
+    return cuda_fail(e, "bwd main launch");
+  return FA2_OK;
 }
 
 int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale, void* stream) {
@@ -258,9 +272,9 @@ int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d
   if (!aligned(dq_acc, 16) || !aligned(dq, 16)) return FA2_ERR_ALIGN;
   const size_t n = static_cast<size_t>(B) * H * N * d;
   if (overlap(range_of(dq_acc, n * 4), range_of(dq, n * 2))) return FA2_ERR_ALIAS;
-  return launch_bwd_dq_convert(dq_acc, dq, B * H, N, d, scale, static_cast<cudaStream_t>(stream)) == 0
-             ? FA2_OK
-             : FA2_ERR_CUDA;
+  if (int e = launch_bwd_dq_convert(dq_acc, dq, B * H, N, d, scale, static_cast<cudaStream_t>(stream)))
+    return cuda_fail(e, "dq convert launch");
+  return FA2_OK;
 }
 
 const char* fa2_status_string(int status) {
@@ -282,11 +296,14 @@ const char* fa2_status_string(int status) {
 int fa2_device_status(int* value, int reset) {
   if (!value) return FA2_ERR_NULL;
   int a = 0, b = 0;
-  if (read_fwd_status(&a, reset != 0) != 0 || read_bwd_status(&b, reset != 0) != 0) return FA2_ERR_CUDA;
+  if (int e = read_fwd_status(&a, reset != 0)) return cuda_fail(e, "read status");
+  if (int e = read_bwd_status(&b, reset != 0)) return cuda_fail(e, "read status");
   *value = a > b ? a : b;
   return FA2_OK;
 }
 
 int fa2_abi_version(void) { return 100; }
+
+const char* fa2_last_error_detail(void) { return g_last_error; }
 
 }  // extern "C"

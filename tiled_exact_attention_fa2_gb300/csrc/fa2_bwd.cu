@@ -45,6 +45,10 @@ __device__ int g_bwd_status;
 
 namespace {
 
+// 10 warps: P/dS warpgroup (0-3), dQ-drain/epilogue warpgroup (4-7), TMA
+// producer (8), MMA issuer (9).  Warps spread round-robin over the four SM
+// sub-partitions (16K registers each), so two sub-partitions hold three
+// warps: at most 168 registers per thread, which the kernel fits unspilled.
 constexpr int kBwdThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.44269504088896341f;
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __rest
 
 // ---------------------------------------------------------------- main
 template <int D, bool CAUSAL>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const float* __restrict__ lse, const float* __restrict__ Dvec, float* __restrict__ dq_acc,
@@ -266,10 +270,15 @@ __global__ void __maxnreg__(200)
       constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, true, true);      // dS x K
       const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ,
                      tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+      const uint32_t sK0 = sK, sV0 = sV, sPt0 = sPt, sDSt0 = sDSt, sQ0 = sQ, sDo0 = sDo;
       bool ok = mbar_wait(&bars[kBarKV], 0, status);
 #pragma unroll 1
       for (int it = 0; ok && it < n_q; ++it) {
         const int qs = it % SQ, qu = it / SQ, ds = it % SD, du = it / SD;
+        // Recompute the operand descriptors every iteration (a few integer
+        // ops) instead of keeping ~40 hoisted 64-bit descriptors live.
+        uint32_t sK = sK0, sV = sV0, sPt = sPt0, sDSt = sDSt0, sQ = sQ0, sDo = sDo0;
+        opaque(sK); opaque(sV); opaque(sPt); opaque(sDSt); opaque(sQ); opaque(sDo);
         const uint32_t q_s = sQ + qs * T::kTileBytes, do_s = sDo + ds * T::kTileBytes;
         // S^T = K Q_i^T.  The S^T columns are free: the compute warps read
         // S^T(i-1) before they signalled P(i-1).
@@ -495,7 +504,7 @@ int launch_preprocess_t(const void* o, const void* dO, float* Dvec, float* dq_ac
   const long long blocks = (threads + 255) / 256;
   fa2_bwd_preprocess_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, rows);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return static_cast<int>(cudaGetLastError());
 }
 
 template <int D, bool CAUSAL>
@@ -503,13 +512,13 @@ int launch_bwd_main_t(const TmapSet& tm, const float* lse, const float* Dvec, fl
                       int BH, int N, float scale, cudaStream_t stream) {
   using C = BwdCfg<D>;
   auto kern = fa2_bwd_kernel<D, CAUSAL>;
-  if (ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes) != 0) return -1;
+  if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_tiles = (N + kTileRows - 1) / kTileRows;
   const dim3 grid(static_cast<unsigned>(num_tiles) * static_cast<unsigned>(BH));
   kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, lse, Dvec, dq_acc,
                                                   static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
                                                   BH, N, scale, scale * kLog2e);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return static_cast<int>(cudaGetLastError());
 }
 
 int launch_dq_convert(const float* dq_acc, void* dq, long long elems, float scale, cudaStream_t stream) {
@@ -519,7 +528,7 @@ int launch_dq_convert(const float* dq_acc, void* dq, long long elems, float scal
   if (blocks < 1) blocks = 1;
   fa2_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace
@@ -532,7 +541,7 @@ int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_
     case 32: return launch_preprocess_t<32>(o, dO, Dvec, dq_acc, rows, stream);
     case 64: return launch_preprocess_t<64>(o, dO, Dvec, dq_acc, rows, stream);
     case 128: return launch_preprocess_t<128>(o, dO, Dvec, dq_acc, rows, stream);
-    default: return -1;
+    default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
 
@@ -547,7 +556,7 @@ int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, floa
                            : launch_bwd_main_t<64, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
     case 128: return causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
                             : launch_bwd_main_t<128, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
-    default: return -1;
+    default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
 
@@ -556,10 +565,10 @@ int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, f
 }
 
 int read_bwd_status(int* value, bool reset) {
-  if (cudaMemcpyFromSymbol(value, g_bwd_status, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaError_t e = cudaMemcpyFromSymbol(value, g_bwd_status, sizeof(int))) return static_cast<int>(e);
   if (reset) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+    if (cudaError_t e = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int))) return static_cast<int>(e);
   }
   return 0;
 }

@@ -333,13 +333,13 @@ template <int D, bool CAUSAL>
 int launch_fwd_t(const TmapSet& tm, void* o, float* lse, int BH, int N, float scale, cudaStream_t stream) {
   using L = FwdSmem<D>;
   auto kern = fa2_fwd_kernel<D, CAUSAL>;
-  if (ensure_max_smem(reinterpret_cast<const void*>(kern), L::kBytes) != 0) return -1;
+  if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), L::kBytes)) return rc;
   const int num_q_tiles = (N + kTileRows - 1) / kTileRows;
   const dim3 grid(static_cast<unsigned>(num_q_tiles) * static_cast<unsigned>(BH));
   const float scale_log2 = scale * 1.44269504088896341f;
   kern<<<grid, kFwdThreads, L::kBytes, stream>>>(tm.q, tm.k, tm.v, static_cast<__nv_bfloat16*>(o), lse, BH, N,
                                                   scale_log2);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace
@@ -355,15 +355,15 @@ int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, flo
                            : launch_fwd_t<64, false>(tm, o, lse, BH, N, scale, stream);
     case 128: return causal ? launch_fwd_t<128, true>(tm, o, lse, BH, N, scale, stream)
                             : launch_fwd_t<128, false>(tm, o, lse, BH, N, scale, stream);
-    default: return -1;
+    default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
 
 int read_fwd_status(int* value, bool reset) {
-  if (cudaMemcpyFromSymbol(value, g_fwd_status, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaError_t e = cudaMemcpyFromSymbol(value, g_fwd_status, sizeof(int))) return static_cast<int>(e);
   if (reset) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_fwd_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+    if (cudaError_t e = cudaMemcpyToSymbol(g_fwd_status, &zero, sizeof(int))) return static_cast<int>(e);
   }
   return 0;
 }

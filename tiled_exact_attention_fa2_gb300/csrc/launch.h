@@ -11,6 +11,8 @@ struct TmapSet {
   CUtensorMap q, k, v, dO;
 };
 
+// Every function below returns 0 or the cudaError_t value of the failure.
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).
 int ensure_max_smem(const void* kernel, int bytes);
 
