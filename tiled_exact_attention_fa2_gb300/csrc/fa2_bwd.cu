@@ -271,23 +271,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ,
                      tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
       const uint32_t sK0 = sK, sV0 = sV, sPt0 = sPt, sDSt0 = sDSt, sQ0 = sQ, sDo0 = sDo;
-      bool ok = mbar_wait(&bars[kBarKV], 0, status);
-#pragma unroll 1
-      for (int it = 0; ok && it < n_q; ++it) {
-        const int qs = it % SQ, qu = it / SQ, ds = it % SD, du = it / SD;
-        // Recompute the operand descriptors every iteration (a few integer
-        // ops) instead of keeping ~40 hoisted 64-bit descriptors live.
-        uint32_t sK = sK0, sV = sV0, sPt = sPt0, sDSt = sDSt0, sQ = sQ0, sDo = sDo0;
-        opaque(sK); opaque(sV); opaque(sPt); opaque(sDSt); opaque(sQ); opaque(sDo);
-        const uint32_t q_s = sQ + qs * T::kTileBytes, do_s = sDo + ds * T::kTileBytes;
-        // S^T = K Q_i^T.  The S^T columns are free: the compute warps read
-        // S^T(i-1) before they signalled P(i-1).
-        if (!(ok = mbar_wait(&bars[kBarQFull + qs], qu & 1, status))) break;
+      // Issue order per query tile i (S^T(i) is issued one tile ahead so the
+      // compute warps find it ready when they finish dS(i-1)):
+      //   dP^T(i), dV(i), S^T(i+1), dQ(i), dK(i)
+      auto issue_s = [&](int it) -> bool {
+        const int qs = it % SQ;
+        if (!mbar_wait(&bars[kBarQFull + qs], (it / SQ) & 1, status)) return false;
+        uint32_t sK = sK0, sQ = sQ0;
+        opaque(sK);
+        opaque(sQ);
+        const uint32_t q_s = sQ + qs * T::kTileBytes;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ss(tS, T::kmajor_desc(sK, kk), T::kmajor_desc(q_s, kk), kIdSq, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarSFull]);
+        return true;
+      };
+      bool ok = mbar_wait(&bars[kBarKV], 0, status) && issue_s(0);
+#pragma unroll 1
+      for (int it = 0; ok && it < n_q; ++it) {
+        const int qs = it % SQ, ds = it % SD, du = it / SD;
+        // Recompute the operand descriptors every iteration (a few integer
+        // ops) instead of keeping ~40 hoisted 64-bit descriptors live.
+        uint32_t sK = sK0, sV = sV0, sPt = sPt0, sDSt = sDSt0, sQ = sQ0, sDo = sDo0;
+        opaque(sK); opaque(sV); opaque(sPt); opaque(sDSt); opaque(sQ); opaque(sDo);
+        const uint32_t q_s = sQ + qs * T::kTileBytes, do_s = sDo + ds * T::kTileBytes;
         // dP^T = V dO_i^T into the columns dQ(i-1) occupied.
         if (!(ok = mbar_wait(&bars[kBarDoFull + ds], du & 1, status))) break;
         if (it >= 1 && !(ok = mbar_wait(&bars[kBarDqDrained], (it - 1) & 1, status))) break;
@@ -305,18 +314,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarDoEmpty + ds]);
         mma_commit(&bars[kBarPtEmpty]);
-        // dK += dS^T Q_i ; dQ_i = dS K (dS read as the MN-major view of dS^T)
+        // S^T(i+1): the compute warps have read S^T(i) (they signalled P(i)).
+        if (it + 1 < n_q && !(ok = issue_s(it + 1))) break;
+        // dQ_i = dS K (dS read as the MN-major view of dS^T); dK += dS^T Q_i
         if (!(ok = mbar_wait(&bars[kBarDsFull], it & 1, status))) break;
         tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_bf16_ss(tDQ, Square::mnmajor_desc(sDSt, kk), T::mnmajor_desc(sK, kk), kIdDQ, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kBarDqFull]);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
           mma_bf16_ss(tDK, Square::kmajor_desc(sDSt, kk), T::mnmajor_desc(q_s, kk), kIdKV,
                       (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarQEmpty + qs]);
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ss(tDQ, Square::mnmajor_desc(sDSt, kk), T::mnmajor_desc(sK, kk), kIdDQ, kk > 0 ? 1u : 0u);
-        mma_commit(&bars[kBarDqFull]);
         mma_commit(&bars[kBarDsEmpty]);
       }
       if (ok) mma_commit(&bars[kBarAccFull]);
@@ -329,17 +340,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int kv_row = kv0 + t;
     bool ok = true;
+    // LSE_i / D_i of this thread's query column, loaded one tile ahead.
+    auto load_stats = [&](int it, float& l2, float& dd) {
+      const int q = (i_begin + it) * kTileRows + t;
+      const bool in = q < N;
+      l2 = in ? __ldg(lse + static_cast<size_t>(bh) * N + q) * kLog2e : INFINITY;
+      dd = in ? __ldg(Dvec + static_cast<size_t>(bh) * N + q) : 0.f;
+    };
+    float nxt_lse, nxt_d;
+    load_stats(0, nxt_lse, nxt_d);
 #pragma unroll 1
     for (int it = 0; it < n_q; ++it) {
       const int i = i_begin + it;
       const int q0 = i * kTileRows;
       const int b = it & 1;
-      {
-        const int q = q0 + t;
-        const bool in = q < N;
-        sLse[b * 128 + t] = in ? lse[static_cast<size_t>(bh) * N + q] * kLog2e : INFINITY;
-        sDv[b * 128 + t] = in ? Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
-      }
+      sLse[b * 128 + t] = nxt_lse;
+      sDv[b * 128 + t] = nxt_d;
+      if (it + 1 < n_q) load_stats(it + 1, nxt_lse, nxt_d);
       // Every compute thread has staged its entry; a buffer is rewritten two
       // iterations later, after all four warps have passed the dS hand-off.
       mbar_arrive(&bars[kBarRowStats + b]);

@@ -1,5 +1,6 @@
 // FlashAttention-2 forward on sm_103a: TMA-fed tiles, tcgen05 MMAs with TMEM
-// accumulators and an online softmax, one CTA per (128-row query tile, head).
+// accumulators and an online softmax.  One CTA per (pair of 128-row query
+// tiles, head).
 //
 // Method: "Revolutionizing Web-Based AI: How a Plain JavaScript Prototype
 // Paved the Way for High-Performance WebGPU Flash Attention 2", section
@@ -10,16 +11,21 @@
 // (softmax reduction computed incrementally).  The per-row log-sum-exp is
 // saved for the backward pass (same article, backward-pass bullet).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t);
-//              reads S, masks, updates m/l, rescales O when m grows, writes
-//              P (bf16) to shared memory, and runs the epilogue.
-//   warp  4    TMA producer: Q once, then K_j / V_j into 2-stage rings.
-//   warp  5    MMA issuer (one thread) + TMEM owner:
-//              S_j = Q K_j^T into one of two TMEM S buffers (double buffered
-//              so S_{j+1} is computed while the softmax works on S_j), and
-//              O += P_j V_j into the TMEM O accumulator.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
+// GB300 design.  Two query tiles (A: rows q0..q0+127, B: q0+128..q0+255)
+// share every K/V tile, so the tensor core alternates between them while the
+// other tile's softmax runs:
+//   warps 0-3  softmax of tile A   (thread t owns row t = TMEM lane t)
+//   warps 4-7  softmax of tile B
+//   warp  8    TMA producer: Q_A, Q_B once, then K_j / V_j into 2-stage rings
+//   warp  9    MMA issuer (one thread) + TMEM owner
+// TMEM columns: S_A [0,128), S_B [128,256), O_A and O_B after them.  The
+// softmax overwrites the first 64 columns of S_X with P_X (bf16 pairs) and
+// O_X += P_X V_j reads P_X straight from TMEM (A operand in TMEM), so P never
+// touches shared memory.  S_X(j+1) is issued only after P_X(j) V_j has
+// completed, because it overwrites the columns that MMA reads.
+// The running max is updated lazily: O and l are rescaled only when a row's
+// max grows by more than 8 (log2 units); otherwise the stale max is kept and
+// P = 2^(s - m) stays <= 256, which is exact after the final O / l.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,8 +39,9 @@ __device__ int g_fwd_status;
 
 namespace {
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 320;
 constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 enum FwdBar {
   kBarQ = 0,
@@ -42,22 +49,23 @@ enum FwdBar {
   kBarKEmpty = 3,   // +stage
   kBarVFull = 5,    // +stage
   kBarVEmpty = 7,   // +stage
-  kBarSFull = 9,    // +buffer (2)
-  kBarSEmpty = 11,  // +buffer
-  kBarPFull = 13,
-  kBarPVDone = 14,
+  kBarSFull = 9,    // +tile (A, B)
+  kBarPFull = 11,   // +tile, 4 warp arrivals
+  kBarPVDone = 13,  // +tile
   kBarDrain = 15,
   kNumFwdBars = 16,
 };
 
 template <int D>
-struct FwdSmem {
+struct FwdCfg {
   using T = HeadDim<D>;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + T::kTileBytes;
+  static constexpr int kCols = D < 32 ? 32 : D;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + kCols;
+  static constexpr int kQ = 0;  // Q_A, Q_B
+  static constexpr int kK = kQ + 2 * T::kTileBytes;
   static constexpr int kV = kK + 2 * T::kTileBytes;
-  static constexpr int kP = kV + 2 * T::kTileBytes;
-  static constexpr int kBars = kP + Square::kTileBytes;
+  static constexpr int kBars = kV + 2 * T::kTileBytes;
   static constexpr int kTmemSlot = kBars + kNumFwdBars * 8;
   static constexpr int kUsed = kTmemSlot + 16;
   // +1024 so the base can be rounded up to a 1024-byte boundary; at least
@@ -71,28 +79,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out_o,
                    float* __restrict__ out_lse, int BH, int N, float scale_log2) {
   using T = HeadDim<D>;
-  using L = FwdSmem<D>;
+  using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
-  const uint32_t sQ = smem_u32(smem + L::kQ);
-  const uint32_t sK = smem_u32(smem + L::kK);
-  const uint32_t sV = smem_u32(smem + L::kV);
-  const uint32_t sP = smem_u32(smem + L::kP);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
   int* status = &g_fwd_status;
 
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // Heaviest query tiles first (causal work grows with the tile index).
-  const int num_q_tiles = (N + kTileRows - 1) / kTileRows;
+  // Heaviest query-tile pairs first (causal work grows with the pair index).
+  const int num_tiles = (N + kTileRows - 1) / kTileRows;
+  const int num_pairs = (num_tiles + 1) / 2;
   const int bh = blockIdx.x % BH;
-  const int qt = num_q_tiles - 1 - static_cast<int>(blockIdx.x / BH);
-  const int q0 = qt * kTileRows;
-  const int n_kv = CAUSAL ? (qt + 1) : num_q_tiles;
+  const int pair = num_pairs - 1 - static_cast<int>(blockIdx.x / BH);
+  const int q0 = pair * 2 * kTileRows;
+  // K/V tiles each query tile visits; a tile with no row < N visits none.
+  const int nA = CAUSAL ? 2 * pair + 1 : num_tiles;
+  const int nB = 2 * pair + 1 >= num_tiles ? 0 : (CAUSAL ? 2 * pair + 2 : num_tiles);
+  const int n_kv = nA > nB ? nA : nB;
 
-  if (threadIdx.x == kFwdThreads - 64) {  // warp 4, lane 0
+  if (threadIdx.x == 8 * 32) {
     mbar_init(&bars[kBarQ], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kBarKFull + s], 1);
@@ -100,14 +108,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars[kBarVFull + s], 1);
       mbar_init(&bars[kBarVEmpty + s], 1);
       mbar_init(&bars[kBarSFull + s], 1);
-      mbar_init(&bars[kBarSEmpty + s], 4);
+      mbar_init(&bars[kBarPFull + s], 4);
+      mbar_init(&bars[kBarPVDone + s], 1);
     }
-    mbar_init(&bars[kBarPFull], 4);
-    mbar_init(&bars[kBarPVDone], 1);
     mbar_init(&bars[kBarDrain], 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -115,104 +122,133 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_O = tmem + 256;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-      mbar_arrive_expect_tx(&bars[kBarQ], T::kTileBytes);
-      for (int b = 0; b < T::kNumBoxes; ++b)
-        tma_load_3d(smem + L::kQ + b * T::kBoxBytes, &tm_q, &bars[kBarQ], b * T::kBoxCols, q0, bh);
+      const int n_q_tiles = nB > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bars[kBarQ], n_q_tiles * T::kTileBytes);
+      for (int x = 0; x < n_q_tiles; ++x)
+        for (int b = 0; b < T::kNumBoxes; ++b)
+          tma_load_3d(smem + C::kQ + x * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQ], b * T::kBoxCols,
+                      q0 + x * kTileRows, bh);
+      int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;
 #pragma unroll 1
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
         if (j >= 2 && !mbar_wait(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
-          tma_load_3d(smem + L::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
+          tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
                       b * T::kBoxCols, j * kTileRows, bh);
-        last_k[st] = j;
+        (st ? last_k1 : last_k0) = j;
         if (j >= 2 && !mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
-          tma_load_3d(smem + L::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
+          tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
                       b * T::kBoxCols, j * kTileRows, bh);
-        last_v[st] = j;
+        (st ? last_v1 : last_v0) = j;
       }
       // Never leave the CTA with a TMA write still landing in shared memory.
       mbar_wait(&bars[kBarQ], 0, status);
-      for (int s = 0; s < 2; ++s) {
-        if (last_k[s] >= 0) mbar_wait(&bars[kBarKFull + s], (last_k[s] >> 1) & 1, status);
-        if (last_v[s] >= 0) mbar_wait(&bars[kBarVFull + s], (last_v[s] >> 1) & 1, status);
-      }
+      if (last_k0 >= 0) mbar_wait(&bars[kBarKFull + 0], (last_k0 >> 1) & 1, status);
+      if (last_k1 >= 0) mbar_wait(&bars[kBarKFull + 1], (last_k1 >> 1) & 1, status);
+      if (last_v0 >= 0) mbar_wait(&bars[kBarVFull + 0], (last_v0 >> 1) & 1, status);
+      if (last_v1 >= 0) mbar_wait(&bars[kBarVFull + 1], (last_v1 >> 1) & 1, status);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q (K-major) x K (K-major)
-      constexpr uint32_t kIdescO = make_idesc_bf16(128, D, false, true);     // P (K-major) x V (MN-major)
-      auto issue_pv = [&](int t) -> bool {
-        const int st = t & 1;
-        if (!mbar_wait(&bars[kBarPFull], t & 1, status)) return false;
-        if (!mbar_wait(&bars[kBarVFull + st], (t >> 1) & 1, status)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sV + st * T::kTileBytes;
+      constexpr uint32_t kIdescO = make_idesc_bf16(128, D, false, true);     // P (TMEM) x V (MN-major)
+      const uint32_t sQ0 = smem_u32(smem + C::kQ), sK0 = smem_u32(smem + C::kK), sV0 = smem_u32(smem + C::kV);
+      // S_x(j) = Q_x K_j^T into TMEM S_x.
+      auto issue_s = [&](int x, int j) {
+        uint32_t sQ = sQ0, sK = sK0;
+        opaque(sQ);
+        opaque(sK);
+        const uint32_t qb = sQ + x * T::kTileBytes, kb = sK + (j & 1) * T::kTileBytes;
+        const uint32_t d_tmem = tmem + (x ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(d_tmem, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kBarSFull + x]);
+      };
+      // O_x += P_x V_j with P_x read from the first 64 columns of S_x.
+      auto issue_pv = [&](int x, int j) {
+        uint32_t sV = sV0;
+        opaque(sV);
+        const uint32_t vb = sV + (j & 1) * T::kTileBytes;
+        const uint32_t a_tmem = tmem + (x ? C::kColS1 : C::kColS0);
+        const uint32_t d_tmem = tmem + (x ? C::kColO1 : C::kColO0);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ss(tmem_O, Square::kmajor_desc(sP, kk), T::mnmajor_desc(vbase, kk), kIdescO,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarPVDone]);
-        mma_commit(&bars[kBarVEmpty + st]);
-        return true;
+          mma_bf16_ts(d_tmem, a_tmem + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarPVDone + x]);
       };
-      bool ok = mbar_wait(&bars[kBarQ], 0, status);
+      bool ok = mbar_wait(&bars[kBarQ], 0, status) && mbar_wait(&bars[kBarKFull + 0], 0, status);
+      if (ok) {
+        tc_fence_after();
+        if (nA > 0) issue_s(0, 0);
+        if (nB > 0) issue_s(1, 0);
+        mma_commit(&bars[kBarKEmpty + 0]);
+      }
 #pragma unroll 1
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j & 1;
-        if (!(ok = mbar_wait(&bars[kBarKFull + st], (j >> 1) & 1, status))) break;
-        if (j >= 2 && !(ok = mbar_wait(&bars[kBarSEmpty + st], ((j >> 1) - 1) & 1, status))) break;
-        tc_fence_after();
-        const uint32_t kbase = sK + st * T::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + st * 128, T::kmajor_desc(sQ, kk), T::kmajor_desc(kbase, kk), kIdescS,
-                      kk > 0 ? 1u : 0u);
-        mma_commit(&bars[kBarSFull + st]);
-        mma_commit(&bars[kBarKEmpty + st]);
-        if (j >= 1) ok = issue_pv(j - 1);
+        const bool nextk = j + 1 < n_kv;
+        if (!(ok = mbar_wait(&bars[kBarVFull + st], (j >> 1) & 1, status))) break;
+        if (nextk && !(ok = mbar_wait(&bars[kBarKFull + (st ^ 1)], ((j + 1) >> 1) & 1, status))) break;
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {
+          const int nx = x == 0 ? nA : nB;
+          if (j >= nx) continue;
+          if (!(ok = mbar_wait(&bars[kBarPFull + x], j & 1, status))) break;
+          tc_fence_after();
+          issue_pv(x, j);
+          if (j + 1 < nx) {
+            // S_x(j+1) overwrites the P_x columns the MMA above reads.
+            if (!(ok = mbar_wait(&bars[kBarPVDone + x], j & 1, status))) break;
+            tc_fence_after();
+            issue_s(x, j + 1);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars[kBarVEmpty + st]);
+        if (nextk) mma_commit(&bars[kBarKEmpty + (st ^ 1)]);
       }
-      if (ok) issue_pv(n_kv - 1);
       // Wait for every MMA issued above before TMEM can be released.
       mma_commit(&bars[kBarDrain]);
       mbar_wait(&bars[kBarDrain], 0, status);
     }
   } else {
-    // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x;  // 0..127 = TMEM lane = row in the tile
-    const int q_row = q0 + r;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float m = -INFINITY;  // running max, log2 units (scores * scale * log2 e)
+    // ------------------------------------------------------------ softmax (tile x)
+    const int x = warp >> 2;
+    const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
+    const int q_row = q0 + x * kTileRows + r;
+    const int nx = x == 0 ? nA : nB;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (x ? C::kColS1 : C::kColS0);
+    const uint32_t tO = tmem + lane_base + (x ? C::kColO1 : C::kColO0);
+    float m = -INFINITY;  // max used for P, log2 units (scores * scale * log2 e)
     float l = 0.f;        // running sum of 2^(x - m)
     bool ok = true;
 #pragma unroll 1
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      if (!(ok = mbar_wait(&bars[kBarSFull + st], (j >> 1) & 1, status))) break;
+    for (int j = 0; j < nx; ++j) {
+      // S_x(j) was issued after O_x += P_x(j-1) V_{j-1} completed, so O_x is
+      // stable once S_x(j) has landed.
+      if (!(ok = mbar_wait(&bars[kBarSFull + x], j & 1, status))) break;
       tc_fence_after();
       float s[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + st * 128 + c * 32, s[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarSEmpty + st]);
 
       const int kv0 = j * kTileRows;
-      if ((CAUSAL && j == n_kv - 1) || kv0 + kTileRows > N) {
+      if ((CAUSAL && j == nx - 1) || kv0 + kTileRows > N) {
         int lim = N - kv0;                              // keys >= N do not exist
         if (CAUSAL) lim = min(lim, q_row - kv0 + 1);    // key j visible iff j <= query
 #pragma unroll
@@ -226,62 +262,54 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e) mx = fmaxf(mx, s[c][e]);
-      const float m_new = fmaxf(m, mx * scale_log2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float m_tile = mx * scale_log2;
+      const bool grow = m_tile > m + kRescaleThreshold;  // always true on the first tile
+      const float m_use = grow ? m_tile : m;
+      const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
+
       float rs = 0.f;
+      uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p = ex2_approx(fmaf(s[c][e], scale_log2, -m_use));
-          s[c][e] = p;
-          rs += p;
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2_approx(fmaf(s[c][e], scale_log2, -m_use));
+          const float p1 = ex2_approx(fmaf(s[c][e + 1], scale_log2, -m_use));
+          rs += p0 + p1;
+          pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
         }
-      const float alpha = ex2_approx(m - m_use);
 
-      if (j >= 1) {
-        // O holds sum_{t<j} P_t V_t relative to the old max: rescale it
-        // before P_j V_j is accumulated (only when some row's max grew).
-        if (!(ok = mbar_wait(&bars[kBarPVDone], (j - 1) & 1, status))) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          if constexpr (D >= 32) {
+      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+        if constexpr (D >= 32) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              float o[32];
-              tmem_ld32(tmem_O + lane_base + c * 32, o);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= alpha;
-              tmem_st32(tmem_O + lane_base + c * 32, o);
-            }
-          } else {
-            float o[16];
-            tmem_ld16(tmem_O + lane_base, o);
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tO + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] *= alpha;
-            tmem_st16(tmem_O + lane_base, o);
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tO + c * 32, o);
           }
-          tmem_wait_st();
+        } else {
+          float o[16];
+          tmem_ld16(tO, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] *= alpha;
+          tmem_st16(tO, o);
         }
       }
-      // P (bf16) -> shared memory, K-major 128B-swizzled for the PV MMA.
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        const float* v = &s[c16 >> 2][(c16 & 3) * 8];
-        store_square_chunk(sP, r, c16, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-      }
-      fence_proxy_async_smem();
+      tmem_st32u(tS, pk);
+      tmem_st32u(tS + 32, pk + 32);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarPFull]);
+      if (lane == 0) mbar_arrive(&bars[kBarPFull + x]);
       l = l * alpha + rs;
-      m = m_new;
+      m = m_use;
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(&bars[kBarPVDone], (n_kv - 1) & 1, status)) {
+    if (nx > 0 && ok && mbar_wait(&bars[kBarPVDone + x], (nx - 1) & 1, status)) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = q_row < N;
@@ -290,7 +318,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tmem_ld32(tmem_O + lane_base + c * 32, o);
+          tmem_ld32(tO + c * 32, o);
           tmem_wait_ld();
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -304,7 +332,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       } else {
         float o[16];
-        tmem_ld16(tmem_O + lane_base, o);
+        tmem_ld16(tO, o);
         tmem_wait_ld();
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow);
@@ -323,7 +351,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -331,13 +359,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 template <int D, bool CAUSAL>
 int launch_fwd_t(const TmapSet& tm, void* o, float* lse, int BH, int N, float scale, cudaStream_t stream) {
-  using L = FwdSmem<D>;
+  using C = FwdCfg<D>;
   auto kern = fa2_fwd_kernel<D, CAUSAL>;
-  if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), L::kBytes)) return rc;
-  const int num_q_tiles = (N + kTileRows - 1) / kTileRows;
-  const dim3 grid(static_cast<unsigned>(num_q_tiles) * static_cast<unsigned>(BH));
+  if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
+  const int num_tiles = (N + kTileRows - 1) / kTileRows;
+  const int num_pairs = (num_tiles + 1) / 2;
+  const dim3 grid(static_cast<unsigned>(num_pairs) * static_cast<unsigned>(BH));
   const float scale_log2 = scale * 1.44269504088896341f;
-  kern<<<grid, kFwdThreads, L::kBytes, stream>>>(tm.q, tm.k, tm.v, static_cast<__nv_bfloat16*>(o), lse, BH, N,
+  kern<<<grid, kFwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, static_cast<__nv_bfloat16*>(o), lse, BH, N,
                                                   scale_log2);
   return static_cast<int>(cudaGetLastError());
 }
