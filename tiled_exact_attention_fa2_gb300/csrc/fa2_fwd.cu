@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tS = tmem + lane_base + (x ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_base + (x ? C::kColO1 : C::kColO0);
     float m = -INFINITY;  // max used for P, log2 units (scores * scale * log2 e)
-    float l = 0.f;        // running sum of 2^(x - m)
+    float l = 0.f;        // running sum of 2^(x - m) in fp32 (gives LSE)
+    float lr = 0.f;       // running sum of the bf16-rounded weights the PV MMA uses (normalises O)
     bool ok = true;
 #pragma unroll 1
     for (int j = 0; j < nx; ++j) {
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float m_use = grow ? m_tile : m;
       const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
 
-      float rs = 0.f;
+      float rs = 0.f, rsr = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -276,7 +277,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float p0 = ex2_approx(fmaf(s[c][e], scale_log2, -m_use));
           const float p1 = ex2_approx(fmaf(s[c][e + 1], scale_log2, -m_use));
           rs += p0 + p1;
-          pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+          const uint32_t w = pack_bf16x2(p0, p1);
+          const float2 pr = unpack_bf16x2(w);
+          rsr += pr.x + pr.y;
+          pk[c * 16 + e / 2] = w;
         }
 
       if (j >= 1 && __any_sync(0xffffffffu, grow)) {
@@ -306,12 +310,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarPFull + x]);
       l = l * alpha + rs;
+      lr = lr * alpha + rsr;
       m = m_use;
     }
     // ------------------------------------------------------------ epilogue
     if (nx > 0 && ok && mbar_wait(&bars[kBarPVDone + x], (nx - 1) & 1, status)) {
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      // O = sum_j bf16(p_j) V_j / sum_j bf16(p_j): the weights' bf16 rounding
+      // cancels in the ratio (the dominant weight need not be 1 under the
+      // lazy max).  LSE uses the fp32 sum.
+      const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
       const bool valid = q_row < N;
       __nv_bfloat16* orow = out_o + (static_cast<size_t>(bh) * N + (valid ? q_row : 0)) * D;
       if constexpr (D >= 32) {
