@@ -69,7 +69,7 @@ enum BwdBar {
   kBarDqDrained = 16,  // dQ_i read out of TMEM (4 warp arrivals)
   kBarAccFull = 17,  // dK, dV complete
   kBarDrain = 18,
-  kBarRowStats = 19,  // +buffer (2): LSE_i / D_i staged in shared memory (128 arrivals)
+  kBarRowStats = 19,  // +buffer (2): LSE_i / D_i staged in shared memory (4 warp arrivals)
   kNumBwdBars = 21,
 };
 
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars[kBarQEmpty + s], 1);
       mbar_init(&bars[kBarDoFull + s], 1);
       mbar_init(&bars[kBarDoEmpty + s], 1);
-      mbar_init(&bars[kBarRowStats + s], 128);
+      mbar_init(&bars[kBarRowStats + s], 4);
     }
     mbar_init(&bars[kBarSFull], 1);
     mbar_init(&bars[kBarDpFull], 1);
@@ -357,9 +357,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       sLse[b * 128 + t] = nxt_lse;
       sDv[b * 128 + t] = nxt_d;
       if (it + 1 < n_q) load_stats(it + 1, nxt_lse, nxt_d);
-      // Every compute thread has staged its entry; a buffer is rewritten two
+      // Every compute thread has staged its entry (one arrival per warp after
+      // __syncwarp orders the lanes' stores); a buffer is rewritten two
       // iterations later, after all four warps have passed the dS hand-off.
-      mbar_arrive(&bars[kBarRowStats + b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarRowStats + b]);
       if (!(ok = mbar_wait(&bars[kBarRowStats + b], (it >> 1) & 1, status))) break;
       const float* lse2 = sLse + b * 128;
       const float* dvec = sDv + b * 128;

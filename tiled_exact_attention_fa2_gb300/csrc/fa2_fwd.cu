@@ -258,17 +258,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (c * 32 + e >= lim) s[c][e] = -INFINITY;
       }
-      float mx = -INFINITY;
+      // Row max as a tree (8 independent chains), not one 128-long chain.
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(s[0][k], s[0][k + 8]);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, s[c][e]);
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], fmaxf(s[0][k + 16], s[0][k + 24]));
+#pragma unroll
+      for (int c = 1; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mx8[k] = fmaxf(mx8[k], fmaxf(fmaxf(s[c][k], s[c][k + 8]), fmaxf(s[c][k + 16], s[c][k + 24])));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_tile = mx * scale_log2;
       const bool grow = m_tile > m + kRescaleThreshold;  // always true on the first tile
       const float m_use = grow ? m_tile : m;
       const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
 
-      float rs = 0.f, rsr = 0.f;
+      // Row sums in 4 independent partial accumulators each.
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f}, rsr4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -276,12 +285,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int e = 0; e < 32; e += 2) {
           const float p0 = ex2_approx(fmaf(s[c][e], scale_log2, -m_use));
           const float p1 = ex2_approx(fmaf(s[c][e + 1], scale_log2, -m_use));
-          rs += p0 + p1;
+          rs4[(e >> 1) & 3] += p0 + p1;
           const uint32_t w = pack_bf16x2(p0, p1);
           const float2 pr = unpack_bf16x2(w);
-          rsr += pr.x + pr.y;
+          rsr4[(e >> 1) & 3] += pr.x + pr.y;
           pk[c * 16 + e / 2] = w;
         }
+      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+      const float rsr = (rsr4[0] + rsr4[1]) + (rsr4[2] + rsr4[3]);
 
       if (j >= 1 && __any_sync(0xffffffffu, grow)) {
         if constexpr (D >= 32) {
