@@ -54,7 +54,8 @@ typedef enum {
   FA2_ERR_ALLOC = 6,     /* stream-ordered workspace allocation failed      */
   FA2_ERR_CUDA = 7,      /* a CUDA runtime / driver call or launch failed   */
   FA2_ERR_WORKSPACE = 8, /* caller workspace NULL, too small or misaligned  */
-  FA2_ERR_ALIAS = 9      /* an output overlaps an input or another output   */
+  FA2_ERR_ALIAS = 9,     /* an output overlaps an input or another output   */
+  FA2_ERR_SCRATCH_CAPACITY = 10 /* fa2_bwd_noalloc: problem exceeds its fixed scratch */
 } fa2_status;
 
 /*
@@ -112,6 +113,30 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
                  float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                  void* stream);
 int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale, void* stream);
+
+/*
+ * fa2_bwd without any device allocation.  The pages describe no such call; it
+ * exists for callers that may not allocate device memory themselves (a host
+ * framework whose allocator owns all GPU memory, a plugin handed fixed
+ * buffers, a latency-critical loop that cannot risk an allocation).  Same
+ * arguments, results and errors as fa2_bwd; the backward scratch (D and the
+ * fp32 dQ accumulator) lives in one statically allocated device array of
+ * fa2_noalloc_scratch_capacity() bytes (64 MiB) that every GPU loading this
+ * library holds until the process exits.  Problems needing more scratch than
+ * that (fa2_bwd_workspace_bytes) return FA2_ERR_SCRATCH_CAPACITY before
+ * anything is enqueued.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, once per device, with that device
+ * current), so make that first call before any stream capture.  Every call
+ * shares the array: calls whose GPU work overlaps in time on one device race
+ * and give wrong results.  Each call zeroes what must start at zero, so
+ * nothing carries over between calls.
+ */
+int fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                    void* stream);
+
+/* Bytes of the fixed scratch array fa2_bwd_noalloc uses. */
+size_t fa2_noalloc_scratch_capacity(void);
 
 /* Static description of a status code (never NULL). */
 const char* fa2_status_string(int status);

@@ -22,7 +22,7 @@ from . import _build
 __all__ = [
     "FA2Error", "load_library", "fa2_fwd", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
     "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
-    "fa2_bwd_stages",
+    "fa2_bwd_stages", "fa2_bwd_noalloc",
     "FA2_OK",
 ]
 
@@ -46,6 +46,8 @@ _SIGNATURES = {
     "fa2_bwd_main": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa2_last_error_detail": (ctypes.c_char_p, []),
+    "fa2_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_noalloc_scratch_capacity": (_sz, []),
 }
 
 
@@ -182,6 +184,21 @@ def fa2_bwd_ws(q, k, v, o, dO, lse, workspace: torch.Tensor, dq=None, dk=None, d
                         _stream(stream, q.device))
     if rc != FA2_OK:
         raise FA2Error("fa2_bwd_ws", rc)
+    return dq, dk, dv
+
+
+def fa2_bwd_noalloc(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optional[float] = None,
+                    causal: bool = True, stream=None):
+    """fa2_bwd for callers that cannot allocate device memory: the library's
+    scratch comes from a fixed 64 MiB device array shared by all calls (see
+    include/fa2.h); concurrent calls on one device race."""
+    lib = load_library()
+    (B, H, N, d), dq, dk, dv = _bwd_common(q, k, v, o, dO, lse, dq, dk, dv)
+    rc = lib.fa2_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                             _scale(scale, d), 1 if causal else 0, _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_noalloc", rc)
     return dq, dk, dv
 
 

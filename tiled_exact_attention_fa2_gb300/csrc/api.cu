@@ -289,6 +289,7 @@ const char* fa2_status_string(int status) {
     case FA2_ERR_CUDA: return "CUDA call or kernel launch failed";
     case FA2_ERR_WORKSPACE: return "workspace NULL, too small or not 256-byte aligned";
     case FA2_ERR_ALIAS: return "an output overlaps an input or another output";
+    case FA2_ERR_SCRATCH_CAPACITY: return "problem needs more scratch than fa2_bwd_noalloc's fixed array holds";
     default: return "unknown fa2 status";
   }
 }
