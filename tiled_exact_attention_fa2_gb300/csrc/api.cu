@@ -67,6 +67,23 @@ int cuda_fail(int cuda_code, const char* where) {
   return FA2_ERR_CUDA;
 }
 
+// [B*H, N, d] fp32 view of the dQ accumulator for TMA reduce-add, box =
+// [1, 128 rows, min(d, 32) columns], swizzle = box row width.
+bool make_tmap_f32(CUtensorMap* out, const void* base, int BH, int N, int d) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const int box_cols = d >= 32 ? 32 : d;
+  const CUtensorMapSwizzle swz = d >= 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), kRowsPerTile, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Range {
@@ -121,9 +138,10 @@ int validate_bwd(const void* q, const void* k, const void* v, const void* o, con
   return FA2_OK;
 }
 
-int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const void* dO, int BH, int N, int d) {
+int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const void* dO, const float* dq_acc, int BH,
+               int N, int d) {
   return (make_tmap(&tm->q, q, BH, N, d) && make_tmap(&tm->k, k, BH, N, d) && make_tmap(&tm->v, v, BH, N, d) &&
-          make_tmap(&tm->dO, dO, BH, N, d))
+          make_tmap(&tm->dO, dO, BH, N, d) && make_tmap_f32(&tm->dqacc, dq_acc, BH, N, d))
              ? FA2_OK
              : cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
 }
@@ -131,13 +149,13 @@ int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const v
 int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
             void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* ws, cudaStream_t st) {
   const int BH = B * H;
-  TmapSet tm;
-  if (int rc = make_tmaps(&tm, q, k, v, dO, BH, N, d)) return rc;
   const size_t rows = static_cast<size_t>(BH) * N;
   float* Dvec = static_cast<float*>(ws);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(rows * sizeof(float)));
+  TmapSet tm;
+  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, BH, N, d)) return rc;
   if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, BH, N, d, st)) return cuda_fail(e, "bwd preprocess launch");
-  if (int e = launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, BH, N, d, scale, causal != 0, st))
+  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, BH, N, d, scale, causal != 0, st))
     return cuda_fail(e, "bwd main launch");
   if (int e = launch_bwd_dq_convert(dq_acc, dq, BH, N, d, scale, st)) return cuda_fail(e, "dq convert launch");
   return FA2_OK;
@@ -258,8 +276,8 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
       if (overlap(outs[a], outs[b])) return FA2_ERR_ALIAS;
   }
   TmapSet tm;
-  if (int rc = make_tmaps(&tm, q, k, v, dO, B * H, N, d)) return rc;
-  if (int e = launch_bwd_main(tm, lse, Dvec, dq_acc, dk, dv, B * H, N, d, scale, causal != 0,
+  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, B * H, N, d)) return rc;
+  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, B * H, N, d, scale, causal != 0,
                               static_cast<cudaStream_t>(stream)))
     return cuda_fail(e, "bwd main launch");
   return FA2_OK;

@@ -61,8 +61,8 @@ enum BwdBar {
   kBarDoEmpty = 7,   // +stage
   kBarSFull = 9,     // S^T in TMEM
   kBarDpFull = 10,   // dP^T in TMEM
-  kBarPFull = 11,    // P^T in shared memory (4 warp arrivals)
-  kBarPtEmpty = 12,  // P^T shared memory free again (dV MMA done)
+  kBarPFull = 11,    // P^T in TMEM (4 warp arrivals)
+  kBarDvDone = 12,   // dV(i) MMA done: the P^T columns may be overwritten by S^T(i+1)
   kBarDsFull = 13,   // dS^T in shared memory, dP^T read out (4 warp arrivals)
   kBarDsEmpty = 14,  // dS^T shared memory free again (dK, dQ MMAs done)
   kBarDqFull = 15,   // dQ_i in TMEM
@@ -70,7 +70,9 @@ enum BwdBar {
   kBarAccFull = 17,  // dK, dV complete
   kBarDrain = 18,
   kBarRowStats = 19,  // +buffer (2): LSE_i / D_i staged in shared memory (4 warp arrivals)
-  kNumBwdBars = 21,
+  kBarStageFull = 21,  // +buffer (2): dQ chunk staged in shared memory (4 warp arrivals)
+  kBarStageFree = 23,  // +buffer (2): the TMA reduce of that chunk has read it
+  kNumBwdBars = 25,
 };
 
 template <int D>
@@ -78,8 +80,9 @@ struct BwdCfg {
   using T = HeadDim<D>;
   static constexpr int kQStages = 2;
   static constexpr int kDoStages = D == 128 ? 1 : 2;  // shared memory is full at D = 128
-  // TMEM: S^T [0,128), dP^T [128,256) (dQ_i reuses these columns once dS^T
-  // is formed), dV and dK after them on 32-column boundaries.
+  // TMEM: S^T [0,128) (P^T, as bf16 pairs, overwrites its first 64 columns),
+  // dP^T [128,256) (dQ_i reuses these columns once dS^T is formed), dV and dK
+  // after them on 32-column boundaries.
   static constexpr int kCols = D < 32 ? 32 : D;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 256 + kCols;
   // shared memory
@@ -87,9 +90,15 @@ struct BwdCfg {
   static constexpr int kV = kK + T::kTileBytes;
   static constexpr int kQ = kV + T::kTileBytes;
   static constexpr int kDo = kQ + kQStages * T::kTileBytes;
-  static constexpr int kPt = kDo + kDoStages * T::kTileBytes;
-  static constexpr int kDSt = kPt + Square::kTileBytes;
-  static constexpr int kLse = kDSt + Square::kTileBytes;  // [2][128] fp32, pre-multiplied by log2 e
+  // dQ partials leave through two staging buffers of 128 rows x kChunk fp32
+  // columns (128B-swizzled, or 64B for D = 16), reduced into the fp32
+  // accumulator by TMA.
+  static constexpr int kChunk = D < 32 ? D : 32;
+  static constexpr int kChunks = D / kChunk;
+  static constexpr int kStageBytes = 128 * kChunk * 4;
+  static constexpr int kDSt = kDo + kDoStages * T::kTileBytes;
+  static constexpr int kStage = kDSt + Square::kTileBytes;
+  static constexpr int kLse = kStage + 2 * kStageBytes;  // [2][128] fp32, pre-multiplied by log2 e
   static constexpr int kDv = kLse + 2 * 128 * 4;          // [2][128] fp32
   static constexpr int kBars = kDv + 2 * 128 * 4;
   static constexpr int kTmemSlot = kBars + kNumBwdBars * 8;
@@ -157,9 +166,9 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const float* __restrict__ lse, const float* __restrict__ Dvec, float* __restrict__ dq_acc,
-                   __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int N, float scale,
-                   float scale_log2) {
+                   const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse,
+                   const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                   int BH, int N, float scale, float scale_log2) {
   using T = HeadDim<D>;
   using C = BwdCfg<D>;
   constexpr int SQ = C::kQStages, SD = C::kDoStages;
@@ -178,7 +187,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sV = smem_u32(smem + C::kV);
   const uint32_t sQ = smem_u32(smem + C::kQ);
   const uint32_t sDo = smem_u32(smem + C::kDo);
-  const uint32_t sPt = smem_u32(smem + C::kPt);
   const uint32_t sDSt = smem_u32(smem + C::kDSt);
 
   const int warp = warp_id();
@@ -202,7 +210,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars[kBarSFull], 1);
     mbar_init(&bars[kBarDpFull], 1);
     mbar_init(&bars[kBarPFull], 4);
-    mbar_init(&bars[kBarPtEmpty], 1);
+    mbar_init(&bars[kBarDvDone], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kBarStageFull + s], 4);
+      mbar_init(&bars[kBarStageFree + s], 1);
+    }
     mbar_init(&bars[kBarDsFull], 4);
     mbar_init(&bars[kBarDsEmpty], 1);
     mbar_init(&bars[kBarDqFull], 1);
@@ -270,7 +282,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, true, true);      // dS x K
       const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ,
                      tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
-      const uint32_t sK0 = sK, sV0 = sV, sPt0 = sPt, sDSt0 = sDSt, sQ0 = sQ, sDo0 = sDo;
+      const uint32_t sK0 = sK, sV0 = sV, sDSt0 = sDSt, sQ0 = sQ, sDo0 = sDo;
       // Issue order per query tile i (S^T(i) is issued one tile ahead so the
       // compute warps find it ready when they finish dS(i-1)):
       //   dP^T(i), dV(i), S^T(i+1), dQ(i), dK(i)
@@ -294,8 +306,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int qs = it % SQ, ds = it % SD, du = it / SD;
         // Recompute the operand descriptors every iteration (a few integer
         // ops) instead of keeping ~40 hoisted 64-bit descriptors live.
-        uint32_t sK = sK0, sV = sV0, sPt = sPt0, sDSt = sDSt0, sQ = sQ0, sDo = sDo0;
-        opaque(sK); opaque(sV); opaque(sPt); opaque(sDSt); opaque(sQ); opaque(sDo);
+        uint32_t sK = sK0, sV = sV0, sDSt = sDSt0, sQ = sQ0, sDo = sDo0;
+        opaque(sK); opaque(sV); opaque(sDSt); opaque(sQ); opaque(sDo);
         const uint32_t q_s = sQ + qs * T::kTileBytes, do_s = sDo + ds * T::kTileBytes;
         // dP^T = V dO_i^T into the columns dQ(i-1) occupied.
         if (!(ok = mbar_wait(&bars[kBarDoFull + ds], du & 1, status))) break;
@@ -305,17 +317,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ss(tDP, T::kmajor_desc(sV, kk), T::kmajor_desc(do_s, kk), kIdSq, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarDpFull]);
-        // dV += P^T dO_i
+        // dV += P^T dO_i, P^T read from the first 64 columns of S^T (TMEM).
         if (!(ok = mbar_wait(&bars[kBarPFull], it & 1, status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ss(tDV, Square::kmajor_desc(sPt, kk), T::mnmajor_desc(do_s, kk), kIdKV,
-                      (it > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tDV, tS + kk * 8, T::mnmajor_desc(do_s, kk), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarDoEmpty + ds]);
-        mma_commit(&bars[kBarPtEmpty]);
-        // S^T(i+1): the compute warps have read S^T(i) (they signalled P(i)).
-        if (it + 1 < n_q && !(ok = issue_s(it + 1))) break;
+        mma_commit(&bars[kBarDvDone]);
+        // S^T(i+1) overwrites the P^T columns dV(i) reads: wait for dV(i).
+        if (it + 1 < n_q) {
+          if (!(ok = mbar_wait(&bars[kBarDvDone], it & 1, status))) break;
+          if (!(ok = issue_s(it + 1))) break;
+        }
         // dQ_i = dS K (dS read as the MN-major view of dS^T); dK += dS^T Q_i
         if (!(ok = mbar_wait(&bars[kBarDsFull], it & 1, status))) break;
         tc_fence_after();
@@ -386,11 +400,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
         }
       }
-      if (it >= 1 && !(ok = mbar_wait(&bars[kBarPtEmpty], (it - 1) & 1, status))) break;
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16)
-        store_square_chunk(sPt, t, c16, pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      fence_proxy_async_smem();
+      // P^T (bf16 pairs) over the first 64 S^T columns, all of which are read.
+      tmem_st32u(tmem + lane_base + C::kColS, pk);
+      tmem_st32u(tmem + lane_base + C::kColS + 32, pk + 32);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarPFull]);
@@ -426,44 +439,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ dQ drain + epilogue warps
     const int t = threadIdx.x - 128;  // TMEM lane: query row q0 + t (dQ), key row kv0 + t (dK, dV)
     const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    // dQ_i leaves TMEM in one go (so its columns are released early), then
+    // goes out in kChunk-column pieces: each is written to a swizzled staging
+    // buffer and reduce-added (fp32) into dQacc by one TMA bulk tensor op,
+    // issued by lane 0 of warp 4.  Rows past N fall outside the tensor map and
+    // are dropped by TMA.
+    const bool issuer = warp == 4 && lane == 0;
+    const uint32_t sStage = smem_u32(smem + C::kStage);
     bool ok = true;
 #pragma unroll 1
     for (int it = 0; it < n_q; ++it) {
-      const int q = (i_begin + it) * kTileRows + t;
+      const int q0 = (i_begin + it) * kTileRows;
       if (!(ok = mbar_wait(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
-      float* dst = dq_acc + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
+      float g[D];
       if constexpr (D >= 32) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float g[32];
-          tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
-          tmem_wait_ld();
-          if (c == D / 32 - 1) {  // every dQ column is in registers: release the TMEM columns early
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
-          }
-          if (q < N) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
-          }
-        }
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, *reinterpret_cast<float(*)[32]>(g + c * 32));
       } else {
-        float g[16];
-        tmem_ld16(tmem + lane_base + C::kColDQ, g);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
-        if (q < N) {
-#pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + e), make_float4(g[e], g[e + 1], g[e + 2], g[e + 3]));
-        }
+        tmem_ld16(tmem + lane_base + C::kColDQ, *reinterpret_cast<float(*)[16]>(g));
       }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        const int gi = it * C::kChunks + c, bsel = gi & 1, u = gi >> 1;
+        if (gi >= 2 && !(ok = mbar_wait(&bars[kBarStageFree + bsel], (u - 1) & 1, status))) break;
+        const uint32_t sb = sStage + bsel * C::kStageBytes;
+#pragma unroll
+        for (int j = 0; j < C::kChunk / 4; ++j) {
+          const float* v4 = g + c * C::kChunk + 4 * j;
+          st_shared_v4(sb + swizzle_offset<C::kChunk * 4>(t, j), __float_as_uint(v4[0]), __float_as_uint(v4[1]),
+                       __float_as_uint(v4[2]), __float_as_uint(v4[3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarStageFull + bsel]);
+        if (issuer) {
+          if ((ok = mbar_wait(&bars[kBarStageFull + bsel], u & 1, status))) {
+            tma_reduce_add_3d(&tm_dqacc, sb, c * C::kChunk, q0, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(&bars[kBarStageFree + bsel]);
+          }
+        }
+        __syncwarp();
+        if (!ok) break;
+      }
+      if (!ok) break;
     }
+    if (issuer) bulk_wait_group0();  // every reduce has landed before the CTA exits
     // ------------------------------------------------------------ epilogue: dV, dK * scale -> bf16
     if (ok && mbar_wait(&bars[kBarAccFull], 0, status)) {
       tc_fence_after();
@@ -527,14 +554,14 @@ int launch_preprocess_t(const void* o, const void* dO, float* Dvec, float* dq_ac
 }
 
 template <int D, bool CAUSAL>
-int launch_bwd_main_t(const TmapSet& tm, const float* lse, const float* Dvec, float* dq_acc, void* dk, void* dv,
-                      int BH, int N, float scale, cudaStream_t stream) {
+int launch_bwd_main_t(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N,
+                      float scale, cudaStream_t stream) {
   using C = BwdCfg<D>;
   auto kern = fa2_bwd_kernel<D, CAUSAL>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_tiles = (N + kTileRows - 1) / kTileRows;
   const dim3 grid(static_cast<unsigned>(num_tiles) * static_cast<unsigned>(BH));
-  kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, lse, Dvec, dq_acc,
+  kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, tm.dqacc, lse, Dvec,
                                                   static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
                                                   BH, N, scale, scale * kLog2e);
   return static_cast<int>(cudaGetLastError());
@@ -564,17 +591,17 @@ int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_
   }
 }
 
-int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, float* dq_acc, void* dk, void* dv, int BH,
-                    int N, int d, float scale, bool causal, cudaStream_t stream) {
+int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N, int d,
+                    float scale, bool causal, cudaStream_t stream) {
   switch (d) {
-    case 16: return causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                           : launch_bwd_main_t<16, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
-    case 32: return causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                           : launch_bwd_main_t<32, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
-    case 64: return causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                           : launch_bwd_main_t<64, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
-    case 128: return causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream)
-                            : launch_bwd_main_t<128, false>(tm, lse, Dvec, dq_acc, dk, dv, BH, N, scale, stream);
+    case 16: return causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
+                           : launch_bwd_main_t<16, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
+    case 32: return causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
+                           : launch_bwd_main_t<32, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
+    case 64: return causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
+                           : launch_bwd_main_t<64, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
+    case 128: return causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
+                            : launch_bwd_main_t<128, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

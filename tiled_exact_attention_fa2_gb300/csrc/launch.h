@@ -6,9 +6,10 @@
 
 namespace fa2 {
 
-// TMA descriptors of the [B*H, N, d] bf16 views of the operands.
+// TMA descriptors of the [B*H, N, d] views of the operands (bf16) and of
+// the fp32 dQ accumulator.
 struct TmapSet {
-  CUtensorMap q, k, v, dO;
+  CUtensorMap q, k, v, dO, dqacc;
 };
 
 // Every function below returns 0 or the cudaError_t value of the failure.
@@ -20,8 +21,8 @@ int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, flo
                cudaStream_t stream);
 int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int BH, int N, int d,
                           cudaStream_t stream);
-int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, float* dq_acc, void* dk, void* dv, int BH,
-                    int N, int d, float scale, bool causal, cudaStream_t stream);
+int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N, int d,
+                    float scale, bool causal, cudaStream_t stream);
 int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, float scale, cudaStream_t stream);
 
 int read_fwd_status(int* value, bool reset);

@@ -39,6 +39,16 @@ struct HeadDim {
   }
 };
 
+// Byte offset of 16-byte chunk j of row `row` in a tile with ROW_BYTES-byte
+// rows (32, 64 or 128) swizzled the way TMA's 32B/64B/128B swizzle lays it
+// out: address bits [4,7) XOR bits [7,10) (masked to the swizzle width).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t swizzle_offset(uint32_t row, uint32_t j) {
+  const uint32_t off = row * ROW_BYTES + j * 16;
+  constexpr uint32_t mask = ROW_BYTES == 128 ? 7u : (ROW_BYTES == 64 ? 3u : 1u);
+  return off ^ (((off >> 7) & mask) << 4);
+}
+
 // 128 x 128 bf16 tile written by threads (P, dS): same layout as HeadDim<128>.
 using Square = HeadDim<128>;
 
