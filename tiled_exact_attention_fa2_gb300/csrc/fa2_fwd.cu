@@ -17,7 +17,10 @@
 //   warps 0-3  softmax of tile A   (thread t owns row t = TMEM lane t)
 //   warps 4-7  softmax of tile B
 //   warp  8    TMA producer: Q_A, Q_B once, then K_j / V_j into 2-stage rings
-//   warp  9    MMA issuer (one thread) + TMEM owner
+//   warp  9    MMA issuer for tile A (one thread) + TMEM owner
+//   warp 10    MMA issuer for tile B (one thread)
+// One issuer per tile, so that waiting on one tile's MMA never delays the
+// other tile's; K/V stages are released once both issuers are done with them.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A and O_B after them.  The
 // softmax overwrites the first 64 columns of S_X with P_X (bf16 pairs) and
 // O_X += P_X V_j reads P_X straight from TMEM (A operand in TMEM), so P never
@@ -39,7 +42,7 @@ __device__ int g_fwd_status;
 
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
@@ -52,8 +55,8 @@ enum FwdBar {
   kBarSFull = 9,    // +tile (A, B)
   kBarPFull = 11,   // +tile, 4 warp arrivals
   kBarPVDone = 13,  // +tile
-  kBarDrain = 15,
-  kNumFwdBars = 16,
+  kBarDrain = 15,   // +tile
+  kNumFwdBars = 17,
 };
 
 template <int D>
@@ -104,14 +107,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(&bars[kBarQ], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kBarKFull + s], 1);
-      mbar_init(&bars[kBarKEmpty + s], 1);
+      mbar_init(&bars[kBarKEmpty + s], 2);
       mbar_init(&bars[kBarVFull + s], 1);
-      mbar_init(&bars[kBarVEmpty + s], 1);
+      mbar_init(&bars[kBarVEmpty + s], 2);
       mbar_init(&bars[kBarSFull + s], 1);
       mbar_init(&bars[kBarPFull + s], 4);
       mbar_init(&bars[kBarPVDone + s], 1);
+      mbar_init(&bars[kBarDrain + s], 1);
     }
-    mbar_init(&bars[kBarDrain], 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -159,70 +162,74 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (last_v0 >= 0) mbar_wait(&bars[kBarVFull + 0], (last_v0 >> 1) & 1, status);
       if (last_v1 >= 0) mbar_wait(&bars[kBarVFull + 1], (last_v1 >> 1) & 1, status);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuer of tile x
     if (lane == 0) {
+      const int x = warp - 9;
+      const int nx = x == 0 ? nA : nB;
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q (K-major) x K (K-major)
       constexpr uint32_t kIdescO = make_idesc_bf16(128, D, false, true);     // P (TMEM) x V (MN-major)
       const uint32_t sQ0 = smem_u32(smem + C::kQ), sK0 = smem_u32(smem + C::kK), sV0 = smem_u32(smem + C::kV);
+      const uint32_t tSx = tmem + (x ? C::kColS1 : C::kColS0), tOx = tmem + (x ? C::kColO1 : C::kColO0);
       // S_x(j) = Q_x K_j^T into TMEM S_x.
-      auto issue_s = [&](int x, int j) {
+      auto issue_s = [&](int j) {
         uint32_t sQ = sQ0, sK = sK0;
         opaque(sQ);
         opaque(sK);
         const uint32_t qb = sQ + x * T::kTileBytes, kb = sK + (j & 1) * T::kTileBytes;
-        const uint32_t d_tmem = tmem + (x ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(d_tmem, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tSx, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarSFull + x]);
+        mma_commit(&bars[kBarKEmpty + (j & 1)]);
       };
       // O_x += P_x V_j with P_x read from the first 64 columns of S_x.
-      auto issue_pv = [&](int x, int j) {
+      auto issue_pv = [&](int j) {
         uint32_t sV = sV0;
         opaque(sV);
         const uint32_t vb = sV + (j & 1) * T::kTileBytes;
-        const uint32_t a_tmem = tmem + (x ? C::kColS1 : C::kColS0);
-        const uint32_t d_tmem = tmem + (x ? C::kColO1 : C::kColO0);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ts(d_tmem, a_tmem + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tOx, tSx + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarPVDone + x]);
+        mma_commit(&bars[kBarVEmpty + (j & 1)]);
       };
-      bool ok = mbar_wait(&bars[kBarQ], 0, status) && mbar_wait(&bars[kBarKFull + 0], 0, status);
-      if (ok) {
-        tc_fence_after();
-        if (nA > 0) issue_s(0, 0);
-        if (nB > 0) issue_s(1, 0);
-        mma_commit(&bars[kBarKEmpty + 0]);
-      }
-#pragma unroll 1
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j & 1;
-        const bool nextk = j + 1 < n_kv;
-        if (!(ok = mbar_wait(&bars[kBarVFull + st], (j >> 1) & 1, status))) break;
-        if (nextk && !(ok = mbar_wait(&bars[kBarKFull + (st ^ 1)], ((j + 1) >> 1) & 1, status))) break;
-#pragma unroll 1
-        for (int x = 0; x < 2; ++x) {
-          const int nx = x == 0 ? nA : nB;
-          if (j >= nx) continue;
-          if (!(ok = mbar_wait(&bars[kBarPFull + x], j & 1, status))) break;
+      bool ok = true;
+      if (nx > 0) {
+        ok = mbar_wait(&bars[kBarQ], 0, status) && mbar_wait(&bars[kBarKFull + 0], 0, status);
+        if (ok) {
           tc_fence_after();
-          issue_pv(x, j);
-          if (j + 1 < nx) {
-            // S_x(j+1) overwrites the P_x columns the MMA above reads.
-            if (!(ok = mbar_wait(&bars[kBarPVDone + x], j & 1, status))) break;
-            tc_fence_after();
-            issue_s(x, j + 1);
-          }
+          issue_s(0);
         }
-        if (!ok) break;
-        mma_commit(&bars[kBarVEmpty + st]);
-        if (nextk) mma_commit(&bars[kBarKEmpty + (st ^ 1)]);
       }
-      // Wait for every MMA issued above before TMEM can be released.
-      mma_commit(&bars[kBarDrain]);
-      mbar_wait(&bars[kBarDrain], 0, status);
+#pragma unroll 1
+      for (int j = 0; ok && j < nx; ++j) {
+        const int st = j & 1;
+        if (!(ok = mbar_wait(&bars[kBarVFull + st], (j >> 1) & 1, status))) break;
+        if (!(ok = mbar_wait(&bars[kBarPFull + x], j & 1, status))) break;
+        tc_fence_after();
+        issue_pv(j);
+        if (j + 1 < nx) {
+          // S_x(j+1) overwrites the P_x columns the MMA above reads.
+          if (!(ok = mbar_wait(&bars[kBarPVDone + x], j & 1, status))) break;
+          if (!(ok = mbar_wait(&bars[kBarKFull + (st ^ 1)], ((j + 1) >> 1) & 1, status))) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+      }
+      // K/V tiles this query tile does not visit: release them once, in
+      // phase order (after the stage's previous use has been released).
+#pragma unroll 1
+      for (int j = nx; ok && j < n_kv; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !(ok = mbar_wait(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status))) break;
+        mbar_arrive(&bars[kBarKEmpty + st]);
+        if (j >= 2 && !(ok = mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status))) break;
+        mbar_arrive(&bars[kBarVEmpty + st]);
+      }
+      // Wait for every MMA this thread issued before TMEM can be released.
+      mma_commit(&bars[kBarDrain + x]);
+      mbar_wait(&bars[kBarDrain + x], 0, status);
     }
   } else {
     // ------------------------------------------------------------ softmax (tile x)
