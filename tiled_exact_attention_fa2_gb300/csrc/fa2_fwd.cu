@@ -26,9 +26,10 @@
 // O_X += P_X V_j reads P_X straight from TMEM (A operand in TMEM), so P never
 // touches shared memory.  S_X(j+1) is issued only after P_X(j) V_j has
 // completed, because it overwrites the columns that MMA reads.
-// The running max is updated lazily: O and l are rescaled only when a row's
-// max grows by more than 8 (log2 units); otherwise the stale max is kept and
-// P = 2^(s - m) stays <= 256, which is exact after the final O / l.
+// O is rescaled in TMEM only when some row of the warp sees its max grow, so
+// every row's largest weight is exactly 1.  The softmax arithmetic runs on
+// packed fp32 pairs (f32x2 FMA/ADD/MUL) and 3-input max to halve its
+// instruction count, which bounds this kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,7 +45,6 @@ namespace {
 
 constexpr int kFwdThreads = 352;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 enum FwdBar {
   kBarQ = 0,
@@ -240,9 +240,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_base + (x ? C::kColO1 : C::kColO0);
-    float m = -INFINITY;  // max used for P, log2 units (scores * scale * log2 e)
-    float l = 0.f;        // running sum of 2^(x - m) in fp32 (gives LSE)
-    float lr = 0.f;       // running sum of the bf16-rounded weights the PV MMA uses (normalises O)
+    float m = -INFINITY;  // running row max, log2 units (scores * scale * log2 e)
+    float l = 0.f;        // running sum of 2^(x - m)
+    const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
 #pragma unroll 1
     for (int j = 0; j < nx; ++j) {
@@ -250,9 +250,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // stable once S_x(j) has landed.
       if (!(ok = mbar_wait(&bars[kBarSFull + x], j & 1, status))) break;
       tc_fence_after();
-      float s[4][32];
+      float s[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + 32 * c));
       tmem_wait_ld();
 
       const int kv0 = j * kTileRows;
@@ -260,48 +260,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int lim = N - kv0;                              // keys >= N do not exist
         if (CAUSAL) lim = min(lim, q_row - kv0 + 1);    // key j visible iff j <= query
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= lim) s[c][e] = -INFINITY;
+        for (int e = 0; e < 128; ++e)
+          if (e >= lim) s[e] = -INFINITY;
       }
-      // Row max as a tree (8 independent chains), not one 128-long chain.
+      // Row max: 8 independent chains of 3-input max.
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(s[0][k], s[0][k + 8]);
+      for (int k = 0; k < 8; ++k) {
+        // chain k covers columns k, k + 8, ..., k + 120
+        float v = fmax3(s[k], s[k + 8], s[k + 16]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], fmaxf(s[0][k + 16], s[0][k + 24]));
-#pragma unroll
-      for (int c = 1; c < 4; ++c)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mx8[k] = fmaxf(mx8[k], fmaxf(fmaxf(s[c][k], s[c][k + 8]), fmaxf(s[c][k + 16], s[c][k + 24])));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_tile = mx * scale_log2;
-      const bool grow = m_tile > m + kRescaleThreshold;  // always true on the first tile
-      const float m_use = grow ? m_tile : m;
-      const float alpha = grow ? ex2_approx(m - m_use) : 1.f;
+        for (int i = 24; i <= 104; i += 16) v = fmax3(v, s[k + i], s[k + i + 8]);
+        mx8[k] = fmaxf(v, s[k + 120]);
+      }
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      const float m_new = fmaxf(m, mx * scale_log2);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const bool grow = m_use > m;  // always true on the first tile
+      const float alpha = ex2_approx(m - m_use);
 
-      // Row sums in 4 independent partial accumulators each.
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f}, rsr4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
+      // P = 2^(s * scale_log2 - m) on packed pairs; 4 independent pair sums.
+      const uint64_t negm2 = f2_pack(-m_use, -m_use);
+      // P goes to TMEM (bf16 pairs over the first 64 S columns, all of which
+      // are already in registers) 16 columns at a time.
+      uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2_approx(fmaf(s[c][e], scale_log2, -m_use));
-          const float p1 = ex2_approx(fmaf(s[c][e + 1], scale_log2, -m_use));
-          rs4[(e >> 1) & 3] += p0 + p1;
-          const uint32_t w = pack_bf16x2(p0, p1);
-          const float2 pr = unpack_bf16x2(w);
-          rsr4[(e >> 1) & 3] += pr.x + pr.y;
-          pk[c * 16 + e / 2] = w;
+        for (int i = 0; i < 16; ++i) {
+          const int e = 32 * c + 2 * i;
+          const float2 xx = f2_unpack(ffma2(f2_pack(s[e], s[e + 1]), scale2, negm2));
+          const float p0 = ex2_approx(xx.x), p1 = ex2_approx(xx.y);
+          acc[i & 3] = fadd2(acc[i & 3], f2_pack(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
         }
-      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-      const float rsr = (rsr4[0] + rsr4[1]) + (rsr4[2] + rsr4[3]);
+        tmem_st16u(tS + 16 * c, pk);
+      }
+      const float2 a01 = f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])));
+      const float rs = a01.x + a01.y;
 
       if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+        const uint64_t alpha2 = f2_pack(alpha, alpha);
         if constexpr (D >= 32) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -309,7 +309,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_ld32(tO + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            for (int e = 0; e < 32; e += 2) {
+              const float2 r = f2_unpack(fmul2(f2_pack(o[e], o[e + 1]), alpha2));
+              o[e] = r.x;
+              o[e + 1] = r.y;
+            }
             tmem_st32(tO + c * 32, o);
           }
         } else {
@@ -321,23 +325,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_st16(tO, o);
         }
       }
-      tmem_st32u(tS, pk);
-      tmem_st32u(tS + 32, pk + 32);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarPFull + x]);
       l = l * alpha + rs;
-      lr = lr * alpha + rsr;
       m = m_use;
     }
     // ------------------------------------------------------------ epilogue
     if (nx > 0 && ok && mbar_wait(&bars[kBarPVDone + x], (nx - 1) & 1, status)) {
       tc_fence_after();
-      // O = sum_j bf16(p_j) V_j / sum_j bf16(p_j): the weights' bf16 rounding
-      // cancels in the ratio (the dominant weight need not be 1 under the
-      // lazy max).  LSE uses the fp32 sum.
-      const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = q_row < N;
       __nv_bfloat16* orow = out_o + (static_cast<size_t>(bh) * N + (valid ? q_row : 0)) * D;
       if constexpr (D >= 32) {
