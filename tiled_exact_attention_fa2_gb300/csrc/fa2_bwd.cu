@@ -69,10 +69,9 @@ enum BwdBar {
   kBarDqDrained = 16,  // dQ_i read out of TMEM (4 warp arrivals)
   kBarAccFull = 17,  // dK, dV complete
   kBarDrain = 18,
-  kBarRowStats = 19,  // +buffer (2): LSE_i / D_i staged in shared memory (4 warp arrivals)
-  kBarStageFull = 21,  // +buffer (2): dQ chunk staged in shared memory (4 warp arrivals)
-  kBarStageFree = 23,  // +buffer (2): the TMA reduce of that chunk has read it
-  kNumBwdBars = 25,
+  kBarStageFull = 19,  // +buffer (2): dQ chunk staged in shared memory (4 warp arrivals)
+  kBarStageFree = 21,  // +buffer (2): the TMA reduce of that chunk has read it
+  kNumBwdBars = 23,
 };
 
 template <int D>
@@ -98,9 +97,10 @@ struct BwdCfg {
   static constexpr int kStageBytes = 128 * kChunk * 4;
   static constexpr int kDSt = kDo + kDoStages * T::kTileBytes;
   static constexpr int kStage = kDSt + Square::kTileBytes;
-  static constexpr int kLse = kStage + 2 * kStageBytes;  // [2][128] fp32, pre-multiplied by log2 e
-  static constexpr int kDv = kLse + 2 * 128 * 4;          // [2][128] fp32
-  static constexpr int kBars = kDv + 2 * 128 * 4;
+  // Per Q stage: -LSE_i * log2 e [128] then -D_i [128] (fp32), written by
+  // the producer warp together with the Q_i tile (same full barrier).
+  static constexpr int kStats = kStage + 2 * kStageBytes;
+  static constexpr int kBars = kStats + kQStages * 256 * 4;
   static constexpr int kTmemSlot = kBars + kNumBwdBars * 8;
   static constexpr int kUsed = kTmemSlot + 16;
   // Request 1 KB of slack to round the base up to 1024 bytes when it fits;
@@ -181,8 +181,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
-  float* sLse = reinterpret_cast<float*>(smem + C::kLse);
-  float* sDv = reinterpret_cast<float*>(smem + C::kDv);
+  float* sStats = reinterpret_cast<float*>(smem + C::kStats);
   const uint32_t sK = smem_u32(smem + C::kK);
   const uint32_t sV = smem_u32(smem + C::kV);
   const uint32_t sQ = smem_u32(smem + C::kQ);
@@ -205,7 +204,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars[kBarQEmpty + s], 1);
       mbar_init(&bars[kBarDoFull + s], 1);
       mbar_init(&bars[kBarDoEmpty + s], 1);
-      mbar_init(&bars[kBarRowStats + s], 4);
     }
     mbar_init(&bars[kBarSFull], 1);
     mbar_init(&bars[kBarDpFull], 1);
@@ -234,46 +232,66 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // Lane 0 issues the TMA loads; all 32 lanes stage -LSE*log2e and -D of
+    // the query tile into the Q stage's stats slot before lane 0 arms the
+    // stage's full barrier (__syncwarp orders the lanes' stores before it).
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      int last_q[2] = {-1, -1}, last_do[2] = {-1, -1};
       mbar_arrive_expect_tx(&bars[kBarKV], 2 * T::kTileBytes);
       for (int b = 0; b < T::kNumBoxes; ++b) {
         tma_load_3d(smem + C::kK + b * T::kBoxBytes, &tm_k, &bars[kBarKV], b * T::kBoxCols, kv0, bh);
         tma_load_3d(smem + C::kV + b * T::kBoxBytes, &tm_v, &bars[kBarKV], b * T::kBoxCols, kv0, bh);
       }
+    }
+    int last_q0 = -1, last_q1 = -1, last_do0 = -1, last_do1 = -1;
+    bool ok = true;
 #pragma unroll 1
-      for (int it = 0; it < n_q; ++it) {
-        const int q0 = (i_begin + it) * kTileRows;
-        {
-          const int st = it % SQ, u = it / SQ;
-          if (it >= SQ && !mbar_wait(&bars[kBarQEmpty + st], (u - 1) & 1, status)) break;
+    for (int it = 0; it < n_q; ++it) {
+      const int q0 = (i_begin + it) * kTileRows;
+      {
+        const int st = it % SQ, u = it / SQ;
+        if (it >= SQ && !(ok = mbar_wait(&bars[kBarQEmpty + st], (u - 1) & 1, status))) break;
+        float* stats = sStats + st * 256;
+#pragma unroll
+        for (int r = lane; r < 128; r += 32) {
+          const int q = q0 + r;
+          const bool in = q < N;
+          stats[r] = in ? -__ldg(lse + static_cast<size_t>(bh) * N + q) * kLog2e : -INFINITY;
+          stats[128 + r] = in ? -__ldg(Dvec + static_cast<size_t>(bh) * N + q) : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
           mbar_arrive_expect_tx(&bars[kBarQFull + st], T::kTileBytes);
           for (int b = 0; b < T::kNumBoxes; ++b)
             tma_load_3d(smem + C::kQ + st * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQFull + st],
                         b * T::kBoxCols, q0, bh);
-          last_q[st] = it;
         }
-        {
-          const int st = it % SD, u = it / SD;
-          if (it >= SD && !mbar_wait(&bars[kBarDoEmpty + st], (u - 1) & 1, status)) break;
+        (st ? last_q1 : last_q0) = it;
+      }
+      {
+        const int st = it % SD, u = it / SD;
+        if (it >= SD && !(ok = mbar_wait(&bars[kBarDoEmpty + st], (u - 1) & 1, status))) break;
+        if (lane == 0) {
           mbar_arrive_expect_tx(&bars[kBarDoFull + st], T::kTileBytes);
           for (int b = 0; b < T::kNumBoxes; ++b)
             tma_load_3d(smem + C::kDo + st * T::kTileBytes + b * T::kBoxBytes, &tm_do, &bars[kBarDoFull + st],
                         b * T::kBoxCols, q0, bh);
-          last_do[st] = it;
         }
-      }
-      // Never leave the CTA with a TMA write still landing in shared memory.
-      mbar_wait(&bars[kBarKV], 0, status);
-      for (int s = 0; s < 2; ++s) {
-        if (last_q[s] >= 0) mbar_wait(&bars[kBarQFull + s], (last_q[s] / SQ) & 1, status);
-        if (last_do[s] >= 0) mbar_wait(&bars[kBarDoFull + s], (last_do[s] / SD) & 1, status);
+        (st ? last_do1 : last_do0) = it;
       }
     }
+    // Never leave the CTA with a TMA write still landing in shared memory.
+    if (lane == 0) {
+      mbar_wait(&bars[kBarKV], 0, status);
+      if (last_q0 >= 0) mbar_wait(&bars[kBarQFull + 0], (last_q0 / SQ) & 1, status);
+      if (last_q1 >= 0) mbar_wait(&bars[kBarQFull + 1], (last_q1 / SQ) & 1, status);
+      if (last_do0 >= 0) mbar_wait(&bars[kBarDoFull + 0], (last_do0 / SD) & 1, status);
+      if (last_do1 >= 0) mbar_wait(&bars[kBarDoFull + 1], (last_do1 / SD) & 1, status);
+    }
+    __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -353,32 +371,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int t = threadIdx.x;  // TMEM lane = key row kv0 + t
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int kv_row = kv0 + t;
+    const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
-    // LSE_i / D_i of this thread's query column, loaded one tile ahead.
-    auto load_stats = [&](int it, float& l2, float& dd) {
-      const int q = (i_begin + it) * kTileRows + t;
-      const bool in = q < N;
-      l2 = in ? __ldg(lse + static_cast<size_t>(bh) * N + q) * kLog2e : INFINITY;
-      dd = in ? __ldg(Dvec + static_cast<size_t>(bh) * N + q) : 0.f;
-    };
-    float nxt_lse, nxt_d;
-    load_stats(0, nxt_lse, nxt_d);
 #pragma unroll 1
     for (int it = 0; it < n_q; ++it) {
       const int i = i_begin + it;
       const int q0 = i * kTileRows;
-      const int b = it & 1;
-      sLse[b * 128 + t] = nxt_lse;
-      sDv[b * 128 + t] = nxt_d;
-      if (it + 1 < n_q) load_stats(it + 1, nxt_lse, nxt_d);
-      // Every compute thread has staged its entry (one arrival per warp after
-      // __syncwarp orders the lanes' stores); a buffer is rewritten two
-      // iterations later, after all four warps have passed the dS hand-off.
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarRowStats + b]);
-      if (!(ok = mbar_wait(&bars[kBarRowStats + b], (it >> 1) & 1, status))) break;
-      const float* lse2 = sLse + b * 128;
-      const float* dvec = sDv + b * 128;
+      const int qs = it % SQ;
+      // The Q stage's full barrier also covers the -LSE / -D the producer
+      // staged for this query tile.
+      if (!(ok = mbar_wait(&bars[kBarQFull + qs], (it / SQ) & 1, status))) break;
+      const float* nlse2 = sStats + qs * 256;  // -LSE_i * log2 e
+      const float* nd = nlse2 + 128;           // -D_i
 
       // P^T = 2^(scale log2e S^T - log2e LSE), masked, kept as packed bf16.
       if (!(ok = mbar_wait(&bars[kBarSFull], it & 1, status))) break;
@@ -393,11 +397,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(sv[e], scale_log2, -lse2[c * 32 + e]));
-          float p1 = ex2_approx(fmaf(sv[e + 1], scale_log2, -lse2[c * 32 + e + 1]));
-          if (row_dead || c * 32 + e < first) p0 = 0.f;
-          if (row_dead || c * 32 + e + 1 < first) p1 = 0.f;
-          pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+          const int col = c * 32 + e;
+          const uint64_t nl = *reinterpret_cast<const uint64_t*>(nlse2 + col);
+          const float2 xx = f2_unpack(ffma2(f2_pack(sv[e], sv[e + 1]), scale2, nl));
+          float p0 = ex2_approx(xx.x);
+          float p1 = ex2_approx(xx.y);
+          if (row_dead || col < first) p0 = 0.f;
+          if (row_dead || col + 1 < first) p1 = 0.f;
+          pk[col / 2] = pack_bf16x2(p0, p1);
         }
       }
       // P^T (bf16 pairs) over the first 64 S^T columns, all of which are read.
@@ -422,9 +429,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t w[4];
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            const float2 pp = unpack_bf16x2(pk[c * 16 + (e + 2 * x) / 2]);
             const int col = c * 32 + e + 2 * x;
-            w[x] = pack_bf16x2(pp.x * (dp[e + 2 * x] - dvec[col]), pp.y * (dp[e + 2 * x + 1] - dvec[col + 1]));
+            const uint64_t diff = fadd2(f2_pack(dp[e + 2 * x], dp[e + 2 * x + 1]),
+                                        *reinterpret_cast<const uint64_t*>(nd + col));
+            const float2 pp = unpack_bf16x2(pk[col / 2]);
+            const float2 ds = f2_unpack(fmul2(f2_pack(pp.x, pp.y), diff));
+            w[x] = pack_bf16x2(ds.x, ds.y);
           }
           store_square_chunk(sDSt, t, c * 4 + e / 8, w[0], w[1], w[2], w[3]);
         }
@@ -481,8 +491,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if ((ok = mbar_wait(&bars[kBarStageFull + bsel], u & 1, status))) {
             tma_reduce_add_3d(&tm_dqacc, sb, c * C::kChunk, q0, bh);
             bulk_commit_group();
-            bulk_wait_group_read0();
-            mbar_arrive(&bars[kBarStageFree + bsel]);
+            // The previous chunk's reduce (other buffer) has read its source
+            // once at most this one is still pending: release that buffer.
+            if (gi >= 1) {
+              bulk_wait_group_read1();
+              mbar_arrive(&bars[kBarStageFree + (bsel ^ 1)]);
+            }
           }
         }
         __syncwarp();
