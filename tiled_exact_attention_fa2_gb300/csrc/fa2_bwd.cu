@@ -390,6 +390,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pk[64];
       const bool row_dead = kv_row >= N;
       const int first = (CAUSAL && i == jt) ? kv_row - q0 : 0;  // queries q0 + c with c < first cannot see this key
+      // P^T goes back to TMEM as bf16 pairs over the first 64 S^T columns, 16
+      // columns per 32 scores: P columns [16c, 16c + 16) cover S columns
+      // [32c, 32c + 32), which are already in registers.
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float sv[32];
@@ -406,10 +409,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (row_dead || col + 1 < first) p1 = 0.f;
           pk[col / 2] = pack_bf16x2(p0, p1);
         }
+        tmem_st16u(tmem + lane_base + C::kColS + 16 * c, pk + 16 * c);
       }
-      // P^T (bf16 pairs) over the first 64 S^T columns, all of which are read.
-      tmem_st32u(tmem + lane_base + C::kColS, pk);
-      tmem_st32u(tmem + lane_base + C::kColS + 32, pk + 32);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -74,14 +74,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// One potentially blocking test of the phase: the thread may be suspended
+// (not spinning, so it takes no issue slots from its neighbours) until the
+// phase completes or roughly kTryWaitSuspendNs have passed.
+constexpr uint32_t kTryWaitSuspendNs = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
+      : "r"(bar_addr), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -90,14 +94,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // false (and records kDevWaitTimeout in *status) after FA2_WAIT_TIMEOUT_NS.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   const uint32_t a = smem_u32(bar);
-#pragma unroll 1
-  for (int i = 0; i < 64; ++i)
-    if (mbar_try_wait(a, parity)) return true;
+  if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
+    for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(a, parity)) return true;
     if (global_timer_ns() - t0 > FA2_WAIT_TIMEOUT_NS) {
       atomicCAS(status, kDevOk, kDevWaitTimeout);
