@@ -45,6 +45,7 @@ import numpy as np
 __all__ = [
     "as_f64", "fp32_scale", "scores", "apply_causal_mask", "row_logsumexp",
     "attn_fwd_head", "attn_bwd_head", "attn_fwd", "attn_bwd", "attn_rows",
+    "attn_bwd_gqa",
 ]
 
 
@@ -188,4 +189,37 @@ def attn_rows(q, k, v, dO, scale: float, causal: bool, rows):
             out["LSE"][b, h] = lse
             out["D"][b, h] = Dr
             out["dQ"][b, h] = s * (dS @ k[b, h])
+    return out
+
+
+def attn_bwd_gqa(q, k, v, dO, scale: float, causal: bool):
+    """Grouped-query attention, forward + backward, fp64.
+
+    Grouped-query attention is named as a next primitive in the article
+    (section "Next Frontiers in WebGPU ML"); the pages give no formula, so the
+    plain reading is used: q, dO are [B, H, N, d], k, v are [B, H_kv, N, d]
+    with H a multiple of H_kv, and query head h attends to key/value head
+    h // (H / H_kv).  Each query head is ordinary attention against its
+    key/value head; because a key/value head feeds H / H_kv query heads, its
+    gradients dK, dV are the sums of the per-query-head gradients over that
+    group.  Returns a dict with O, LSE, D, dQ ([B, H, ...]) and dK, dV
+    ([B, H_kv, N, d]).
+    """
+    q, k, v, dO = as_f64(q), as_f64(k), as_f64(v), as_f64(dO)
+    s = fp32_scale(scale)
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if H % Hkv:
+        raise ValueError("H must be a multiple of H_kv")
+    G = H // Hkv
+    out = {"O": np.empty((B, H, N, d)), "LSE": np.empty((B, H, N)), "D": np.empty((B, H, N)),
+           "dQ": np.empty((B, H, N, d)), "dK": np.zeros((B, Hkv, N, d)), "dV": np.zeros((B, Hkv, N, d))}
+    for b in range(B):
+        for h in range(H):
+            hk = h // G
+            r = attn_bwd_head(q[b, h], k[b, hk], v[b, hk], dO[b, h], s, causal)
+            for key in ("O", "LSE", "D", "dQ"):
+                out[key][b, h] = r[key]
+            out["dK"][b, hk] += r["dK"]
+            out["dV"][b, hk] += r["dV"]
     return out

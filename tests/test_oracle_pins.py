@@ -322,3 +322,64 @@ def test_planted_mistakes_are_caught(name):
         except (AssertionError, ValueError, FloatingPointError):
             failed.append(pin.__name__)
     assert failed, f"no pin caught planted mistake {name}"
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query attention (K/V heads shared by groups of query heads).
+# ---------------------------------------------------------------------------
+
+def test_gqa_with_one_query_head_per_group_is_plain_attention():
+    x = workloads.make_inputs(2, 3, 17, 8, seed=301)
+    for causal in (True, False):
+        a = oracle.attn_bwd_gqa(x["q"], x["k"], x["v"], x["dO"], 0.35, causal)
+        b = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dO"], 0.35, causal)
+        for key in a:
+            np.testing.assert_allclose(a[key], b[key], rtol=0, atol=1e-13)
+
+
+def test_gqa_equals_attention_on_repeated_kv_with_summed_gradients():
+    # Independent construction: repeat each K/V head G times (a library
+    # routine, np.repeat), run plain attention on the repeated tensors with
+    # torch's fp64 autograd, and sum the K/V gradients back over each group.
+    B, H, Hkv, N, d = 1, 6, 2, 13, 4
+    r = np.random.Generator(np.random.PCG64(302))
+    q, dO = r.standard_normal((B, H, N, d)), r.standard_normal((B, H, N, d))
+    k, v = r.standard_normal((B, Hkv, N, d)), r.standard_normal((B, Hkv, N, d))
+    G = H // Hkv
+    for causal in (True, False):
+        tq = torch.tensor(q, requires_grad=True)
+        tk = torch.tensor(k, requires_grad=True)
+        tv = torch.tensor(v, requires_grad=True)
+        kr = tk.repeat_interleave(G, dim=1)
+        vr = tv.repeat_interleave(G, dim=1)
+        o = torch.nn.functional.scaled_dot_product_attention(tq, kr, vr, is_causal=causal, scale=0.5)
+        (o * torch.tensor(dO)).sum().backward()
+        got = oracle.attn_bwd_gqa(q, k, v, dO, 0.5, causal)
+        np.testing.assert_allclose(got["O"], o.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(got["dQ"], tq.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(got["dK"], tk.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(got["dV"], tv.grad.numpy(), atol=1e-12)
+
+
+def test_gqa_finite_differences_through_shared_kv():
+    # dL/dK and dL/dV of a shared head collect every query head of its group.
+    B, H, Hkv, N, d, s, h = 1, 4, 1, 5, 3, 0.7, 1e-6
+    r = np.random.Generator(np.random.PCG64(303))
+    q, dO = r.standard_normal((B, H, N, d)), r.standard_normal((B, H, N, d))
+    k, v = r.standard_normal((B, Hkv, N, d)), r.standard_normal((B, Hkv, N, d))
+    for causal in (True, False):
+        g = oracle.attn_bwd_gqa(q, k, v, dO, s, causal)
+
+        def loss(kk, vv):
+            return float((oracle.attn_bwd_gqa(q, kk, vv, dO, s, causal)["O"] * dO).sum())
+
+        for name, grad in (("k", g["dK"]), ("v", g["dV"])):
+            fd = np.zeros_like(grad)
+            for idx in np.ndindex(*grad.shape):
+                args = {"k": k.copy(), "v": v.copy()}
+                args[name][idx] += h
+                lp = loss(args["k"], args["v"])
+                args[name][idx] -= 2 * h
+                lm = loss(args["k"], args["v"])
+                fd[idx] = (lp - lm) / (2 * h)
+            assert np.abs(fd - grad).max() < 1e-7 * max(1.0, np.abs(grad).max()), name

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q0 = (i_begin + it) * kTileRows;
       {
         const int st = it % SQ, u = it / SQ;
-        if (it >= SQ && !(ok = mbar_wait(&bars[kBarQEmpty + st], (u - 1) & 1, status))) break;
+        if (it >= SQ && !(ok = mbar_wait_sleep(&bars[kBarQEmpty + st], (u - 1) & 1, status))) break;
         float* stats = sStats + st * 256;
 #pragma unroll
         for (int r = lane; r < 128; r += 32) {
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       {
         const int st = it % SD, u = it / SD;
-        if (it >= SD && !(ok = mbar_wait(&bars[kBarDoEmpty + st], (u - 1) & 1, status))) break;
+        if (it >= SD && !(ok = mbar_wait_sleep(&bars[kBarDoEmpty + st], (u - 1) & 1, status))) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars[kBarDoFull + st], T::kTileBytes);
           for (int b = 0; b < T::kNumBoxes; ++b)
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
     for (int it = 0; it < n_q; ++it) {
       const int q0 = (i_begin + it) * kTileRows;
-      if (!(ok = mbar_wait(&bars[kBarDqFull], it & 1, status))) break;
+      if (!(ok = mbar_wait_sleep(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
       float g[D];
       if constexpr (D >= 32) {
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
         const int gi = it * C::kChunks + c, bsel = gi & 1, u = gi >> 1;
-        if (gi >= 2 && !(ok = mbar_wait(&bars[kBarStageFree + bsel], (u - 1) & 1, status))) break;
+        if (gi >= 2 && !(ok = mbar_wait_sleep(&bars[kBarStageFree + bsel], (u - 1) & 1, status))) break;
         const uint32_t sb = sStage + bsel * C::kStageBytes;
 #pragma unroll
         for (int j = 0; j < C::kChunk / 4; ++j) {
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (issuer) bulk_wait_group0();  // every reduce has landed before the CTA exits
     // ------------------------------------------------------------ epilogue: dV, dK * scale -> bf16
-    if (ok && mbar_wait(&bars[kBarAccFull], 0, status)) {
+    if (ok && mbar_wait_sleep(&bars[kBarAccFull], 0, status)) {
       tc_fence_after();
       const int kv_row = kv0 + t;
       const bool valid = kv_row < N;

@@ -142,13 +142,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll 1
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status)) break;
+        if (j >= 2 && !mbar_wait_sleep(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
                       b * T::kBoxCols, j * kTileRows, bh);
         (st ? last_k1 : last_k0) = j;
-        if (j >= 2 && !mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
+        if (j >= 2 && !mbar_wait_sleep(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],

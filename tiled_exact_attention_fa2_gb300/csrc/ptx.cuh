@@ -74,11 +74,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// One potentially blocking test of the phase: the thread may be suspended
-// (not spinning, so it takes no issue slots from its neighbours) until the
-// phase completes or roughly kTryWaitSuspendNs have passed.
-constexpr uint32_t kTryWaitSuspendNs = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Same test, but the thread may stay suspended (taking no issue slots from
+// its neighbours) until the phase completes or about kTryWaitSuspendNs pass.
+// For waits that are long and off the critical path: waking up can lag the
+// phase completion.
+constexpr uint32_t kTryWaitSuspendNs = 100000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
@@ -92,20 +105,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 
 // Wait until the phase with the given parity has completed.  Bounded: returns
 // false (and records kDevWaitTimeout in *status) after FA2_WAIT_TIMEOUT_NS.
+template <bool SLEEP = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto test = [&]() { return SLEEP ? mbar_try_wait_sleep(a, parity) : mbar_try_wait(a, parity); };
+#pragma unroll 1
+  for (int i = 0; i < (SLEEP ? 1 : 64); ++i)
+    if (test()) return true;
   const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(a, parity)) return true;
+    for (int i = 0; i < (SLEEP ? 16 : 256); ++i)
+      if (test()) return true;
     if (global_timer_ns() - t0 > FA2_WAIT_TIMEOUT_NS) {
       atomicCAS(status, kDevOk, kDevWaitTimeout);
       return false;
     }
   }
+}
+
+// Sleeping variant for long, non-critical waits.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, int* status) {
+  return mbar_wait<true>(bar, parity, status);
 }
 
 // ---------------------------------------------------------------- TMA
