@@ -78,6 +78,25 @@ int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
             void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* stream);
 
+/*
+ * Grouped-query attention (GQA; multi-query attention when H_kv = 1), named
+ * as a next primitive in the article's section "Next Frontiers in WebGPU ML".
+ * q, o, dO, dq: [B, H, N, d]; k, v, dk, dv: [B, H_kv, N, d]; lse: [B, H, N];
+ * H must be a multiple of H_kv, and query head h attends to key/value head
+ * h / (H / H_kv).  dk and dv are the sums over each group of query heads.
+ * Same rules and errors as fa2_fwd / fa2_bwd / fa2_bwd_ws (FA2_ERR_SHAPE if
+ * H_kv < 1 or H % H_kv != 0); fa2_fwd(...) is fa2_fwd_gqa(..., H_kv = H, ...).
+ * The workspace is fa2_bwd_workspace_bytes(B, H, N, d) (query heads).
+ */
+int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                int d, float scale, int causal, void* stream);
+int fa2_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale, int causal,
+                void* stream);
+int fa2_bwd_gqa_ws(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale, int causal,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device scratch fa2_bwd needs: D (fp32 [B,H,N]) and the fp32 dQ
  * accumulator [B,H,N,d], each 256-byte aligned.  0 on invalid sizes. */
 size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);

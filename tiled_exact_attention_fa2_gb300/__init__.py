@@ -22,7 +22,7 @@ from . import _build
 __all__ = [
     "FA2Error", "load_library", "fa2_fwd", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
     "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
-    "fa2_bwd_stages", "fa2_bwd_noalloc",
+    "fa2_bwd_stages", "fa2_bwd_noalloc", "fa2_fwd_gqa", "fa2_bwd_gqa",
     "FA2_OK",
 ]
 
@@ -48,6 +48,10 @@ _SIGNATURES = {
     "fa2_last_error_detail": (ctypes.c_char_p, []),
     "fa2_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_noalloc_scratch_capacity": (_sz, []),
+    "fa2_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_bwd_gqa_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
+                            _vp]),
 }
 
 
@@ -184,6 +188,51 @@ def fa2_bwd_ws(q, k, v, o, dO, lse, workspace: torch.Tensor, dq=None, dk=None, d
                         _stream(stream, q.device))
     if rc != FA2_OK:
         raise FA2Error("fa2_bwd_ws", rc)
+    return dq, dk, dv
+
+
+def _gqa_shapes(q, k, v):
+    B, H, N, d = _shape(q, "q")
+    Bk, Hkv, Nk, dk_ = _shape(k, "k")
+    if (Bk, Nk, dk_) != (B, N, d) or _shape(v, "v") != (B, Hkv, N, d):
+        raise ValueError("k and v must be [B, H_kv, N, d] with q's B, N and d")
+    return B, H, Hkv, N, d
+
+
+def fa2_fwd_gqa(q, k, v, o=None, lse=None, scale: Optional[float] = None, causal: bool = True, stream=None):
+    """Grouped-query forward: q [B,H,N,d], k/v [B,H_kv,N,d]; query head h reads K/V head h // (H // H_kv)."""
+    lib = load_library()
+    B, H, Hkv, N, d = _gqa_shapes(q, k, v)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _shape(o, "o")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    rc = lib.fa2_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
+                         _scale(scale, d), 1 if causal else 0, _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_fwd_gqa", rc)
+    return o, lse
+
+
+def fa2_bwd_gqa(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optional[float] = None,
+                causal: bool = True, stream=None):
+    """Grouped-query backward: dk/dv [B,H_kv,N,d] are sums over each group of query heads."""
+    lib = load_library()
+    B, H, Hkv, N, d = _gqa_shapes(q, k, v)
+    for name, t in (("o", o), ("dO", dO)):
+        if _shape(t, name) != (B, H, N, d):
+            raise ValueError(f"{name} must have q's shape")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    rc = lib.fa2_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, d, _scale(scale, d),
+                         1 if causal else 0, _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_gqa", rc)
     return dq, dk, dv
 
 

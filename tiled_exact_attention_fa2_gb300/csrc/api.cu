@@ -115,19 +115,24 @@ size_t workspace_bytes(int B, int H, int N, int d) {
   return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
 }
 
+// Query heads H, key/value heads Hkv (H a multiple of Hkv).
+int check_heads(int H, int Hkv) { return (Hkv >= 1 && Hkv <= H && H % Hkv == 0) ? FA2_OK : FA2_ERR_SHAPE; }
+
 int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                 void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale) {
+                 void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, float scale) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA2_ERR_NULL;
   if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (int rc = check_heads(H, Hkv)) return rc;
   if (int rc = check_scale(scale)) return rc;
   const void* bf[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : bf)
     if (!aligned(p, 16)) return FA2_ERR_ALIGN;
   if (!aligned(lse, 4)) return FA2_ERR_ALIGN;
   const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t kb = static_cast<size_t>(B) * Hkv * N * d * 2;
   const size_t lb = static_cast<size_t>(B) * H * N * 4;
-  const Range outs[] = {range_of(dq, tb), range_of(dk, tb), range_of(dv, tb)};
-  const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(o, tb), range_of(dO, tb),
+  const Range outs[] = {range_of(dq, tb), range_of(dk, kb), range_of(dv, kb)};
+  const Range ins[] = {range_of(q, tb), range_of(k, kb), range_of(v, kb), range_of(o, tb), range_of(dO, tb),
                        range_of(lse, lb)};
   for (int a = 0; a < 3; ++a) {
     for (const Range& r : ins)
@@ -139,23 +144,24 @@ int validate_bwd(const void* q, const void* k, const void* v, const void* o, con
 }
 
 int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const void* dO, const float* dq_acc, int BH,
-               int N, int d) {
-  return (make_tmap(&tm->q, q, BH, N, d) && make_tmap(&tm->k, k, BH, N, d) && make_tmap(&tm->v, v, BH, N, d) &&
+               int BHkv, int N, int d) {
+  return (make_tmap(&tm->q, q, BH, N, d) && make_tmap(&tm->k, k, BHkv, N, d) && make_tmap(&tm->v, v, BHkv, N, d) &&
           make_tmap(&tm->dO, dO, BH, N, d) && make_tmap_f32(&tm->dqacc, dq_acc, BH, N, d))
              ? FA2_OK
              : cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
 }
 
 int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
-            void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* ws, cudaStream_t st) {
+            void* dk, void* dv, int B, int H, int Hkv, int N, int d, float scale, int causal, void* ws,
+            cudaStream_t st) {
   const int BH = B * H;
   const size_t rows = static_cast<size_t>(BH) * N;
   float* Dvec = static_cast<float*>(ws);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(rows * sizeof(float)));
   TmapSet tm;
-  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, BH, N, d)) return rc;
+  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, BH, B * Hkv, N, d)) return rc;
   if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, BH, N, d, st)) return cuda_fail(e, "bwd preprocess launch");
-  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, BH, N, d, scale, causal != 0, st))
+  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, BH, N, d, H / Hkv, scale, causal != 0, st))
     return cuda_fail(e, "bwd main launch");
   if (int e = launch_bwd_dq_convert(dq_acc, dq, BH, N, d, scale, st)) return cuda_fail(e, "dq convert launch");
   return FA2_OK;
@@ -182,28 +188,35 @@ using namespace fa2;
 
 extern "C" {
 
-int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-            float scale, int causal, void* stream) {
+int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                int d, float scale, int causal, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
   if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (int rc = check_heads(H, H_kv)) return rc;
   if (int rc = check_scale(scale)) return rc;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA2_ERR_ALIGN;
   const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t kb = static_cast<size_t>(B) * H_kv * N * d * 2;
   const size_t lb = static_cast<size_t>(B) * H * N * 4;
   const Range ro = range_of(o, tb), rl = range_of(lse, lb);
-  const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb)};
+  const Range ins[] = {range_of(q, tb), range_of(k, kb), range_of(v, kb)};
   for (const Range& r : ins)
     if (overlap(ro, r) || overlap(rl, r)) return FA2_ERR_ALIAS;
   if (overlap(ro, rl)) return FA2_ERR_ALIAS;
 
   const int BH = B * H;
   TmapSet tm;
-  if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, BH, N, d) || !make_tmap(&tm.v, v, BH, N, d))
+  if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, B * H_kv, N, d) || !make_tmap(&tm.v, v, B * H_kv, N, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
-  if (int e = launch_fwd(tm, o, lse, BH, N, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
+  if (int e = launch_fwd(tm, o, lse, BH, N, d, H / H_kv, scale, causal != 0, static_cast<cudaStream_t>(stream)))
     return cuda_fail(e, "fwd launch");
   return FA2_OK;
+}
+
+int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+            float scale, int causal, void* stream) {
+  return fa2_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
 }
 
 size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -211,19 +224,27 @@ size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d) {
   return workspace_bytes(B, H, N, d);
 }
 
-int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-               void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
-               void* workspace, size_t workspace_bytes_given, void* stream) {
-  if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale)) return rc;
+int fa2_bwd_gqa_ws(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale, int causal,
+                   void* workspace, size_t workspace_bytes_given, void* stream) {
+  if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale)) return rc;
   if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < workspace_bytes(B, H, N, d))
     return FA2_ERR_WORKSPACE;
-  return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+  return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, workspace,
                  static_cast<cudaStream_t>(stream));
 }
 
-int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-            void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* stream) {
-  if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale)) return rc;
+int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+               void* workspace, size_t workspace_bytes_given, void* stream) {
+  return fa2_bwd_gqa_ws(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d, scale, causal, workspace,
+                        workspace_bytes_given, stream);
+}
+
+int fa2_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale, int causal,
+                void* stream) {
+  if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale)) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = workspace_bytes(B, H, N, d);
   void* ws = nullptr;
@@ -232,9 +253,14 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const vo
     cuda_fail(static_cast<int>(e), "cudaMallocAsync");
     return FA2_ERR_ALLOC;
   }
-  const int rc = run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, st);
+  const int rc = run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, ws, st);
   if (cudaError_t e = cudaFreeAsync(ws, st)) return cuda_fail(static_cast<int>(e), "cudaFreeAsync");
   return rc;
+}
+
+int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+            void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* stream) {
+  return fa2_bwd_gqa(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d, scale, causal, stream);
 }
 
 int fa2_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H, int N, int d,
@@ -276,8 +302,8 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
       if (overlap(outs[a], outs[b])) return FA2_ERR_ALIAS;
   }
   TmapSet tm;
-  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, B * H, N, d)) return rc;
-  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, B * H, N, d, scale, causal != 0,
+  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, B * H, B * H, N, d)) return rc;
+  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, B * H, N, d, 1, scale, causal != 0,
                               static_cast<cudaStream_t>(stream)))
     return cuda_fail(e, "bwd main launch");
   return FA2_OK;

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse,
                    const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                   int BH, int N, float scale, float scale_log2) {
+                   int BH, int N, int group, float scale, float scale_log2) {
   using T = HeadDim<D>;
   using C = BwdCfg<D>;
   constexpr int SQ = C::kQStages, SD = C::kDoStages;
@@ -191,11 +191,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
   const int num_tiles = (N + kTileRows - 1) / kTileRows;
-  const int bh = blockIdx.x % BH;
-  const int jt = blockIdx.x / BH;  // key/value tile; causal work shrinks with jt, so heavy tiles go first
+  // One CTA per (key/value tile, K/V head); it visits the query tiles of all
+  // `group` query heads that share the K/V head, so dK and dV accumulate the
+  // group sum in TMEM.  Iteration it covers query head g = it / n_q, query
+  // tile i = i_begin + it % n_q.
+  const int BHkv = BH / group;
+  const int bh_kv = blockIdx.x % BHkv;
+  const int jt = blockIdx.x / BHkv;  // key/value tile; causal work shrinks with jt, so heavy tiles go first
   const int kv0 = jt * kTileRows;
   const int i_begin = CAUSAL ? jt : 0;
   const int n_q = num_tiles - i_begin;
+  const int n_iter = n_q * group;
 
   if (threadIdx.x == 8 * 32) {
     mbar_init(&bars[kBarKV], 1);
@@ -242,15 +248,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars[kBarKV], 2 * T::kTileBytes);
       for (int b = 0; b < T::kNumBoxes; ++b) {
-        tma_load_3d(smem + C::kK + b * T::kBoxBytes, &tm_k, &bars[kBarKV], b * T::kBoxCols, kv0, bh);
-        tma_load_3d(smem + C::kV + b * T::kBoxBytes, &tm_v, &bars[kBarKV], b * T::kBoxCols, kv0, bh);
+        tma_load_3d(smem + C::kK + b * T::kBoxBytes, &tm_k, &bars[kBarKV], b * T::kBoxCols, kv0, bh_kv);
+        tma_load_3d(smem + C::kV + b * T::kBoxBytes, &tm_v, &bars[kBarKV], b * T::kBoxCols, kv0, bh_kv);
       }
     }
     int last_q0 = -1, last_q1 = -1, last_do0 = -1, last_do1 = -1;
     bool ok = true;
 #pragma unroll 1
-    for (int it = 0; it < n_q; ++it) {
-      const int q0 = (i_begin + it) * kTileRows;
+    for (int it = 0; it < n_iter; ++it) {
+      const int q0 = (i_begin + it % n_q) * kTileRows;
+      const int bh = bh_kv * group + it / n_q;
       {
         const int st = it % SQ, u = it / SQ;
         if (it >= SQ && !(ok = mbar_wait_sleep(&bars[kBarQEmpty + st], (u - 1) & 1, status))) break;
@@ -320,7 +327,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       bool ok = mbar_wait(&bars[kBarKV], 0, status) && issue_s(0);
 #pragma unroll 1
-      for (int it = 0; ok && it < n_q; ++it) {
+      for (int it = 0; ok && it < n_iter; ++it) {
         const int qs = it % SQ, ds = it % SD, du = it / SD;
         // Recompute the operand descriptors every iteration (a few integer
         // ops) instead of keeping ~40 hoisted 64-bit descriptors live.
@@ -344,7 +351,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(&bars[kBarDoEmpty + ds]);
         mma_commit(&bars[kBarDvDone]);
         // S^T(i+1) overwrites the P^T columns dV(i) reads: wait for dV(i).
-        if (it + 1 < n_q) {
+        if (it + 1 < n_iter) {
           if (!(ok = mbar_wait(&bars[kBarDvDone], it & 1, status))) break;
           if (!(ok = issue_s(it + 1))) break;
         }
@@ -374,8 +381,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
 #pragma unroll 1
-    for (int it = 0; it < n_q; ++it) {
-      const int i = i_begin + it;
+    for (int it = 0; it < n_iter; ++it) {
+      const int i = i_begin + it % n_q;
       const int q0 = i * kTileRows;
       const int qs = it % SQ;
       // The Q stage's full barrier also covers the -LSE / -D the producer
@@ -459,8 +466,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t sStage = smem_u32(smem + C::kStage);
     bool ok = true;
 #pragma unroll 1
-    for (int it = 0; it < n_q; ++it) {
-      const int q0 = (i_begin + it) * kTileRows;
+    for (int it = 0; it < n_iter; ++it) {
+      const int q0 = (i_begin + it % n_q) * kTileRows;
+      const int bh = bh_kv * group + it / n_q;
       if (!(ok = mbar_wait_sleep(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
       float g[D];
@@ -511,7 +519,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int kv_row = kv0 + t;
       const bool valid = kv_row < N;
-      const size_t off = (static_cast<size_t>(bh) * N + (valid ? kv_row : 0)) * D;
+      const size_t off = (static_cast<size_t>(bh_kv) * N + (valid ? kv_row : 0)) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
@@ -570,15 +578,15 @@ int launch_preprocess_t(const void* o, const void* dO, float* Dvec, float* dq_ac
 
 template <int D, bool CAUSAL>
 int launch_bwd_main_t(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N,
-                      float scale, cudaStream_t stream) {
+                      int group, float scale, cudaStream_t stream) {
   using C = BwdCfg<D>;
   auto kern = fa2_bwd_kernel<D, CAUSAL>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_tiles = (N + kTileRows - 1) / kTileRows;
-  const dim3 grid(static_cast<unsigned>(num_tiles) * static_cast<unsigned>(BH));
+  const dim3 grid(static_cast<unsigned>(num_tiles) * static_cast<unsigned>(BH / group));
   kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, tm.dqacc, lse, Dvec,
                                                   static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-                                                  BH, N, scale, scale * kLog2e);
+                                                  BH, N, group, scale, scale * kLog2e);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -607,16 +615,16 @@ int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_
 }
 
 int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N, int d,
-                    float scale, bool causal, cudaStream_t stream) {
+                    int group, float scale, bool causal, cudaStream_t stream) {
   switch (d) {
-    case 16: return causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
-                           : launch_bwd_main_t<16, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
-    case 32: return causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
-                           : launch_bwd_main_t<32, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
-    case 64: return causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
-                           : launch_bwd_main_t<64, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
-    case 128: return causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dk, dv, BH, N, scale, stream)
-                            : launch_bwd_main_t<128, false>(tm, lse, Dvec, dk, dv, BH, N, scale, stream);
+    case 16: return causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
+                           : launch_bwd_main_t<16, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
+    case 32: return causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
+                           : launch_bwd_main_t<32, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
+    case 64: return causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
+                           : launch_bwd_main_t<64, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
+    case 128: return causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
+                            : launch_bwd_main_t<128, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

@@ -80,7 +80,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out_o,
-                   float* __restrict__ out_lse, int BH, int N, float scale_log2) {
+                   float* __restrict__ out_lse, int BH, int N, int group, float scale_log2) {
   using T = HeadDim<D>;
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int num_tiles = (N + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_tiles + 1) / 2;
   const int bh = blockIdx.x % BH;
+  const int bh_kv = bh / group;  // query heads [g*group, (g+1)*group) share K/V head g
   const int pair = num_pairs - 1 - static_cast<int>(blockIdx.x / BH);
   const int q0 = pair * 2 * kTileRows;
   // K/V tiles each query tile visits; a tile with no row < N visits none.
@@ -142,17 +143,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll 1
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait_sleep(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status)) break;
+        if (j >= 2 && !mbar_wait(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
-                      b * T::kBoxCols, j * kTileRows, bh);
+                      b * T::kBoxCols, j * kTileRows, bh_kv);
         (st ? last_k1 : last_k0) = j;
-        if (j >= 2 && !mbar_wait_sleep(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
+        if (j >= 2 && !mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
-                      b * T::kBoxCols, j * kTileRows, bh);
+                      b * T::kBoxCols, j * kTileRows, bh_kv);
         (st ? last_v1 : last_v0) = j;
       }
       // Never leave the CTA with a TMA write still landing in shared memory.
@@ -382,7 +383,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 template <int D, bool CAUSAL>
-int launch_fwd_t(const TmapSet& tm, void* o, float* lse, int BH, int N, float scale, cudaStream_t stream) {
+int launch_fwd_t(const TmapSet& tm, void* o, float* lse, int BH, int N, int group, float scale,
+                 cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fa2_fwd_kernel<D, CAUSAL>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
@@ -391,23 +393,23 @@ int launch_fwd_t(const TmapSet& tm, void* o, float* lse, int BH, int N, float sc
   const dim3 grid(static_cast<unsigned>(num_pairs) * static_cast<unsigned>(BH));
   const float scale_log2 = scale * 1.44269504088896341f;
   kern<<<grid, kFwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, static_cast<__nv_bfloat16*>(o), lse, BH, N,
-                                                  scale_log2);
+                                                  group, scale_log2);
   return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace
 
-int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, float scale, bool causal,
+int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, int group, float scale, bool causal,
                cudaStream_t stream) {
   switch (d) {
-    case 16: return causal ? launch_fwd_t<16, true>(tm, o, lse, BH, N, scale, stream)
-                           : launch_fwd_t<16, false>(tm, o, lse, BH, N, scale, stream);
-    case 32: return causal ? launch_fwd_t<32, true>(tm, o, lse, BH, N, scale, stream)
-                           : launch_fwd_t<32, false>(tm, o, lse, BH, N, scale, stream);
-    case 64: return causal ? launch_fwd_t<64, true>(tm, o, lse, BH, N, scale, stream)
-                           : launch_fwd_t<64, false>(tm, o, lse, BH, N, scale, stream);
-    case 128: return causal ? launch_fwd_t<128, true>(tm, o, lse, BH, N, scale, stream)
-                            : launch_fwd_t<128, false>(tm, o, lse, BH, N, scale, stream);
+    case 16: return causal ? launch_fwd_t<16, true>(tm, o, lse, BH, N, group, scale, stream)
+                           : launch_fwd_t<16, false>(tm, o, lse, BH, N, group, scale, stream);
+    case 32: return causal ? launch_fwd_t<32, true>(tm, o, lse, BH, N, group, scale, stream)
+                           : launch_fwd_t<32, false>(tm, o, lse, BH, N, group, scale, stream);
+    case 64: return causal ? launch_fwd_t<64, true>(tm, o, lse, BH, N, group, scale, stream)
+                           : launch_fwd_t<64, false>(tm, o, lse, BH, N, group, scale, stream);
+    case 128: return causal ? launch_fwd_t<128, true>(tm, o, lse, BH, N, group, scale, stream)
+                            : launch_fwd_t<128, false>(tm, o, lse, BH, N, group, scale, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
