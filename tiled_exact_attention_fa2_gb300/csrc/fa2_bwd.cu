@@ -45,11 +45,13 @@ __device__ int g_bwd_status;
 
 namespace {
 
-// 10 warps: P/dS warpgroup (0-3), dQ-drain/epilogue warpgroup (4-7), TMA
-// producer (8), MMA issuer (9).  Warps spread round-robin over the four SM
-// sub-partitions (16K registers each), so two sub-partitions hold three
-// warps: at most 168 registers per thread, which the kernel fits unspilled.
-constexpr int kBwdThreads = 320;
+// 14 warps: two P/dS warpgroups (0-3 for query columns 0-63 of each tile,
+// 4-7 for columns 64-127), the dQ-drain / epilogue warpgroup (8-11), the TMA
+// producer (12) and the MMA issuer (13).  Warps spread round-robin over the
+// four SM sub-partitions (16K registers each), two of which then hold four
+// warps: at most 128 registers per thread (launch bound 512 threads).
+constexpr int kBwdThreads = 448;
+constexpr int kWarpDrain = 8, kWarpProducer = 12, kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.44269504088896341f;
 
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __rest
 
 // ---------------------------------------------------------------- main
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(512, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse,
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int n_q = num_tiles - i_begin;
   const int n_iter = n_q * group;
 
-  if (threadIdx.x == 8 * 32) {
+  if (threadIdx.x == kWarpProducer * 32) {
     mbar_init(&bars[kBarKV], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kBarQFull + s], 1);
@@ -213,13 +215,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars[kBarSFull], 1);
     mbar_init(&bars[kBarDpFull], 1);
-    mbar_init(&bars[kBarPFull], 4);
+    mbar_init(&bars[kBarPFull], 8);
     mbar_init(&bars[kBarDvDone], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kBarStageFull + s], 4);
       mbar_init(&bars[kBarStageFree + s], 1);
     }
-    mbar_init(&bars[kBarDsFull], 4);
+    mbar_init(&bars[kBarDsFull], 8);
     mbar_init(&bars[kBarDsEmpty], 1);
     mbar_init(&bars[kBarDqFull], 1);
     mbar_init(&bars[kBarDqDrained], 4);
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars[kBarDrain], 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     // Lane 0 issues the TMA loads; all 32 lanes stage -LSE*log2e and -D of
     // the query tile into the Q stage's stats slot before lane 0 arms the
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (last_do1 >= 0) mbar_wait(&bars[kBarDoFull + 1], (last_do1 / SD) & 1, status);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdSq = make_idesc_bf16(128, 128, false, false);  // K x Q^T, V x dO^T
@@ -373,10 +375,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(&bars[kBarDrain]);
       mbar_wait(&bars[kBarDrain], 0, status);
     }
-  } else if (warp < 4) {
+  } else if (warp < kWarpDrain) {
     // ------------------------------------------------------------ P / dS warps
-    const int t = threadIdx.x;  // TMEM lane = key row kv0 + t
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Warpgroup hh handles query columns [64 hh, 64 hh + 64) of every tile;
+    // thread t owns key row kv0 + t (TMEM lane t).
+    const int hh = warp >> 2;
+    const int t = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int kv_row = kv0 + t;
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
@@ -394,29 +399,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P^T = 2^(scale log2e S^T - log2e LSE), masked, kept as packed bf16.
       if (!(ok = mbar_wait(&bars[kBarSFull], it & 1, status))) break;
       tc_fence_after();
-      uint32_t pk[64];
+      uint32_t pk[32];  // this half's 64 weights as bf16 pairs
       const bool row_dead = kv_row >= N;
       const int first = (CAUSAL && i == jt) ? kv_row - q0 : 0;  // queries q0 + c with c < first cannot see this key
       // P^T goes back to TMEM as bf16 pairs over the first 64 S^T columns, 16
-      // columns per 32 scores: P columns [16c, 16c + 16) cover S columns
-      // [32c, 32c + 32), which are already in registers.
+      // columns per 32 scores: P columns [col0 / 2, col0 / 2 + 16) cover S
+      // columns [col0, col0 + 32), which are already in registers.
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * hh + 32 * c;
         float sv[32];
-        tmem_ld32(tmem + lane_base + C::kColS + c * 32, sv);
+        tmem_ld32(tmem + lane_base + C::kColS + col0, sv);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int col = c * 32 + e;
+          const int col = col0 + e;
           const uint64_t nl = *reinterpret_cast<const uint64_t*>(nlse2 + col);
           const float2 xx = f2_unpack(ffma2(f2_pack(sv[e], sv[e + 1]), scale2, nl));
           float p0 = ex2_approx(xx.x);
           float p1 = ex2_approx(xx.y);
           if (row_dead || col < first) p0 = 0.f;
           if (row_dead || col + 1 < first) p1 = 0.f;
-          pk[col / 2] = pack_bf16x2(p0, p1);
+          pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
         }
-        tmem_st16u(tmem + lane_base + C::kColS + 16 * c, pk + 16 * c);
+        tmem_st16u(tmem + lane_base + C::kColS + col0 / 2, pk + 16 * c);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -428,23 +434,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (it >= 1 && !(ok = mbar_wait(&bars[kBarDsEmpty], (it - 1) & 1, status))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * hh + 32 * c;
         float dp[32];
-        tmem_ld32(tmem + lane_base + C::kColDP + c * 32, dp);
+        tmem_ld32(tmem + lane_base + C::kColDP + col0, dp);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint32_t w[4];
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            const int col = c * 32 + e + 2 * x;
+            const int col = col0 + e + 2 * x;
             const uint64_t diff = fadd2(f2_pack(dp[e + 2 * x], dp[e + 2 * x + 1]),
                                         *reinterpret_cast<const uint64_t*>(nd + col));
-            const float2 pp = unpack_bf16x2(pk[col / 2]);
+            const float2 pp = unpack_bf16x2(pk[16 * c + (e + 2 * x) / 2]);
             const float2 ds = f2_unpack(fmul2(f2_pack(pp.x, pp.y), diff));
             w[x] = pack_bf16x2(ds.x, ds.y);
           }
-          store_square_chunk(sDSt, t, c * 4 + e / 8, w[0], w[1], w[2], w[3]);
+          store_square_chunk(sDSt, t, (col0 + e) / 8, w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
@@ -453,16 +460,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kBarDsFull]);
     }
     tc_fence_before();
-  } else if (warp < 8) {
+  } else if (warp < kWarpProducer) {
     // ------------------------------------------------------------ dQ drain + epilogue warps
-    const int t = threadIdx.x - 128;  // TMEM lane: query row q0 + t (dQ), key row kv0 + t (dK, dV)
-    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    // dQ_i leaves TMEM in one go (so its columns are released early), then
-    // goes out in kChunk-column pieces: each is written to a swizzled staging
-    // buffer and reduce-added (fp32) into dQacc by one TMA bulk tensor op,
-    // issued by lane 0 of warp 4.  Rows past N fall outside the tensor map and
-    // are dropped by TMA.
-    const bool issuer = warp == 4 && lane == 0;
+    const int t = (warp - kWarpDrain) * 32 + lane;  // TMEM lane: query row q0 + t (dQ), key row kv0 + t (dK, dV)
+    const uint32_t lane_base = static_cast<uint32_t>((warp - kWarpDrain) * 32) << 16;
+    // dQ_i goes out in kChunk-column pieces: each is read from TMEM (the
+    // columns are released after the last piece), written to a swizzled
+    // staging buffer and reduce-added (fp32) into dQacc by one TMA bulk tensor
+    // op, issued by lane 0 of the first drain warp.  Rows past N fall outside
+    // the tensor map and are dropped by TMA.
+    const bool issuer = warp == kWarpDrain && lane == 0;
     const uint32_t sStage = smem_u32(smem + C::kStage);
     bool ok = true;
 #pragma unroll 1
@@ -471,25 +478,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int bh = bh_kv * group + it / n_q;
       if (!(ok = mbar_wait_sleep(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
-      float g[D];
-      if constexpr (D >= 32) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, *reinterpret_cast<float(*)[32]>(g + c * 32));
-      } else {
-        tmem_ld16(tmem + lane_base + C::kColDQ, *reinterpret_cast<float(*)[16]>(g));
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
         const int gi = it * C::kChunks + c, bsel = gi & 1, u = gi >> 1;
+        float g[C::kChunk];
+        if constexpr (C::kChunk == 32)
+          tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
+        else
+          tmem_ld16(tmem + lane_base + C::kColDQ, g);
+        tmem_wait_ld();
+        if (c == C::kChunks - 1) {  // every dQ column has been read: release the TMEM columns
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+        }
         if (gi >= 2 && !(ok = mbar_wait_sleep(&bars[kBarStageFree + bsel], (u - 1) & 1, status))) break;
         const uint32_t sb = sStage + bsel * C::kStageBytes;
 #pragma unroll
         for (int j = 0; j < C::kChunk / 4; ++j) {
-          const float* v4 = g + c * C::kChunk + 4 * j;
+          const float* v4 = g + 4 * j;
           st_shared_v4(sb + swizzle_offset<C::kChunk * 4>(t, j), __float_as_uint(v4[0]), __float_as_uint(v4[1]),
                        __float_as_uint(v4[2]), __float_as_uint(v4[3]));
         }
@@ -559,7 +566,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
