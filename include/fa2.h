@@ -170,6 +170,13 @@ int fa2_device_status(int* value, int reset);
  * Empty if none.  Valid until the next failing call on the same thread. */
 const char* fa2_last_error_detail(void);
 
+/* Failure-detection self-test (no counterpart on the pages): launches a
+ * one-CTA kernel that waits on an mbarrier nothing arrives at, bounded by
+ * timeout_us (1 .. 5e6) microseconds, synchronises, and stores the kernel's
+ * status word in *status_out (1 = the wait timed out and was reported, as
+ * every wait in the attention kernels does after 2 s).  Faults nothing. */
+int fa2_check_wait_timeout(int timeout_us, int* status_out);
+
 /* ABI version of this header (major * 100 + minor). */
 int fa2_abi_version(void);
 

@@ -52,6 +52,7 @@ _SIGNATURES = {
     "fa2_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_gqa_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
                             _vp]),
+    "fa2_check_wait_timeout": (_i, [_i, ctypes.POINTER(_i)]),
 }
 
 

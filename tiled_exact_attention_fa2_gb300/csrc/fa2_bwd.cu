@@ -81,7 +81,8 @@ struct BwdCfg {
   using T = HeadDim<D>;
   static constexpr int kQStages = 2;
   static constexpr int kDoStages = D == 128 ? 1 : 2;  // shared memory is full at D = 128
-  // TMEM: S^T [0,128) (P^T, as bf16 pairs, overwrites its first 64 columns),
+  // TMEM: S^T [0,128) (P^T, as bf16 pairs, overwrites columns [0,32) and
+  // [64,96): each P/dS warpgroup writes inside its own half),
   // dP^T [128,256) (dQ_i reuses these columns once dS^T is formed), dV and dK
   // after them on 32-column boundaries.
   static constexpr int kCols = D < 32 ? 32 : D;
@@ -344,12 +345,14 @@ __global__ void __launch_bounds__(512, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ss(tDP, T::kmajor_desc(sV, kk), T::kmajor_desc(do_s, kk), kIdSq, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarDpFull]);
-        // dV += P^T dO_i, P^T read from the first 64 columns of S^T (TMEM).
+        // dV += P^T dO_i, P^T read from TMEM: query columns [0, 64) as bf16
+        // pairs in S^T columns [0, 32), columns [64, 128) in [64, 96).
         if (!(ok = mbar_wait(&bars[kBarPFull], it & 1, status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ts(tDV, tS + kk * 8, T::mnmajor_desc(do_s, kk), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tDV, tS + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)), T::mnmajor_desc(do_s, kk), kIdKV,
+                      (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarDoEmpty + ds]);
         mma_commit(&bars[kBarDvDone]);
         // S^T(i+1) overwrites the P^T columns dV(i) reads: wait for dV(i).
@@ -402,9 +405,10 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t pk[32];  // this half's 64 weights as bf16 pairs
       const bool row_dead = kv_row >= N;
       const int first = (CAUSAL && i == jt) ? kv_row - q0 : 0;  // queries q0 + c with c < first cannot see this key
-      // P^T goes back to TMEM as bf16 pairs over the first 64 S^T columns, 16
-      // columns per 32 scores: P columns [col0 / 2, col0 / 2 + 16) cover S
-      // columns [col0, col0 + 32), which are already in registers.
+      // P^T goes back to TMEM as bf16 pairs inside this warpgroup's own S^T
+      // columns (the other warpgroup may still be reading its half): the 64
+      // weights of columns [64 hh, 64 hh + 64) land in TMEM columns
+      // [64 hh, 64 hh + 32), 16 per 32 scores, over S columns already read.
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int col0 = 64 * hh + 32 * c;
@@ -422,7 +426,7 @@ __global__ void __launch_bounds__(512, 1)
           if (row_dead || col + 1 < first) p1 = 0.f;
           pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
         }
-        tmem_st16u(tmem + lane_base + C::kColS + col0 / 2, pk + 16 * c);
+        tmem_st16u(tmem + lane_base + C::kColS + 64 * hh + 16 * c, pk + 16 * c);
       }
       tmem_wait_st();
       tc_fence_before();

@@ -104,9 +104,11 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t 
 }
 
 // Wait until the phase with the given parity has completed.  Bounded: returns
-// false (and records kDevWaitTimeout in *status) after FA2_WAIT_TIMEOUT_NS.
+// false (and records kDevWaitTimeout in *status) after timeout_ns of
+// %globaltimer time (FA2_WAIT_TIMEOUT_NS unless given).
 template <bool SLEEP = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint64_t timeout_ns = FA2_WAIT_TIMEOUT_NS) {
   const uint32_t a = smem_u32(bar);
   auto test = [&]() { return SLEEP ? mbar_try_wait_sleep(a, parity) : mbar_try_wait(a, parity); };
 #pragma unroll 1
@@ -118,7 +120,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 #pragma unroll 1
     for (int i = 0; i < (SLEEP ? 16 : 256); ++i)
       if (test()) return true;
-    if (global_timer_ns() - t0 > FA2_WAIT_TIMEOUT_NS) {
+    if (global_timer_ns() - t0 > timeout_ns) {
       atomicCAS(status, kDevOk, kDevWaitTimeout);
       return false;
     }
