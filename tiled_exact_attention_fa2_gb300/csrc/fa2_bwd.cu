@@ -482,25 +482,35 @@ __global__ void __launch_bounds__(512, 1)
       const int bh = bh_kv * group + it / n_q;
       if (!(ok = mbar_wait_sleep(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
+      // Pieces are read from TMEM two at a time (64 registers); the columns
+      // are released right after the last read, before the staging of the
+      // last two pieces can wait on earlier reduces.
+      float g[2][C::kChunk];
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
         const int gi = it * C::kChunks + c, bsel = gi & 1, u = gi >> 1;
-        float g[C::kChunk];
-        if constexpr (C::kChunk == 32)
-          tmem_ld32(tmem + lane_base + C::kColDQ + c * 32, g);
-        else
-          tmem_ld16(tmem + lane_base + C::kColDQ, g);
-        tmem_wait_ld();
-        if (c == C::kChunks - 1) {  // every dQ column has been read: release the TMEM columns
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+        if ((c & 1) == 0) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (c + k < C::kChunks) {
+              if constexpr (C::kChunk == 32)
+                tmem_ld32(tmem + lane_base + C::kColDQ + (c + k) * 32, g[k]);
+              else
+                tmem_ld16(tmem + lane_base + C::kColDQ, g[k]);
+            }
+          }
+          tmem_wait_ld();
+          if (c + 2 >= C::kChunks) {  // every dQ column has been read: release the TMEM columns
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+          }
         }
         if (gi >= 2 && !(ok = mbar_wait_sleep(&bars[kBarStageFree + bsel], (u - 1) & 1, status))) break;
         const uint32_t sb = sStage + bsel * C::kStageBytes;
 #pragma unroll
         for (int j = 0; j < C::kChunk / 4; ++j) {
-          const float* v4 = g + 4 * j;
+          const float* v4 = g[c & 1] + 4 * j;
           st_shared_v4(sb + swizzle_offset<C::kChunk * 4>(t, j), __float_as_uint(v4[0]), __float_as_uint(v4[1]),
                        __float_as_uint(v4[2]), __float_as_uint(v4[3]));
         }
