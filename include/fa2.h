@@ -97,6 +97,29 @@ int fa2_bwd_gqa_ws(const void* q, const void* k, const void* v, const void* o, c
                    void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale, int causal,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Split-KV forward ("flash-decoding", named as a next primitive in the
+ * article's section "Next Frontiers in WebGPU ML"), for queries shorter than
+ * the key/value sequence (decoding against a key-value cache).
+ * q, o: [B, H, Nq, d]; k, v: [B, H_kv, Nk, d]; lse: [B, H, Nq]; H a multiple
+ * of H_kv.  With causal != 0 the Nq queries are the last Nq positions of the
+ * Nk-long sequence: query i sees key j iff j <= i + Nk - Nq (Nk >= Nq
+ * required).  The G = H / H_kv query heads of a K/V head are packed into the
+ * rows of one 128-row tile (G * Nq rows per K/V head), so K and V are read
+ * once per group.  The keys are cut into at most num_splits ranges of whole
+ * 128-key tiles processed by separate CTAs; each writes its fp32 partial O
+ * and LSE to the workspace and a combine kernel merges them with
+ * LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
+ * workspace: device pointer, 256-byte aligned, of at least
+ * fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits) bytes (may be
+ * NULL when that is 0, i.e. a single split).  Two launches (one if a single
+ * split).  Other rules as fa2_fwd.
+ */
+size_t fa2_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
+                    int Nk, int d, float scale, int causal, int num_splits, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
 /* Bytes of device scratch fa2_bwd needs: D (fp32 [B,H,N]) and the fp32 dQ
  * accumulator [B,H,N,d], each 256-byte aligned.  0 on invalid sizes. */
 size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);

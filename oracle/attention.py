@@ -45,7 +45,7 @@ import numpy as np
 __all__ = [
     "as_f64", "fp32_scale", "scores", "apply_causal_mask", "row_logsumexp",
     "attn_fwd_head", "attn_bwd_head", "attn_fwd", "attn_bwd", "attn_rows",
-    "attn_bwd_gqa",
+    "attn_bwd_gqa", "attn_fwd_general",
 ]
 
 
@@ -223,3 +223,39 @@ def attn_bwd_gqa(q, k, v, dO, scale: float, causal: bool):
             out["dK"][b, hk] += r["dK"]
             out["dV"][b, hk] += r["dV"]
     return out
+
+
+def attn_fwd_general(q, k, v, scale: float, causal: bool):
+    """Forward pass with separate query and key lengths and grouped K/V heads.
+
+    q is [B, H, Nq, d]; k, v are [B, H_kv, Nk, d] with H a multiple of H_kv
+    (query head h reads key/value head h // (H / H_kv)).  The pages name
+    flash-decoding as a next primitive (article, section "Next Frontiers in
+    WebGPU ML") but give no formula; the plain reading for Nq != Nk is the
+    usual key-value-cache alignment: the Nq queries are the last Nq positions
+    of the Nk-long sequence, so with causal masking query i sees key j iff
+    j <= i + (Nk - Nq).  Requires Nk >= Nq when causal.  Returns
+    (O [B, H, Nq, d], LSE [B, H, Nq]) in fp64.
+    """
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    s = fp32_scale(scale)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if H % Hkv:
+        raise ValueError("H must be a multiple of H_kv")
+    if causal and Nk < Nq:
+        raise ValueError("causal attention needs Nk >= Nq")
+    G = H // Hkv
+    O = np.empty((B, H, Nq, d))
+    L = np.empty((B, H, Nq))
+    i = np.arange(Nq)[:, None]
+    j = np.arange(Nk)[None, :]
+    for b in range(B):
+        for h in range(H):
+            S = scores(q[b, h], k[b, h // G], s)
+            if causal:
+                S = np.where(j > i + (Nk - Nq), -np.inf, S)
+            lse = row_logsumexp(S)
+            O[b, h] = _probabilities(S, lse) @ v[b, h // G]
+            L[b, h] = lse
+    return O, L

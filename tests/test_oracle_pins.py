@@ -383,3 +383,59 @@ def test_gqa_finite_differences_through_shared_kv():
                 lm = loss(args["k"], args["v"])
                 fd[idx] = (lp - lm) / (2 * h)
             assert np.abs(fd - grad).max() < 1e-7 * max(1.0, np.abs(grad).max()), name
+
+
+# ---------------------------------------------------------------------------
+# Separate query / key lengths (key-value-cache alignment) and grouped heads.
+# ---------------------------------------------------------------------------
+
+def test_general_forward_equal_lengths_is_plain_attention():
+    x = workloads.make_inputs(1, 2, 40, 8, seed=501, with_grad=False)
+    for causal in (True, False):
+        a = oracle.attn_fwd_general(x["q"], x["k"], x["v"], 0.3, causal)
+        b = oracle.attn_fwd(x["q"], x["k"], x["v"], 0.3, causal)
+        np.testing.assert_allclose(a[0], b[0], atol=1e-13)
+        np.testing.assert_allclose(a[1], b[1], atol=1e-13)
+
+
+def test_general_forward_is_suffix_of_square_causal_problem():
+    # With Nq < Nk the queries are the last Nq positions: embedding them at the
+    # end of a full-length query block and running square causal attention
+    # must give the same rows.
+    r = np.random.Generator(np.random.PCG64(502))
+    Nk, Nq, d = 23, 5, 6
+    k, v = r.standard_normal((1, 1, Nk, d)), r.standard_normal((1, 1, Nk, d))
+    full_q = r.standard_normal((1, 1, Nk, d))
+    q = full_q[:, :, Nk - Nq:]
+    o, lse = oracle.attn_fwd_general(q, k, v, 0.6, True)
+    o_full, lse_full = oracle.attn_fwd(full_q, k, v, 0.6, True)
+    np.testing.assert_allclose(o, o_full[:, :, Nk - Nq:], atol=1e-12)
+    np.testing.assert_allclose(lse, lse_full[:, :, Nk - Nq:], atol=1e-12)
+
+
+def test_general_forward_against_torch_with_explicit_mask_and_groups():
+    r = np.random.Generator(np.random.PCG64(503))
+    B, H, Hkv, Nq, Nk, d = 2, 6, 3, 4, 19, 8
+    q = r.standard_normal((B, H, Nq, d))
+    k, v = r.standard_normal((B, Hkv, Nk, d)), r.standard_normal((B, Hkv, Nk, d))
+    kr = torch.tensor(k).repeat_interleave(H // Hkv, dim=1)
+    vr = torch.tensor(v).repeat_interleave(H // Hkv, dim=1)
+    for causal in (True, False):
+        mask = None
+        if causal:
+            mask = torch.tensor(np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq))
+        # 0.375 is exact in fp32, so the oracle's fp32 scale equals torch's
+        o = torch.nn.functional.scaled_dot_product_attention(torch.tensor(q), kr, vr, attn_mask=mask, scale=0.375)
+        got, _ = oracle.attn_fwd_general(q, k, v, 0.375, causal)
+        np.testing.assert_allclose(got, o.numpy(), atol=1e-12)
+
+
+def test_single_query_decode_sees_every_key():
+    # Nq = 1 with causal masking: the one query is the last position and sees
+    # all Nk keys, so causal and non-causal agree.
+    x = workloads.make_inputs(1, 2, 1, 16, seed=504, with_grad=False)
+    kv = workloads.make_inputs(1, 2, 33, 16, seed=505, with_grad=False)
+    a = oracle.attn_fwd_general(x["q"], kv["k"], kv["v"], 0.25, True)
+    b = oracle.attn_fwd_general(x["q"], kv["k"], kv["v"], 0.25, False)
+    np.testing.assert_allclose(a[0], b[0], atol=1e-14)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-14)

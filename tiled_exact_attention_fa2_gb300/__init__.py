@@ -22,7 +22,7 @@ from . import _build
 __all__ = [
     "FA2Error", "load_library", "fa2_fwd", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
     "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
-    "fa2_bwd_stages", "fa2_bwd_noalloc", "fa2_fwd_gqa", "fa2_bwd_gqa",
+    "fa2_bwd_stages", "fa2_bwd_noalloc", "fa2_fwd_gqa", "fa2_bwd_gqa", "fa2_fwd_splitkv",
     "FA2_OK",
 ]
 
@@ -53,6 +53,8 @@ _SIGNATURES = {
     "fa2_bwd_gqa_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
                             _vp]),
     "fa2_check_wait_timeout": (_i, [_i, ctypes.POINTER(_i)]),
+    "fa2_fwd_splitkv_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "fa2_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
 }
 
 
@@ -235,6 +237,32 @@ def fa2_bwd_gqa(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optional[
     if rc != FA2_OK:
         raise FA2Error("fa2_bwd_gqa", rc)
     return dq, dk, dv
+
+
+def fa2_fwd_splitkv(q, k, v, num_splits: int, o=None, lse=None, workspace=None, scale: Optional[float] = None,
+                    causal: bool = True, stream=None):
+    """Split-KV forward for Nq <= Nk (decoding): q [B,H,Nq,d], k/v [B,H_kv,Nk,d].
+
+    Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32).  ``workspace`` (a CUDA
+    byte tensor) is allocated here when not given."""
+    lib = load_library()
+    B, H, Nq, d = _shape(q, "q")
+    Bk, Hkv, Nk, dk_ = _shape(k, "k")
+    if (Bk, dk_) != (B, d) or _shape(v, "v") != (B, Hkv, Nk, d):
+        raise ValueError("k and v must be [B, H_kv, Nk, d] with q's B and d")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = lib.fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wptr = workspace.data_ptr() if workspace is not None else None
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.fa2_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq,
+                             Nk, d, _scale(scale, d), 1 if causal else 0, num_splits, wptr, wbytes,
+                             _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_fwd_splitkv", rc)
+    return o, lse
 
 
 def fa2_bwd_noalloc(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optional[float] = None,

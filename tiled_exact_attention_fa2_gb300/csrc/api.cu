@@ -209,7 +209,17 @@ int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse
   TmapSet tm;
   if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, B * H_kv, N, d) || !make_tmap(&tm.v, v, B * H_kv, N, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
-  if (int e = launch_fwd(tm, o, lse, BH, N, d, H / H_kv, scale, causal != 0, static_cast<cudaStream_t>(stream)))
+  FwdProblem p{};
+  p.RH = BH;
+  p.M = N;
+  p.Nq = N;
+  p.Nk = N;
+  p.kvdiv = H / H_kv;
+  p.splits = 1;
+  p.tiles_per_split = (N + kRowsPerTile - 1) / kRowsPerTile;
+  p.o = o;
+  p.lse = lse;
+  if (int e = launch_fwd(tm, p, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
     return cuda_fail(e, "fwd launch");
   return FA2_OK;
 }
@@ -217,6 +227,93 @@ int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
             float scale, int causal, void* stream) {
   return fa2_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
+}
+
+}  // extern "C" (reopened below)
+
+namespace {
+
+// Split plan for fa2_fwd_splitkv: at most `requested` ranges of whole
+// 128-key tiles, none empty.
+void splitkv_plan(int Nk, int requested, int* splits, int* tiles_per_split) {
+  const int tiles = (Nk + kRowsPerTile - 1) / kRowsPerTile;
+  const int want = requested < 1 ? 1 : (requested > tiles ? tiles : requested);
+  *tiles_per_split = (tiles + want - 1) / want;
+  *splits = (tiles + *tiles_per_split - 1) / *tiles_per_split;
+}
+
+int check_splitkv_sizes(int B, int H, int H_kv, int Nq, int Nk, int d, int causal, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_splits < 1) return FA2_ERR_SHAPE;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  if (int rc = check_heads(H, H_kv)) return rc;
+  if (causal && Nk < Nq) return FA2_ERR_SHAPE;
+  const long long rows = static_cast<long long>(H / H_kv) * Nq;  // packed rows per K/V head
+  const long long rh = static_cast<long long>(B) * H_kv;
+  const long long pairs = (rows + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile);
+  if (rows > (1 << 30) || Nk > (1 << 30) || rh * pairs * num_splits > 0x7fffffffLL) return FA2_ERR_SHAPE;
+  return FA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa2_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_splits < 1) return 0;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
+  int splits = 0, tps = 0;
+  splitkv_plan(Nk, num_splits, &splits, &tps);
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(splits) * B * H * Nq;
+  return round_up(rows * d * sizeof(float)) + round_up(rows * sizeof(float));
+}
+
+int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
+                    int Nk, int d, float scale, int causal, int num_splits, void* workspace,
+                    size_t workspace_bytes_given, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
+  if (int rc = check_splitkv_sizes(B, H, H_kv, Nq, Nk, d, causal, num_splits)) return rc;
+  if (int rc = check_scale(scale)) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA2_ERR_ALIGN;
+  const size_t qb = static_cast<size_t>(B) * H * Nq * d * 2;
+  const size_t kb = static_cast<size_t>(B) * H_kv * Nk * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * Nq * 4;
+  const Range ro = range_of(o, qb), rl = range_of(lse, lb);
+  const Range ins[] = {range_of(q, qb), range_of(k, kb), range_of(v, kb)};
+  for (const Range& r : ins)
+    if (overlap(ro, r) || overlap(rl, r)) return FA2_ERR_ALIAS;
+  if (overlap(ro, rl)) return FA2_ERR_ALIAS;
+  const size_t need = fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits);
+  if (need > 0 && (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < need))
+    return FA2_ERR_WORKSPACE;
+
+  // Packed grouped rows: the G query heads of a K/V head and their Nq rows
+  // form one row-head of G * Nq rows ([B * H_kv, G * Nq, d] view of q / o).
+  const int G = H / H_kv;
+  FwdProblem p{};
+  p.RH = B * H_kv;
+  p.M = G * Nq;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.kvdiv = 1;
+  splitkv_plan(Nk, num_splits, &p.splits, &p.tiles_per_split);
+  p.o = o;
+  p.lse = lse;
+  if (p.splits > 1) {
+    const size_t rows = static_cast<size_t>(p.splits) * B * H * Nq;
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * d * sizeof(float)));
+  }
+  TmapSet tm;
+  if (!make_tmap(&tm.q, q, p.RH, p.M, d) || !make_tmap(&tm.k, k, B * H_kv, Nk, d) ||
+      !make_tmap(&tm.v, v, B * H_kv, Nk, d))
+    return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (int e = launch_fwd(tm, p, d, scale, causal != 0, st)) return cuda_fail(e, "split-kv fwd launch");
+  if (p.splits > 1)
+    if (int e = launch_splitkv_combine(p, d, st)) return cuda_fail(e, "split-kv combine launch");
+  return FA2_OK;
 }
 
 size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -79,8 +79,7 @@ struct FwdCfg {
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out_o,
-                   float* __restrict__ out_lse, int BH, int N, int group, float scale_log2) {
+                   const __grid_constant__ CUtensorMap tm_v, const FwdProblem p, float scale_log2) {
   using T = HeadDim<D>;
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -92,16 +91,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // Heaviest query-tile pairs first (causal work grows with the pair index).
-  const int num_tiles = (N + kTileRows - 1) / kTileRows;
-  const int num_pairs = (num_tiles + 1) / 2;
-  const int bh = blockIdx.x % BH;
-  const int bh_kv = bh / group;  // query heads [g*group, (g+1)*group) share K/V head g
-  const int pair = num_pairs - 1 - static_cast<int>(blockIdx.x / BH);
+  // CTA = (key split, pair of 128-row tiles, row-head); heaviest pairs first
+  // within a split (causal work grows with the pair index).  Row r of
+  // row-head rh is query r % Nq; the row-head reads K/V head rh / kvdiv.
+  const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
+  const int num_pairs = (num_row_tiles + 1) / 2;
+  const int num_kv_tiles = (p.Nk + kTileRows - 1) / kTileRows;
+  const int rh = blockIdx.x % p.RH;
+  const int rest = static_cast<int>(blockIdx.x / p.RH);
+  const int pair = num_pairs - 1 - rest % num_pairs;
+  const int split = rest / num_pairs;
+  const int rh_kv = rh / p.kvdiv;
   const int q0 = pair * 2 * kTileRows;
-  // K/V tiles each query tile visits; a tile with no row < N visits none.
-  const int nA = CAUSAL ? 2 * pair + 1 : num_tiles;
-  const int nB = 2 * pair + 1 >= num_tiles ? 0 : (CAUSAL ? 2 * pair + 2 : num_tiles);
+  const int off = p.Nk - p.Nq;  // causal: query i sees key j iff j <= i + off
+  const int jb = split * p.tiles_per_split;
+  const int je = min(num_kv_tiles, jb + p.tiles_per_split);
+  // Local K/V tiles (from jb) each row tile visits, and the smallest query
+  // index among its rows (for the causal-mask test).
+  int cnt[2], imin[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int rx0 = q0 + x * kTileRows;
+    cnt[x] = 0;
+    imin[x] = 0;
+    if (rx0 < p.M) {
+      const int rlast = min(rx0 + kTileRows - 1, p.M - 1);
+      const bool one_head = rx0 / p.Nq == rlast / p.Nq;
+      const int i_max = one_head ? rlast % p.Nq : p.Nq - 1;
+      imin[x] = one_head ? rx0 % p.Nq : 0;
+      const int kv_end = CAUSAL ? min(num_kv_tiles, (i_max + off) / kTileRows + 1) : num_kv_tiles;
+      cnt[x] = max(0, min(je, kv_end) - jb);
+    }
+  }
+  const int nA = cnt[0], nB = cnt[1];
   const int n_kv = nA > nB ? nA : nB;
 
   if (threadIdx.x == 8 * 32) {
@@ -133,12 +155,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int n_q_tiles = nB > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&bars[kBarQ], n_q_tiles * T::kTileBytes);
-      for (int x = 0; x < n_q_tiles; ++x)
-        for (int b = 0; b < T::kNumBoxes; ++b)
-          tma_load_3d(smem + C::kQ + x * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQ], b * T::kBoxCols,
-                      q0 + x * kTileRows, bh);
+      const int n_q_tiles = (nA > 0) + (nB > 0);
+      if (n_q_tiles > 0) mbar_arrive_expect_tx(&bars[kBarQ], n_q_tiles * T::kTileBytes);
+      for (int x = 0; x < 2; ++x)
+        if (cnt[x] > 0)
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_load_3d(smem + C::kQ + x * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQ],
+                        b * T::kBoxCols, q0 + x * kTileRows, rh);
       int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;
 #pragma unroll 1
       for (int j = 0; j < n_kv; ++j) {
@@ -147,17 +170,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
-                      b * T::kBoxCols, j * kTileRows, bh_kv);
+                      b * T::kBoxCols, (jb + j) * kTileRows, rh_kv);
         (st ? last_k1 : last_k0) = j;
         if (j >= 2 && !mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
-                      b * T::kBoxCols, j * kTileRows, bh_kv);
+                      b * T::kBoxCols, (jb + j) * kTileRows, rh_kv);
         (st ? last_v1 : last_v0) = j;
       }
       // Never leave the CTA with a TMA write still landing in shared memory.
-      mbar_wait(&bars[kBarQ], 0, status);
+      if (n_q_tiles > 0) mbar_wait(&bars[kBarQ], 0, status);
       if (last_k0 >= 0) mbar_wait(&bars[kBarKFull + 0], (last_k0 >> 1) & 1, status);
       if (last_k1 >= 0) mbar_wait(&bars[kBarKFull + 1], (last_k1 >> 1) & 1, status);
       if (last_v0 >= 0) mbar_wait(&bars[kBarVFull + 0], (last_v0 >> 1) & 1, status);
@@ -236,7 +259,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------ softmax (tile x)
     const int x = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
-    const int q_row = q0 + x * kTileRows + r;
+    const int q_row = q0 + x * kTileRows + r;  // row in the row-head
+    const int qi = q_row % p.Nq;               // its query index
+    const int imin_x = x ? imin[1] : imin[0];
     const int nx = x == 0 ? nA : nB;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x ? C::kColS1 : C::kColS0);
@@ -256,10 +281,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + 32 * c));
       tmem_wait_ld();
 
-      const int kv0 = j * kTileRows;
-      if ((CAUSAL && j == nx - 1) || kv0 + kTileRows > N) {
-        int lim = N - kv0;                              // keys >= N do not exist
-        if (CAUSAL) lim = min(lim, q_row - kv0 + 1);    // key j visible iff j <= query
+      const int kv0 = (jb + j) * kTileRows;
+      if ((CAUSAL && kv0 + kTileRows - 1 > imin_x + off) || kv0 + kTileRows > p.Nk) {
+        int lim = p.Nk - kv0;                                // keys >= Nk do not exist
+        if (CAUSAL) lim = min(lim, qi + off - kv0 + 1);      // key j visible iff j <= query + off
 #pragma unroll
         for (int e = 0; e < 128; ++e)
           if (e >= lim) s[e] = -INFINITY;
@@ -334,43 +359,51 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       m = m_use;
     }
     // ------------------------------------------------------------ epilogue
-    if (nx > 0 && ok && mbar_wait(&bars[kBarPVDone + x], (nx - 1) & 1, status)) {
+    // One split: O / l in bf16 and LSE.  Several splits: this split's O / l
+    // and LSE in fp32 for the combine kernel (a split that sees no key of a
+    // row leaves O = 0, LSE = -inf there).
+    const bool valid = q_row < p.M;
+    const bool partial = p.splits > 1;
+    const size_t row_idx = (partial ? static_cast<size_t>(split) * p.RH + rh : static_cast<size_t>(rh)) * p.M +
+                           (valid ? q_row : 0);
+    if (nx == 0) {
+      if (partial && valid && ok) {
+        float4* dst = reinterpret_cast<float4*>(p.o_part + row_idx * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.lse_part[row_idx] = -INFINITY;
+      }
+    } else if (ok && mbar_wait(&bars[kBarPVDone + x], (nx - 1) & 1, status)) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool valid = q_row < N;
-      __nv_bfloat16* orow = out_o + (static_cast<size_t>(bh) * N + (valid ? q_row : 0)) * D;
-      if constexpr (D >= 32) {
+      constexpr int kC = D >= 32 ? 32 : 16;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
+      for (int c = 0; c < D / kC; ++c) {
+        float o[kC];
+        if constexpr (kC == 32)
           tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        else
+          tmem_ld16(tO, o);
+        tmem_wait_ld();
+        if (valid) {
+          if (partial) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + row_idx * D + c * kC);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < kC / 4; ++q)
+              dst[q] = make_float4(o[4 * q] * inv_l, o[4 * q + 1] * inv_l, o[4 * q + 2] * inv_l, o[4 * q + 3] * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + row_idx * D + c * kC);
+#pragma unroll
+            for (int q = 0; q < kC / 8; ++q)
               dst[q] = make_uint4(pack_bf16x2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l),
                                   pack_bf16x2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l),
                                   pack_bf16x2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l),
                                   pack_bf16x2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l));
           }
         }
-      } else {
-        float o[16];
-        tmem_ld16(tO, o);
-        tmem_wait_ld();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            dst[q] = make_uint4(pack_bf16x2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l),
-                                pack_bf16x2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l),
-                                pack_bf16x2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l),
-                                pack_bf16x2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l));
-        }
       }
       // LSE in natural log of the scaled scores: ln 2 * (m + log2 l).
-      if (valid) out_lse[static_cast<size_t>(bh) * N + q_row] = (m + log2f(l)) * 0.69314718055994531f;
+      if (valid) (partial ? p.lse_part : p.lse)[row_idx] = (m + log2f(l)) * 0.69314718055994531f;
     }
     tc_fence_before();
   }
@@ -383,35 +416,82 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 template <int D, bool CAUSAL>
-int launch_fwd_t(const TmapSet& tm, void* o, float* lse, int BH, int N, int group, float scale,
-                 cudaStream_t stream) {
+int launch_fwd_t(const TmapSet& tm, const FwdProblem& p, float scale, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fa2_fwd_kernel<D, CAUSAL>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
-  const int num_tiles = (N + kTileRows - 1) / kTileRows;
-  const int num_pairs = (num_tiles + 1) / 2;
-  const dim3 grid(static_cast<unsigned>(num_pairs) * static_cast<unsigned>(BH));
+  const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
+  const int num_pairs = (num_row_tiles + 1) / 2;
+  const dim3 grid(static_cast<unsigned>(num_pairs) * static_cast<unsigned>(p.RH) * static_cast<unsigned>(p.splits));
   const float scale_log2 = scale * 1.44269504088896341f;
-  kern<<<grid, kFwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, static_cast<__nv_bfloat16*>(o), lse, BH, N,
-                                                  group, scale_log2);
+  kern<<<grid, kFwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, p, scale_log2);
   return static_cast<int>(cudaGetLastError());
+}
+
+// Merge per-split results: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
+// One warp per row; lane l holds columns [l * D / 32, (l + 1) * D / 32).
+template <int D>
+__global__ void __launch_bounds__(256) fa2_splitkv_combine_kernel(const float* __restrict__ o_part,
+                                                                  const float* __restrict__ lse_part,
+                                                                  __nv_bfloat16* __restrict__ o,
+                                                                  float* __restrict__ lse, long long rows,
+                                                                  int splits) {
+  constexpr int kPer = D >= 32 ? D / 32 : 1;  // columns per lane
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, lse_part[static_cast<size_t>(s) * rows + row]);
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  float total = -INFINITY;
+  if (mx != -INFINITY) {
+    float sum = 0.f;
+    for (int s = 0; s < splits; ++s) sum += expf(lse_part[static_cast<size_t>(s) * rows + row] - mx);
+    total = mx + logf(sum);
+    const bool active = D >= 32 || lane < D;
+    for (int s = 0; s < splits; ++s) {
+      const float w = expf(lse_part[static_cast<size_t>(s) * rows + row] - total);
+      if (w == 0.f || !active) continue;
+      const float* src = o_part + (static_cast<size_t>(s) * rows + row) * D + lane * kPer;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) acc[k] = fmaf(w, src[k], acc[k]);
+    }
+  }
+  if (D >= 32 || lane < D) {
+    __nv_bfloat16* dst = o + static_cast<size_t>(row) * D + lane * kPer;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) dst[k] = __float2bfloat16_rn(acc[k]);
+  }
+  if (lane == 0) lse[row] = total;
 }
 
 }  // namespace
 
-int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, int group, float scale, bool causal,
-               cudaStream_t stream) {
+int launch_fwd(const TmapSet& tm, const FwdProblem& p, int d, float scale, bool causal, cudaStream_t stream) {
   switch (d) {
-    case 16: return causal ? launch_fwd_t<16, true>(tm, o, lse, BH, N, group, scale, stream)
-                           : launch_fwd_t<16, false>(tm, o, lse, BH, N, group, scale, stream);
-    case 32: return causal ? launch_fwd_t<32, true>(tm, o, lse, BH, N, group, scale, stream)
-                           : launch_fwd_t<32, false>(tm, o, lse, BH, N, group, scale, stream);
-    case 64: return causal ? launch_fwd_t<64, true>(tm, o, lse, BH, N, group, scale, stream)
-                           : launch_fwd_t<64, false>(tm, o, lse, BH, N, group, scale, stream);
-    case 128: return causal ? launch_fwd_t<128, true>(tm, o, lse, BH, N, group, scale, stream)
-                            : launch_fwd_t<128, false>(tm, o, lse, BH, N, group, scale, stream);
+    case 16: return causal ? launch_fwd_t<16, true>(tm, p, scale, stream) : launch_fwd_t<16, false>(tm, p, scale, stream);
+    case 32: return causal ? launch_fwd_t<32, true>(tm, p, scale, stream) : launch_fwd_t<32, false>(tm, p, scale, stream);
+    case 64: return causal ? launch_fwd_t<64, true>(tm, p, scale, stream) : launch_fwd_t<64, false>(tm, p, scale, stream);
+    case 128:
+      return causal ? launch_fwd_t<128, true>(tm, p, scale, stream) : launch_fwd_t<128, false>(tm, p, scale, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
+}
+
+int launch_splitkv_combine(const FwdProblem& p, int d, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.RH) * p.M;
+  const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+  auto o = static_cast<__nv_bfloat16*>(p.o);
+  switch (d) {
+    case 16: fa2_splitkv_combine_kernel<16><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
+    case 32: fa2_splitkv_combine_kernel<32><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
+    case 64: fa2_splitkv_combine_kernel<64><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
+    case 128: fa2_splitkv_combine_kernel<128><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+  return static_cast<int>(cudaGetLastError());
 }
 
 int read_fwd_status(int* value, bool reset) {

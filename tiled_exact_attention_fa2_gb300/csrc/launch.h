@@ -17,10 +17,26 @@ struct TmapSet {
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).
 int ensure_max_smem(const void* kernel, int bytes);
 
-// BH counts query heads (B * H); query head bh reads K/V head bh / group
-// (group = H / H_kv, 1 for ordinary attention).
-int launch_fwd(const TmapSet& tm, void* o, float* lse, int BH, int N, int d, int group, float scale, bool causal,
-               cudaStream_t stream);
+// Forward problem in row-head form.  The query / output tensors are viewed
+// as [RH, M, d]; row r of row-head rh is query r % Nq and reads K/V head
+// rh / kvdiv ([B * H_kv, Nk, d] view).  Plain attention: RH = B * H, M = Nq,
+// kvdiv = H / H_kv.  Packed grouped decoding: RH = B * H_kv, M = (H / H_kv) *
+// Nq, kvdiv = 1 (all query heads of a group share one 128-row tile).  With
+// causal masking query i sees key j iff j <= i + Nk - Nq.  The keys are cut
+// into `splits` ranges of tiles_per_split 128-key tiles; with one split the
+// kernel writes bf16 o and lse, with more it writes per-split fp32 results
+// to o_part [splits, RH, M, d] / lse_part [splits, RH, M] for
+// launch_splitkv_combine.
+struct FwdProblem {
+  int RH, M, Nq, Nk, kvdiv, splits, tiles_per_split;
+  void* o;
+  float* lse;
+  float* o_part;
+  float* lse_part;
+};
+
+int launch_fwd(const TmapSet& tm, const FwdProblem& p, int d, float scale, bool causal, cudaStream_t stream);
+int launch_splitkv_combine(const FwdProblem& p, int d, cudaStream_t stream);
 int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int BH, int N, int d,
                           cudaStream_t stream);
 // BH counts query heads; one CTA per (key/value tile, K/V head) loops over the
