@@ -76,7 +76,9 @@ struct FwdCfg {
   static constexpr int kBytes = (kUsed + 1024) > 116 * 1024 ? (kUsed + 1024) : 116 * 1024;
 };
 
-template <int D, bool CAUSAL>
+// GENERAL = false compiles the plain prefill case (M = Nq = Nk, one split),
+// where a row's query index is the row itself and the causal offset is 0.
+template <int D, bool CAUSAL, bool GENERAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdProblem p, float scale_log2) {
@@ -103,24 +105,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int split = rest / num_pairs;
   const int rh_kv = rh / p.kvdiv;
   const int q0 = pair * 2 * kTileRows;
-  const int off = p.Nk - p.Nq;  // causal: query i sees key j iff j <= i + off
+  const int off = GENERAL ? p.Nk - p.Nq : 0;  // causal: query i sees key j iff j <= i + off
   const int jb = split * p.tiles_per_split;
   const int je = min(num_kv_tiles, jb + p.tiles_per_split);
   // Local K/V tiles (from jb) each row tile visits, and the smallest query
   // index among its rows (for the causal-mask test).
   int cnt[2], imin[2];
+  if constexpr (!GENERAL) {
+    // Square problem: tile A sees tiles 0..2*pair (causal), tile B one more.
+    cnt[0] = CAUSAL ? 2 * pair + 1 : num_kv_tiles;
+    cnt[1] = 2 * pair + 1 >= num_row_tiles ? 0 : (CAUSAL ? 2 * pair + 2 : num_kv_tiles);
+    imin[0] = q0;
+    imin[1] = q0 + kTileRows;
+  } else {
 #pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    const int rx0 = q0 + x * kTileRows;
-    cnt[x] = 0;
-    imin[x] = 0;
-    if (rx0 < p.M) {
-      const int rlast = min(rx0 + kTileRows - 1, p.M - 1);
-      const bool one_head = rx0 / p.Nq == rlast / p.Nq;
-      const int i_max = one_head ? rlast % p.Nq : p.Nq - 1;
-      imin[x] = one_head ? rx0 % p.Nq : 0;
-      const int kv_end = CAUSAL ? min(num_kv_tiles, (i_max + off) / kTileRows + 1) : num_kv_tiles;
-      cnt[x] = max(0, min(je, kv_end) - jb);
+    for (int x = 0; x < 2; ++x) {
+      const int rx0 = q0 + x * kTileRows;
+      cnt[x] = 0;
+      imin[x] = 0;
+      if (rx0 < p.M) {
+        const int rlast = min(rx0 + kTileRows - 1, p.M - 1);
+        const bool one_head = rx0 / p.Nq == rlast / p.Nq;
+        const int i_max = one_head ? rlast % p.Nq : p.Nq - 1;
+        imin[x] = one_head ? rx0 % p.Nq : 0;
+        const int kv_end = CAUSAL ? min(num_kv_tiles, (i_max + off) / kTileRows + 1) : num_kv_tiles;
+        cnt[x] = max(0, min(je, kv_end) - jb);
+      }
     }
   }
   const int nA = cnt[0], nB = cnt[1];
@@ -260,7 +270,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int x = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
     const int q_row = q0 + x * kTileRows + r;  // row in the row-head
-    const int qi = q_row % p.Nq;               // its query index
+    const int qi = GENERAL ? q_row % p.Nq : q_row;  // its query index
     const int imin_x = x ? imin[1] : imin[0];
     const int nx = x == 0 ? nA : nB;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_wait_ld();
 
       const int kv0 = (jb + j) * kTileRows;
-      if ((CAUSAL && kv0 + kTileRows - 1 > imin_x + off) || kv0 + kTileRows > p.Nk) {
+      if ((CAUSAL && (GENERAL ? kv0 + kTileRows - 1 > imin_x + off : j == nx - 1)) || kv0 + kTileRows > p.Nk) {
         int lim = p.Nk - kv0;                                // keys >= Nk do not exist
         if (CAUSAL) lim = min(lim, qi + off - kv0 + 1);      // key j visible iff j <= query + off
 #pragma unroll
@@ -363,10 +373,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // and LSE in fp32 for the combine kernel (a split that sees no key of a
     // row leaves O = 0, LSE = -inf there).
     const bool valid = q_row < p.M;
-    const bool partial = p.splits > 1;
+    const bool partial = GENERAL && p.splits > 1;
     const size_t row_idx = (partial ? static_cast<size_t>(split) * p.RH + rh : static_cast<size_t>(rh)) * p.M +
                            (valid ? q_row : 0);
-    if (nx == 0) {
+    if (GENERAL && nx == 0) {
       if (partial && valid && ok) {
         float4* dst = reinterpret_cast<float4*>(p.o_part + row_idx * D);
 #pragma unroll
@@ -386,7 +396,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_ld16(tO, o);
         tmem_wait_ld();
         if (valid) {
-          if (partial) {
+          if (GENERAL && partial) {
             float4* dst = reinterpret_cast<float4*>(p.o_part + row_idx * D + c * kC);
 #pragma unroll
             for (int q = 0; q < kC / 4; ++q)
@@ -418,7 +428,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int D, bool CAUSAL>
 int launch_fwd_t(const TmapSet& tm, const FwdProblem& p, float scale, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa2_fwd_kernel<D, CAUSAL>;
+  const bool general = p.splits > 1 || p.M != p.Nq || p.Nq != p.Nk;
+  auto kern = general ? fa2_fwd_kernel<D, CAUSAL, true> : fa2_fwd_kernel<D, CAUSAL, false>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
