@@ -42,7 +42,26 @@ METRIC = "causal bf16 FA2 fwd / bwd TFLOPS and % of GB300 dense bf16 peak (1 GPU
 # capture of the same kernel build on this workload; None when no capture of
 # the current kernel exists.  The profile summary under profiles/ names the
 # command that produced the figure.
-DOMINANT_KERNEL_TRAFFIC = {}
+DOMINANT_KERNEL_TRAFFIC = {
+    # profiles/dram_traffic_long_causal.md: dram__bytes_read.sum 810.06 MB +
+    # dram__bytes_write.sum 485.51 MB for one fa2_bwd_kernel<128, causal> launch.
+    ("fa2_bwd_kernel", "long", True): 810.06e6 + 485.51e6,
+    # same capture: 406.10 MB + 116.85 MB for one fa2_fwd_kernel<128, causal> launch.
+    ("fa2_fwd_kernel", "long", True): 406.10e6 + 116.85e6,
+}
+
+
+def algorithmic_bytes(kernel, B, H, N, d):
+    """HBM bytes a kernel must move at least, per launch.
+
+    Forward: read Q, K, V (bf16), write O (bf16) and LSE (fp32).  Backward
+    main kernel: read Q, K, V, dO (bf16), LSE and D (fp32); write dK, dV
+    (bf16) and the fp32 dQ accumulator once.
+    """
+    rows = B * H * N
+    if kernel == "fa2_fwd_kernel":
+        return rows * (4 * d * 2 + 4)
+    return rows * (6 * d * 2 + d * 4 + 8)
 
 
 def _peaks():
@@ -317,6 +336,7 @@ def run_gpu(args, w, causal):
                      "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "frac": dom_tf / peaks["bf16_tflops_sustained"],
                      "traffic": DOMINANT_KERNEL_TRAFFIC.get((dominant, w.name, causal)),
+                     "algorithmic_bytes": algorithmic_bytes(dominant, B, H, N, d),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
                      "frac_of_burst": dom_tf / peaks["bf16_tflops"]},
         "gpu_launches": 4 * args.steps,

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(512, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse,
                    const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                   int BH, int N, int group, float scale, float scale_log2) {
+                   int BH, int N, int group, int heads_per_group, float scale, float scale_log2) {
   using T = HeadDim<D>;
   using C = BwdCfg<D>;
   constexpr int SQ = C::kQStages, SD = C::kDoStages;
@@ -198,9 +198,17 @@ __global__ void __launch_bounds__(512, 1)
   // `group` query heads that share the K/V head, so dK and dV accumulate the
   // group sum in TMEM.  Iteration it covers query head g = it / n_q, query
   // tile i = i_begin + it % n_q.
+  // CTAs come in groups of `heads_per_group` K/V heads, so that the group's
+  // Q, dO and fp32 dQ rows stay in L2 while its CTAs run; inside a group the
+  // key/value tile index is the slow one (causal work shrinks with jt, so
+  // heavy tiles go first).
   const int BHkv = BH / group;
-  const int bh_kv = blockIdx.x % BHkv;
-  const int jt = blockIdx.x / BHkv;  // key/value tile; causal work shrinks with jt, so heavy tiles go first
+  const int per_group = heads_per_group * num_tiles;
+  const int hg0 = static_cast<int>(blockIdx.x / per_group) * heads_per_group;
+  const int within = static_cast<int>(blockIdx.x % per_group);
+  const int hg = min(heads_per_group, BHkv - hg0);
+  const int jt = within / hg;  // key/value tile
+  const int bh_kv = hg0 + within % hg;
   const int kv0 = jt * kTileRows;
   const int i_begin = CAUSAL ? jt : 0;
   const int n_q = num_tiles - i_begin;
@@ -605,9 +613,13 @@ int launch_bwd_main_t(const TmapSet& tm, const float* lse, const float* Dvec, vo
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_tiles = (N + kTileRows - 1) / kTileRows;
   const dim3 grid(static_cast<unsigned>(num_tiles) * static_cast<unsigned>(BH / group));
+  // Bytes one K/V head's CTAs keep re-reading: Q, dO (bf16), the fp32 dQ
+  // accumulator and LSE, D of its `group` query heads.
+  const size_t per_head = static_cast<size_t>(group) * N * (static_cast<size_t>(D) * 8 + 8);
+  const int hpg = heads_per_l2_group(per_head, BH / group);
   kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, tm.dqacc, lse, Dvec,
                                                   static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-                                                  BH, N, group, scale, scale * kLog2e);
+                                                  BH, N, group, hpg, scale, scale * kLog2e);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -93,16 +93,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // CTA = (key split, pair of 128-row tiles, row-head); heaviest pairs first
-  // within a split (causal work grows with the pair index).  Row r of
-  // row-head rh is query r % Nq; the row-head reads K/V head rh / kvdiv.
+  // CTA = (key split, group of heads_per_group row-heads, pair of 128-row
+  // tiles, row-head), slowest first: a group's K/V rows stay in L2 while its
+  // CTAs run, and inside a group the heaviest pairs go first (causal work
+  // grows with the pair index).  Row r of row-head rh is query r % Nq; the
+  // row-head reads K/V head rh / kvdiv.
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
   const int num_kv_tiles = (p.Nk + kTileRows - 1) / kTileRows;
-  const int rh = blockIdx.x % p.RH;
-  const int rest = static_cast<int>(blockIdx.x / p.RH);
-  const int pair = num_pairs - 1 - rest % num_pairs;
-  const int split = rest / num_pairs;
+  const int per_split = num_pairs * p.RH;
+  const int split = static_cast<int>(blockIdx.x / per_split);
+  const int local = static_cast<int>(blockIdx.x % per_split);
+  const int per_group = p.heads_per_group * num_pairs;
+  const int hg0 = local / per_group * p.heads_per_group;
+  const int hg = min(p.heads_per_group, p.RH - hg0);
+  const int pair = num_pairs - 1 - (local % per_group) / hg;
+  const int rh = hg0 + (local % per_group) % hg;
   const int rh_kv = rh / p.kvdiv;
   const int q0 = pair * 2 * kTileRows;
   const int off = GENERAL ? p.Nk - p.Nq : 0;  // causal: query i sees key j iff j <= i + off
@@ -426,9 +432,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 template <int D, bool CAUSAL>
-int launch_fwd_t(const TmapSet& tm, const FwdProblem& p, float scale, cudaStream_t stream) {
+int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stream) {
   using C = FwdCfg<D>;
   const bool general = p.splits > 1 || p.M != p.Nq || p.Nq != p.Nk;
+  // Every row-head re-reads the K and V rows of its split.
+  const int kv_rows = min(p.Nk, p.tiles_per_split * kTileRows);
+  p.heads_per_group = heads_per_l2_group(static_cast<size_t>(kv_rows) * D * 4 / p.kvdiv, p.RH);
   auto kern = general ? fa2_fwd_kernel<D, CAUSAL, true> : fa2_fwd_kernel<D, CAUSAL, false>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;

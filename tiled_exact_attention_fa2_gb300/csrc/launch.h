@@ -17,6 +17,19 @@ struct TmapSet {
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).
 int ensure_max_smem(const void* kernel, int bytes);
 
+// The attention kernels order their CTAs head-group-major: all CTAs of a
+// group of heads run before the next group's, so the rows every CTA of a head
+// re-reads (K/V in the forward pass, Q/dO/dQ in the backward pass) are read
+// from HBM about once per group instead of once per wave of CTAs.  A group's
+// re-read set is kept to about a quarter of the L2.
+constexpr size_t kL2GroupBytes = size_t(32) << 20;
+inline int heads_per_l2_group(size_t bytes_per_head, int heads) {
+  size_t g = bytes_per_head ? kL2GroupBytes / bytes_per_head : static_cast<size_t>(heads);
+  if (g < 1) g = 1;
+  if (g > static_cast<size_t>(heads)) g = static_cast<size_t>(heads);
+  return static_cast<int>(g);
+}
+
 // Forward problem in row-head form.  The query / output tensors are viewed
 // as [RH, M, d]; row r of row-head rh is query r % Nq and reads K/V head
 // rh / kvdiv ([B * H_kv, Nk, d] view).  Plain attention: RH = B * H, M = Nq,
@@ -29,6 +42,7 @@ int ensure_max_smem(const void* kernel, int bytes);
 // launch_splitkv_combine.
 struct FwdProblem {
   int RH, M, Nq, Nk, kvdiv, splits, tiles_per_split;
+  int heads_per_group;  // row-heads per CTA group (set by launch_fwd)
   void* o;
   float* lse;
   float* o_part;
