@@ -32,7 +32,12 @@ Readings where the pages are silent (each is stated again where it is used):
   * a row with no visible key (impossible for N_q = N_k causal) has O = 0,
     LSE = -inf and zero gradients;
   * inputs are the bf16 values the GPU receives, widened exactly to fp64, and
-    the scale is the fp32 value the GPU receives, widened to fp64.
+    the scale is the fp32 value the GPU receives, widened to fp64;
+  * separate query / key lengths (attn_fwd_general, attn_varlen) align the
+    queries with the end of the keys (key-value-cache alignment): query i
+    sees key j iff j <= i + Nk - Nq under causal masking;
+  * a variable-length batch (attn_varlen) is packed [total, H, d] with
+    cu_seqlens offsets, LSE [H, total_q]; sequences never see each other.
 
 Every function here is pinned by tests/test_oracle_pins.py against closed
 forms, invariants, central finite differences, a brute-force scalar loop and
@@ -45,7 +50,7 @@ import numpy as np
 __all__ = [
     "as_f64", "fp32_scale", "scores", "apply_causal_mask", "row_logsumexp",
     "attn_fwd_head", "attn_bwd_head", "attn_fwd", "attn_bwd", "attn_rows",
-    "attn_bwd_gqa", "attn_fwd_general",
+    "attn_bwd_gqa", "attn_fwd_general", "attn_varlen",
 ]
 
 
@@ -259,3 +264,68 @@ def attn_fwd_general(q, k, v, scale: float, causal: bool):
             O[b, h] = _probabilities(S, lse) @ v[b, h // G]
             L[b, h] = lse
     return O, L
+
+
+def attn_varlen(q, k, v, dO, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool):
+    """Variable-length batch: forward (and backward when dO is given), fp64.
+
+    The pages do not treat batches of sequences of different lengths; this is
+    the usual packed form of the same attention (read here the plainest way):
+    q, dO are [total_q, H, d], k, v are [total_k, H_kv, d]; sequence b owns
+    query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1] - 1 and key rows
+    cu_seqlens_k[b] .. cu_seqlens_k[b+1] - 1, and attends only within itself.
+    Query head h reads key/value head h // (H / H_kv).  With causal masking
+    the Lq queries of a sequence are its last Lq positions (key-value-cache
+    alignment, as in attn_fwd_general): query i sees key j iff
+    j <= i + (Lk - Lq).  A query that sees no key (Lk = 0, or Lk < Lq under
+    causal masking) gets O = 0, LSE = -inf and zero gradients.
+    Returns a dict with O [total_q, H, d] and LSE [H, total_q]; with dO also
+    dQ [total_q, H, d], dK and dV [total_k, H_kv, d].
+    """
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    dO = None if dO is None else as_f64(dO)
+    cq = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    ck = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    if len(cq) != len(ck) or cq[0] != 0 or ck[0] != 0:
+        raise ValueError("cu_seqlens must start at 0 and have the same length")
+    if any(b < a for a, b in zip(cq, cq[1:])) or any(b < a for a, b in zip(ck, ck[1:])):
+        raise ValueError("cu_seqlens must be non-decreasing")
+    s = fp32_scale(scale)
+    total_q, H, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if cq[-1] != total_q or ck[-1] != total_k:
+        raise ValueError("cu_seqlens must end at the packed lengths")
+    if H % Hkv:
+        raise ValueError("H must be a multiple of H_kv")
+    G = H // Hkv
+    out = {"O": np.zeros((total_q, H, d)), "LSE": np.full((H, total_q), -np.inf)}
+    if dO is not None:
+        out["dQ"] = np.zeros((total_q, H, d))
+        out["dK"] = np.zeros((total_k, Hkv, d))
+        out["dV"] = np.zeros((total_k, Hkv, d))
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        Lq, Lk = q1 - q0, k1 - k0
+        if Lq == 0 or Lk == 0:
+            continue  # no query, or nothing to see: outputs stay 0 / -inf
+        i = np.arange(Lq)[:, None]
+        j = np.arange(Lk)[None, :]
+        for h in range(H):
+            hk = h // G
+            S = scores(q[q0:q1, h], k[k0:k1, hk], s)
+            if causal:
+                S = np.where(j > i + (Lk - Lq), -np.inf, S)
+            lse = row_logsumexp(S)
+            P = _probabilities(S, lse)
+            O = P @ v[k0:k1, hk]
+            out["O"][q0:q1, h] = O
+            out["LSE"][h, q0:q1] = lse
+            if dO is None:
+                continue
+            g = dO[q0:q1, h]
+            D = (g * O).sum(axis=1)
+            dS = P * (g @ v[k0:k1, hk].T - D[:, None])
+            out["dQ"][q0:q1, h] = s * (dS @ k[k0:k1, hk])
+            out["dK"][k0:k1, hk] += s * (dS.T @ q[q0:q1, h])
+            out["dV"][k0:k1, hk] += P.T @ g
+    return out

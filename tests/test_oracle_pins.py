@@ -154,13 +154,20 @@ def pin_finite_differences(impl):
 
 
 def _brute_force(q, k, v, dO, s, causal):
-    """Scalar-loop attention written independently of the oracle (pure Python)."""
-    N, d = len(q), len(q[0])
+    """Scalar-loop attention written independently of the oracle (pure Python).
+
+    len(q) queries, len(k) keys; with causal masking query i sees key j iff
+    j <= i + len(k) - len(q).  A query that sees nothing gets O = 0, LSE = -inf.
+    """
+    N, Nk, d = len(q), len(k), len(q[0])
+    off = Nk - N
     O = [[0.0] * d for _ in range(N)]
-    LSE = [0.0] * N
-    P = [[0.0] * N for _ in range(N)]
+    LSE = [-math.inf] * N
+    P = [[0.0] * Nk for _ in range(N)]
     for i in range(N):
-        vis = [j for j in range(N) if (not causal or j <= i)]
+        vis = [j for j in range(Nk) if (not causal or j <= i + off)]
+        if not vis:
+            continue
         logits = {j: s * sum(q[i][c] * k[j][c] for c in range(d)) for j in vis}
         top = max(logits.values())
         tot = sum(math.exp(x - top) for x in logits.values())
@@ -170,11 +177,11 @@ def _brute_force(q, k, v, dO, s, causal):
         for c in range(d):
             O[i][c] = sum(P[i][j] * v[j][c] for j in vis)
     dQ = [[0.0] * d for _ in range(N)]
-    dK = [[0.0] * d for _ in range(N)]
-    dV = [[0.0] * d for _ in range(N)]
+    dK = [[0.0] * d for _ in range(Nk)]
+    dV = [[0.0] * d for _ in range(Nk)]
     for i in range(N):
         # dL/dlogit_ij = p_ij * dO_i . (v_j - O_i)
-        for j in range(N):
+        for j in range(Nk):
             if P[i][j] == 0.0:
                 continue
             g = P[i][j] * sum(dO[i][c] * (v[j][c] - O[i][c]) for c in range(d))
@@ -439,3 +446,183 @@ def test_single_query_decode_sees_every_key():
     b = oracle.attn_fwd_general(x["q"], kv["k"], kv["v"], 0.25, False)
     np.testing.assert_allclose(a[0], b[0], atol=1e-14)
     np.testing.assert_allclose(a[1], b[1], atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Variable-length batches (packed [total, H, d], cu_seqlens offsets).
+# ---------------------------------------------------------------------------
+
+# (lens_q, lens_k) mixes: ragged, equal, Lq < Lk (cache alignment), Lq > Lk
+# (leading queries see nothing under causal masking) and empty sequences.
+VARLEN_CASES = {
+    "mixed": ([5, 1, 9, 3], [5, 7, 9, 2]),
+    "with_empty": ([0, 4, 3], [3, 0, 6]),
+}
+
+
+def _varlen_inputs(case, H, Hkv, d, seed):
+    lq, lk = VARLEN_CASES[case]
+    return workloads.make_varlen_inputs(lq, lk, H, Hkv, d, seed)
+
+
+def pin_varlen_brute_force(fn):
+    # Each sequence and head against the pure-Python scalar loop, with K/V
+    # head h // G and K/V gradients summed over the group by hand.
+    for case in VARLEN_CASES:
+        for causal in (True, False):
+            x = _varlen_inputs(case, 4, 2, 3, 611)
+            q, k, v, dO = (oa.as_f64(x[n]) for n in ("q", "k", "v", "dO"))
+            cq, ck = x["cu_q"].tolist(), x["cu_k"].tolist()
+            got = fn(x["q"], x["k"], x["v"], x["dO"], cq, ck, 0.625, causal)
+            dK = np.zeros_like(k)
+            dV = np.zeros_like(v)
+            for b in range(len(cq) - 1):
+                for h in range(4):
+                    hk = h // 2
+                    sq, sk = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+                    if cq[b + 1] == cq[b]:
+                        continue
+                    if ck[b + 1] == ck[b]:
+                        np.testing.assert_allclose(got["O"][sq, h], 0, atol=0)
+                        assert np.all(got["LSE"][h, sq] == -np.inf)
+                        continue
+                    w = _brute_force(q[sq, h].tolist(), k[sk, hk].tolist(), v[sk, hk].tolist(),
+                                     dO[sq, h].tolist(), 0.625, causal)
+                    np.testing.assert_allclose(got["O"][sq, h], w["O"], atol=1e-12)
+                    np.testing.assert_allclose(got["LSE"][h, sq], w["LSE"], atol=1e-12)
+                    np.testing.assert_allclose(got["dQ"][sq, h], w["dQ"], atol=1e-12)
+                    dK[sk, hk] += w["dK"]
+                    dV[sk, hk] += w["dV"]
+            np.testing.assert_allclose(got["dK"], dK, atol=1e-12)
+            np.testing.assert_allclose(got["dV"], dV, atol=1e-12)
+
+
+def pin_varlen_torch_autograd(fn):
+    # Library special case: per sequence, torch fp64 attention with an explicit
+    # bottom-right causal mask on the repeated K/V heads, plus autograd.
+    lq, lk = [6, 2, 7], [9, 2, 7]  # every query sees at least one key
+    x = workloads.make_varlen_inputs(lq, lk, 6, 3, 5, seed=612)
+    cq, ck = x["cu_q"].tolist(), x["cu_k"].tolist()
+    for causal in (True, False):
+        got = fn(x["q"], x["k"], x["v"], x["dO"], cq, ck, 0.375, causal)
+        for b in range(3):
+            tq = x["q"][cq[b]:cq[b + 1]].double().permute(1, 0, 2).clone().requires_grad_(True)
+            tk = x["k"][ck[b]:ck[b + 1]].double().permute(1, 0, 2).clone().requires_grad_(True)
+            tv = x["v"][ck[b]:ck[b + 1]].double().permute(1, 0, 2).clone().requires_grad_(True)
+            g = x["dO"][cq[b]:cq[b + 1]].double().permute(1, 0, 2)
+            Lq, Lk = lq[b], lk[b]
+            mask = None
+            if causal:
+                mask = torch.tensor(np.arange(Lk)[None, :] <= np.arange(Lq)[:, None] + (Lk - Lq))
+            o = torch.nn.functional.scaled_dot_product_attention(
+                tq, tk.repeat_interleave(2, dim=0), tv.repeat_interleave(2, dim=0), attn_mask=mask, scale=0.375)
+            (o * g).sum().backward()
+            sl, kl = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+            np.testing.assert_allclose(got["O"][sl], o.detach().permute(1, 0, 2).numpy(), atol=1e-12)
+            np.testing.assert_allclose(got["dQ"][sl], tq.grad.permute(1, 0, 2).numpy(), atol=1e-12)
+            np.testing.assert_allclose(got["dK"][kl], tk.grad.permute(1, 0, 2).numpy(), atol=1e-12)
+            np.testing.assert_allclose(got["dV"][kl], tv.grad.permute(1, 0, 2).numpy(), atol=1e-12)
+
+
+def pin_varlen_rows_without_keys(fn):
+    # Lq = 5 queries, Lk = 2 keys, causal: queries 0..2 see nothing (O = 0,
+    # LSE = -inf, dQ = 0); query 3 sees key 0 only (O = V_0, LSE = s q.k_0).
+    x = workloads.make_varlen_inputs([5], [2], 1, 1, 4, seed=613)
+    got = fn(x["q"], x["k"], x["v"], x["dO"], [0, 5], [0, 2], 0.5, True)
+    q, k, v = (oa.as_f64(x[n]) for n in ("q", "k", "v"))
+    np.testing.assert_allclose(got["O"][:3], 0, atol=0)
+    assert np.all(got["LSE"][0, :3] == -np.inf)
+    np.testing.assert_allclose(got["dQ"][:3], 0, atol=0)
+    np.testing.assert_allclose(got["O"][3, 0], v[0, 0], atol=1e-14)
+    np.testing.assert_allclose(got["LSE"][0, 3], 0.5 * float(q[3, 0] @ k[0, 0]), atol=1e-14)
+
+
+def pin_varlen_sequences_are_independent(fn):
+    # Changing one sequence's inputs leaves every other sequence's outputs
+    # and gradients bit-identical.
+    x = _varlen_inputs("mixed", 2, 1, 4, 614)
+    cq, ck = x["cu_q"].tolist(), x["cu_k"].tolist()
+    a = fn(x["q"], x["k"], x["v"], x["dO"], cq, ck, 0.5, True)
+    y = {n: x[n].clone() for n in ("q", "k", "v", "dO")}
+    y["q"][cq[1]:cq[2]] *= -2
+    y["k"][ck[1]:ck[2]] += 1
+    y["v"][ck[1]:ck[2]] *= 3
+    b = fn(y["q"], y["k"], y["v"], y["dO"], cq, ck, 0.5, True)
+    for key, rows in (("O", cq), ("dQ", cq), ("dK", ck), ("dV", ck)):
+        for s0 in (0, 2, 3):
+            np.testing.assert_array_equal(a[key][rows[s0]:rows[s0 + 1]], b[key][rows[s0]:rows[s0 + 1]])
+    assert not np.array_equal(a["O"][cq[1]:cq[2]], b["O"][cq[1]:cq[2]])
+
+
+def pin_varlen_finite_differences(fn):
+    # Central differences of L = sum(O * dO) with respect to every entry of
+    # Q, K, V of a tiny packed batch (GQA, Lq != Lk, causal).
+    lq, lk = [3, 2], [4, 2]
+    r = np.random.Generator(np.random.PCG64(615))
+    q = r.standard_normal((5, 2, 2))
+    k = r.standard_normal((6, 1, 2))
+    v = r.standard_normal((6, 1, 2))
+    dO = r.standard_normal((5, 2, 2))
+    cq, ck, s, h = [0, 3, 5], [0, 4, 6], 0.8, 1e-6
+    g = fn(q, k, v, dO, cq, ck, s, True)
+
+    def loss(qq, kk, vv):
+        return float((fn(qq, kk, vv, None, cq, ck, s, True)["O"] * dO).sum())
+
+    for name, grad in (("q", g["dQ"]), ("k", g["dK"]), ("v", g["dV"])):
+        fd = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            args = {"q": q.copy(), "k": k.copy(), "v": v.copy()}
+            args[name][idx] += h
+            lp = loss(args["q"], args["k"], args["v"])
+            args[name][idx] -= 2 * h
+            lm = loss(args["q"], args["k"], args["v"])
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.abs(fd - grad).max() < 1e-7 * max(1.0, np.abs(grad).max()), name
+
+
+VARLEN_PINS = [pin_varlen_brute_force, pin_varlen_torch_autograd, pin_varlen_rows_without_keys,
+               pin_varlen_sequences_are_independent, pin_varlen_finite_differences]
+
+
+@pytest.mark.parametrize("pin", VARLEN_PINS, ids=lambda p: p.__name__)
+def test_varlen_oracle_pins(pin):
+    pin(oracle.attn_varlen)
+
+
+def test_varlen_equal_lengths_is_batched_attention():
+    # All sequences of one length N: the packed batch is the [B, H, N, d]
+    # problem with the sequence and head axes swapped.
+    x = workloads.make_varlen_inputs([24, 24], [24, 24], 4, 2, 8, seed=616)
+    q, k, v, dO = (x[n].reshape(2, 24, -1, 8).permute(0, 2, 1, 3) for n in ("q", "k", "v", "dO"))
+    for causal in (True, False):
+        got = oracle.attn_varlen(x["q"], x["k"], x["v"], x["dO"], x["cu_q"], x["cu_k"], 0.3, causal)
+        want = oracle.attn_bwd_gqa(q, k, v, dO, 0.3, causal)
+        np.testing.assert_allclose(got["O"], want["O"].transpose(0, 2, 1, 3).reshape(48, 4, 8), atol=1e-13)
+        np.testing.assert_allclose(got["LSE"], want["LSE"].transpose(1, 0, 2).reshape(4, 48), atol=1e-13)
+        np.testing.assert_allclose(got["dK"], want["dK"].transpose(0, 2, 1, 3).reshape(48, 2, 8), atol=1e-13)
+
+
+VARLEN_MUTANTS = {
+    "top_left_alignment": ("S = np.where(j > i + (Lk - Lq), -np.inf, S)\n            lse = row_logsumexp(S)\n            P",
+                           "S = np.where(j > i, -np.inf, S)\n            lse = row_logsumexp(S)\n            P"),
+    "offset_sign": ("S = np.where(j > i + (Lk - Lq), -np.inf, S)\n            lse = row_logsumexp(S)\n            P",
+                    "S = np.where(j > i - (Lk - Lq), -np.inf, S)\n            lse = row_logsumexp(S)\n            P"),
+    "head_group_modulo": ("            hk = h // G\n            S = scores(q[q0:q1, h]",
+                          "            hk = h % Hkv\n            S = scores(q[q0:q1, h]"),
+    "dK_overwritten": ('out["dK"][k0:k1, hk] += s', 'out["dK"][k0:k1, hk] = s'),
+    "dQ_wrong_keys": ('out["dQ"][q0:q1, h] = s * (dS @ k[k0:k1, hk])', 'out["dQ"][q0:q1, h] = s * (dS @ k[q0:q0 + Lk, hk])'),
+}
+
+
+@pytest.mark.parametrize("name", sorted(VARLEN_MUTANTS))
+def test_varlen_planted_mistakes_are_caught(name):
+    old, new = VARLEN_MUTANTS[name]
+    mod = _mutant_module(None, old, new)
+    failed = []
+    for pin in VARLEN_PINS:
+        try:
+            pin(mod.attn_varlen)
+        except (AssertionError, ValueError, FloatingPointError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught planted mistake {name}"

@@ -90,3 +90,40 @@ def sample_rows(N: int, count: int, seed: int) -> np.ndarray:
     while len(rows) < count:
         rows.add(next(extra))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def make_varlen_inputs(lens_q, lens_k, H: int, H_kv: int, d: int, seed: int, qk_mult: float = 1.0,
+                       with_grad: bool = True):
+    """Packed variable-length batch: q, dO [total_q, H, d], k, v [total_k, H_kv, d].
+
+    Same recipe as make_inputs (i.i.d. N(0, 1) fp32 in the order Q, K, V, dO,
+    Q and K times qk_mult, bf16 once); sequence b owns query rows
+    cu_q[b] .. cu_q[b+1] - 1 and key rows cu_k[b] .. cu_k[b+1] - 1.  Returns
+    a dict with those tensors (CPU) and cu_q, cu_k as int32 tensors of B + 1
+    entries.
+    """
+    lens_q, lens_k = [int(x) for x in lens_q], [int(x) for x in lens_k]
+    if len(lens_q) != len(lens_k) or min(lens_q + lens_k) < 0:
+        raise ValueError("need one non-negative query and key length per sequence")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    tq, tk = sum(lens_q), sum(lens_k)
+    shapes = {"q": (tq, H, d), "k": (tk, H_kv, d), "v": (tk, H_kv, d), "dO": (tq, H, d)}
+    names = ("q", "k", "v", "dO") if with_grad else ("q", "k", "v")
+    out = {}
+    for name in names:
+        x = rng.standard_normal(size=shapes[name], dtype=np.float32)
+        if name in ("q", "k") and qk_mult != 1.0:
+            x *= np.float32(qk_mult)
+        out[name] = torch.from_numpy(x).to(torch.bfloat16).contiguous()
+    out["cu_q"] = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    out["cu_k"] = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32)
+    return out
+
+
+def varlen_lengths(B: int, max_len: int, seed: int) -> list:
+    """Seeded length mix for a variable-length batch: uniform in [1, max_len],
+    with the first sequence at max_len (so the longest is always present)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 104729))
+    lens = rng.integers(1, max_len + 1, size=B).tolist()
+    lens[0] = max_len
+    return [int(x) for x in lens]
