@@ -120,6 +120,42 @@ int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float*
                     int Nk, int d, float scale, int causal, int num_splits, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/*
+ * Variable-length batches (packed sequences).  The pages treat one sequence
+ * length per call; this is the usual packed form of the same attention, in
+ * the plainest reading: B sequences of different lengths are stored back to
+ * back without padding.  q, o, dO, dq: [total_q, H, d]; k, v, dk, dv:
+ * [total_k, H_kv, d] (bf16, row-major); lse: fp32 [H, total_q].
+ * cu_seqlens_q / cu_seqlens_k: DEVICE int32 arrays of B + 1 offsets, 0 first,
+ * non-decreasing, last = total_q / total_k: sequence b owns query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1] - 1 and key rows cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1] - 1 and never sees another sequence.  max_seqlen_q /
+ * max_seqlen_k bound every sequence's lengths (they size the grid).  Query
+ * head h reads key/value head h / (H / H_kv).  With causal != 0 a sequence's
+ * Lq queries are its last Lq positions (key-value-cache alignment): query i
+ * sees key j iff j <= i + Lk - Lq; a query that sees no key (Lk = 0, or
+ * Lk < Lq when causal) gets o = 0 and lse = -inf and contributes nothing to
+ * the gradients.  Rows outside every sequence are not written.
+ * The host cannot read the device offsets without a synchronisation, so the
+ * kernels check them: a sequence whose offsets are out of order, outside
+ * [0, total] or longer than the stated maximum is skipped and the device
+ * status word (fa2_device_status) is set to 3.
+ * Sizes: B >= 1, total_q, total_k >= 0 (<= 2^30), 0 <= max_seqlen <= total,
+ * max_seqlen >= 1 when its total is > 0.  Pointers of tensors with zero rows
+ * may be NULL.  fa2_fwd_varlen: one kernel launch.  fa2_bwd_varlen: the same
+ * three stages as fa2_bwd_ws with caller scratch of
+ * fa2_bwd_varlen_workspace_bytes(H, total_q, d) bytes (256-byte aligned; may
+ * be NULL when total_q or total_k is 0, which only zeroes dk, dv or dq).
+ */
+int fa2_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                   const int* cu_seqlens_k, int B, int H, int H_kv, int total_q, int total_k, int max_seqlen_q,
+                   int max_seqlen_k, int d, float scale, int causal, void* stream);
+size_t fa2_bwd_varlen_workspace_bytes(int H, int total_q, int d);
+int fa2_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                   int H_kv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, float scale,
+                   int causal, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device scratch fa2_bwd needs: D (fp32 [B,H,N]) and the fp32 dQ
  * accumulator [B,H,N,d], each 256-byte aligned.  0 on invalid sizes. */
 size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);
@@ -184,7 +220,8 @@ size_t fa2_noalloc_scratch_capacity(void);
 const char* fa2_status_string(int status);
 
 /* Read (and if `reset` != 0, clear) the kernels' device status word on the
- * current device: 0 = every wait completed, 1 = some wait timed out.
+ * current device: 0 = every wait completed, 1 = some wait timed out,
+ * 2 = shared memory base misaligned, 3 = invalid cu_seqlens (varlen calls).
  * Synchronous with respect to the device. Returns an fa2_status. */
 int fa2_device_status(int* value, int reset);
 

@@ -126,3 +126,55 @@ def test_python_binding_checks_metadata():
         fa2.fa2_fwd(q, q, q)  # CPU tensors are refused before any call
     with pytest.raises(ValueError):
         fa2.fa2_fwd(q.float(), q, q)
+
+
+def fwd_varlen(lib, q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, cuq=6 * A, cuk=7 * A, B=2, H=2, Hkv=1,
+               tq=300, tk=400, mq=200, mk=300, d=64, scale=0.125, causal=1):
+    return lib.fa2_fwd_varlen(q, k, v, o, lse, cuq, cuk, B, H, Hkv, tq, tk, mq, mk, d, scale, causal, None)
+
+
+def test_fwd_varlen_rejects_bad_arguments(lib):
+    assert fwd_varlen(lib, B=0) == 2
+    assert fwd_varlen(lib, Hkv=3) == 2           # H not a multiple of H_kv
+    assert fwd_varlen(lib, mq=301) == 2          # a sequence longer than the packed total
+    assert fwd_varlen(lib, mq=0) == 2            # queries exist but the maximum length is 0
+    assert fwd_varlen(lib, tq=-1) == 2
+    assert fwd_varlen(lib, tq=(1 << 30) + 1, mq=5) == 2
+    assert fwd_varlen(lib, d=48) == 3
+    assert fwd_varlen(lib, scale=0.0) == 5
+    assert fwd_varlen(lib, cuq=None) == 1
+    assert fwd_varlen(lib, k=None) == 1
+    assert fwd_varlen(lib, cuk=7 * A + 2) == 4   # offsets must be 4-byte aligned
+    assert fwd_varlen(lib, q=A + 8) == 4
+    assert fwd_varlen(lib, o=A) == 9             # o aliases q
+    assert fwd_varlen(lib, lse=6 * A) == 9       # lse over the query offsets
+    # no query rows: valid, nothing to do (returns before any CUDA call)
+    assert fwd_varlen(lib, q=None, o=None, lse=None, tq=0, mq=0) == 0
+
+
+def test_bwd_varlen_rejects_bad_arguments(lib):
+    p = [A * (i + 1) for i in range(9)]
+    cu = [10 * A, 11 * A]
+    need = lib.fa2_bwd_varlen_workspace_bytes(2, 300, 64)
+    assert need >= 300 * 2 * 4 + 300 * 2 * 64 * 4
+    ws = 64 * A
+
+    def call(ptrs=p, cus=cu, wsp=ws, wsb=need, **kw):
+        a = dict(B=2, H=2, Hkv=1, tq=300, tk=400, mq=200, mk=300, d=64)
+        a.update(kw)
+        return lib.fa2_bwd_varlen(*ptrs, *cus, a["B"], a["H"], a["Hkv"], a["tq"], a["tk"], a["mq"], a["mk"],
+                                  a["d"], 0.125, 1, wsp, wsb, None)
+
+    assert call(B=0) == 2
+    assert call(d=24) == 3
+    assert call(cus=[None, 11 * A]) == 1
+    for i in range(9):
+        q = list(p)
+        q[i] = None
+        assert call(q) == 1
+    q = list(p)
+    q[7] = q[6]  # dk == dq
+    assert call(q) == 9
+    assert call(wsp=None) == 8
+    assert call(wsb=need - 1) == 8
+    assert call(wsp=ws + 16) == 8

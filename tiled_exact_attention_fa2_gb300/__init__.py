@@ -23,7 +23,7 @@ __all__ = [
     "FA2Error", "load_library", "fa2_fwd", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
     "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
     "fa2_bwd_stages", "fa2_bwd_noalloc", "fa2_fwd_gqa", "fa2_bwd_gqa", "fa2_fwd_splitkv",
-    "FA2_OK",
+    "fa2_fwd_varlen", "fa2_bwd_varlen", "FA2_OK",
 ]
 
 FA2_OK = 0
@@ -55,6 +55,10 @@ _SIGNATURES = {
     "fa2_check_wait_timeout": (_i, [_i, ctypes.POINTER(_i)]),
     "fa2_fwd_splitkv_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "fa2_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
+    "fa2_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_bwd_varlen_workspace_bytes": (_sz, [_i, _i, _i]),
+    "fa2_bwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                            _f, _i, _vp, _sz, _vp]),
 }
 
 
@@ -263,6 +267,92 @@ def fa2_fwd_splitkv(q, k, v, num_splits: int, o=None, lse=None, workspace=None, 
     if rc != FA2_OK:
         raise FA2Error("fa2_fwd_splitkv", rc)
     return o, lse
+
+
+def _packed(t, name: str):
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be packed [total, heads, d], got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    return tuple(t.shape)
+
+
+def _cu(t, name: str):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.dim() != 1 or t.numel() < 2:
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor of B + 1 offsets")
+    return t.numel() - 1
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None and t.numel() > 0 else None
+
+
+def _varlen_shapes(q, k, v, cu_seqlens_q, cu_seqlens_k):
+    tq, H, d = _packed(q, "q")
+    tk, Hkv, dk_ = _packed(k, "k")
+    if dk_ != d or _packed(v, "v") != (tk, Hkv, d):
+        raise ValueError("k and v must be [total_k, H_kv, d] with q's d")
+    B = _cu(cu_seqlens_q, "cu_seqlens_q")
+    if _cu(cu_seqlens_k, "cu_seqlens_k") != B:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    return B, H, Hkv, tq, tk, d
+
+
+def _max_len(cu, given):
+    if given is not None:
+        return int(given)
+    return int((cu[1:] - cu[:-1]).max().item()) if cu.numel() > 1 else 0
+
+
+def fa2_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: Optional[int] = None,
+                   max_seqlen_k: Optional[int] = None, o=None, lse=None, scale: Optional[float] = None,
+                   causal: bool = True, stream=None):
+    """Variable-length forward on packed sequences: q [total_q,H,d], k/v [total_k,H_kv,d],
+    cu_seqlens_* CUDA int32 [B+1].  Returns (o [total_q,H,d] bf16, lse [H,total_q] fp32).
+    The maximum lengths are read from the offsets (a device sync) when not given."""
+    lib = load_library()
+    B, H, Hkv, tq, tk, d = _varlen_shapes(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    mq, mk = _max_len(cu_seqlens_q, max_seqlen_q), _max_len(cu_seqlens_k, max_seqlen_k)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((H, tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if _packed(o, "o") != (tq, H, d):
+        raise ValueError("o must have q's shape")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (H, tq):
+        raise ValueError("lse must be a contiguous fp32 [H, total_q] tensor")
+    rc = lib.fa2_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), cu_seqlens_q.data_ptr(),
+                            cu_seqlens_k.data_ptr(), B, H, Hkv, tq, tk, mq, mk, d, _scale(scale, d),
+                            1 if causal else 0, _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_fwd_varlen", rc)
+    return o, lse
+
+
+def fa2_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: Optional[int] = None,
+                   max_seqlen_k: Optional[int] = None, dq=None, dk=None, dv=None, workspace=None,
+                   scale: Optional[float] = None, causal: bool = True, stream=None):
+    """Variable-length backward: returns (dq [total_q,H,d], dk, dv [total_k,H_kv,d]); dk, dv
+    sum over each group of query heads.  ``workspace`` is allocated here when not given."""
+    lib = load_library()
+    B, H, Hkv, tq, tk, d = _varlen_shapes(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    mq, mk = _max_len(cu_seqlens_q, max_seqlen_q), _max_len(cu_seqlens_k, max_seqlen_k)
+    for name, t in (("o", o), ("dO", dO)):
+        if _packed(t, name) != (tq, H, d):
+            raise ValueError(f"{name} must have q's shape")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (H, tq):
+        raise ValueError("lse must be a contiguous fp32 [H, total_q] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = lib.fa2_bwd_varlen_workspace_bytes(H, tq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.fa2_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                            cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, H, Hkv, tq, tk, mq, mk, d,
+                            _scale(scale, d), 1 if causal else 0, workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_varlen", rc)
+    return dq, dk, dv
 
 
 def fa2_bwd_noalloc(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optional[float] = None,

@@ -38,23 +38,40 @@ EncodeTiledFn encode_tiled() {
 
 constexpr int kRowsPerTile = 128;
 
-// [B*H, N, d] bf16 view, box = [1, 128 rows, min(d, 64) columns], swizzle
-// width = box row width.  Rows past N in a head read as zero.
-bool make_tmap(CUtensorMap* out, const void* base, int BH, int N, int d) {
+// (heads, rows, d) view of a bf16 or fp32 tensor for TMA: coordinates are
+// (column, row, head); consecutive rows of a head are row_stride elements
+// apart, heads head_stride elements apart.  [B*H, N, d]: row_stride = d,
+// head_stride = N d.  Packed [total, H, d]: row_stride = H d, head_stride = d.
+// Box = [1, 128 rows, box_cols columns] with the swizzle as wide as the box
+// row; rows past `rows` read as zero and are dropped by reduce-adds.
+bool encode_rows(CUtensorMap* out, const void* base, bool f32, int heads, long long rows, int d,
+                 long long row_stride, long long head_stride) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
-  const int box_cols = d >= 64 ? 64 : d;
-  const CUtensorMapSwizzle swz = d >= 64   ? CU_TENSOR_MAP_SWIZZLE_128B
-                                 : d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                           : CU_TENSOR_MAP_SWIZZLE_32B;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const int esz = f32 ? 4 : 2;
+  const int box_cols = f32 ? (d >= 32 ? 32 : d) : (d >= 64 ? 64 : d);
+  const int row_bytes = box_cols * esz;
+  const CUtensorMapSwizzle swz = row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_32B;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride) * esz, static_cast<cuuint64_t>(head_stride) * esz};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), kRowsPerTile, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [B*H, N, d] bf16 view, box = [1, 128 rows, min(d, 64) columns].
+bool make_tmap(CUtensorMap* out, const void* base, int BH, int N, int d) {
+  return encode_rows(out, base, false, BH, N, d, d, static_cast<long long>(N) * d);
+}
+
+// Packed [total, heads, d] bf16 view (variable-length batches).
+bool make_tmap_packed(CUtensorMap* out, const void* base, int heads, int total, int d) {
+  return encode_rows(out, base, false, heads, total, d, static_cast<long long>(heads) * d, d);
 }
 
 // Text of the last CUDA failure seen by an entry point on this host thread.
@@ -70,18 +87,7 @@ int cuda_fail(int cuda_code, const char* where) {
 // [B*H, N, d] fp32 view of the dQ accumulator for TMA reduce-add, box =
 // [1, 128 rows, min(d, 32) columns], swizzle = box row width.
 bool make_tmap_f32(CUtensorMap* out, const void* base, int BH, int N, int d) {
-  EncodeTiledFn enc = encode_tiled();
-  if (!enc) return false;
-  const int box_cols = d >= 32 ? 32 : d;
-  const CUtensorMapSwizzle swz = d >= 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), kRowsPerTile, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_rows(out, base, true, BH, N, d, d, static_cast<long long>(N) * d);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -161,8 +167,15 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
   TmapSet tm;
   if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, BH, B * Hkv, N, d)) return rc;
   if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, BH, N, d, st)) return cuda_fail(e, "bwd preprocess launch");
-  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, BH, N, d, H / Hkv, scale, causal != 0, st))
-    return cuda_fail(e, "bwd main launch");
+  BwdProblem p{};
+  p.lse = lse;
+  p.Dvec = Dvec;
+  p.dk = dk;
+  p.dv = dv;
+  p.BH = BH;
+  p.N = N;
+  p.group = H / Hkv;
+  if (int e = launch_bwd_main(tm, p, d, scale, causal != 0, st)) return cuda_fail(e, "bwd main launch");
   if (int e = launch_bwd_dq_convert(dq_acc, dq, BH, N, d, scale, st)) return cuda_fail(e, "dq convert launch");
   return FA2_OK;
 }
@@ -400,8 +413,15 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
   }
   TmapSet tm;
   if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, B * H, B * H, N, d)) return rc;
-  if (int e = launch_bwd_main(tm, lse, Dvec, dk, dv, B * H, N, d, 1, scale, causal != 0,
-                              static_cast<cudaStream_t>(stream)))
+  BwdProblem p{};
+  p.lse = lse;
+  p.Dvec = Dvec;
+  p.dk = dk;
+  p.dv = dv;
+  p.BH = B * H;
+  p.N = N;
+  p.group = 1;
+  if (int e = launch_bwd_main(tm, p, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
     return cuda_fail(e, "bwd main launch");
   return FA2_OK;
 }
@@ -415,6 +435,162 @@ int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d
   if (overlap(range_of(dq_acc, n * 4), range_of(dq, n * 2))) return FA2_ERR_ALIAS;
   if (int e = launch_bwd_dq_convert(dq_acc, dq, B * H, N, d, scale, static_cast<cudaStream_t>(stream)))
     return cuda_fail(e, "dq convert launch");
+  return FA2_OK;
+}
+
+}  // extern "C" (reopened below)
+
+namespace {
+
+// Sizes of a packed variable-length batch (see fa2_fwd_varlen).
+int check_varlen_sizes(int B, int H, int H_kv, int total_q, int total_k, int max_q, int max_k, int d) {
+  if (B < 1 || H < 1 || total_q < 0 || total_k < 0 || max_q < 0 || max_k < 0) return FA2_ERR_SHAPE;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  if (int rc = check_heads(H, H_kv)) return rc;
+  if (max_q > total_q || max_k > total_k || total_q > (1 << 30) || total_k > (1 << 30)) return FA2_ERR_SHAPE;
+  if ((total_q > 0 && max_q < 1) || (total_k > 0 && max_k < 1)) return FA2_ERR_SHAPE;
+  const long long pairs = (static_cast<long long>(max_q) + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile);
+  const long long kt = (static_cast<long long>(max_k) + kRowsPerTile - 1) / kRowsPerTile;
+  if (static_cast<long long>(B) * H * pairs > 0x7fffffffLL || static_cast<long long>(B) * H_kv * kt > 0x7fffffffLL)
+    return FA2_ERR_SHAPE;
+  return FA2_OK;
+}
+
+size_t varlen_bwd_workspace(int H, int total_q, int d) {
+  const size_t rows = static_cast<size_t>(total_q) * H;
+  return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa2_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                   const int* cu_seqlens_k, int B, int H, int H_kv, int total_q, int total_k, int max_seqlen_q,
+                   int max_seqlen_k, int d, float scale, int causal, void* stream) {
+  if (int rc = check_varlen_sizes(B, H, H_kv, total_q, total_k, max_seqlen_q, max_seqlen_k, d)) return rc;
+  if (int rc = check_scale(scale)) return rc;
+  if (total_q == 0) return FA2_OK;  // no query rows: nothing to write
+  if (!q || !o || !lse || !cu_seqlens_q || !cu_seqlens_k || (total_k > 0 && (!k || !v))) return FA2_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4) || (total_k > 0 && (!aligned(k, 16) || !aligned(v, 16))))
+    return FA2_ERR_ALIGN;
+  const size_t qb = static_cast<size_t>(total_q) * H * d * 2;
+  const size_t kb = static_cast<size_t>(total_k) * H_kv * d * 2;
+  const size_t lb = static_cast<size_t>(total_q) * H * 4;
+  const size_t cb = static_cast<size_t>(B + 1) * 4;
+  const Range ro = range_of(o, qb), rl = range_of(lse, lb);
+  const Range ins[] = {range_of(q, qb), range_of(k, kb), range_of(v, kb), range_of(cu_seqlens_q, cb),
+                       range_of(cu_seqlens_k, cb)};
+  for (const Range& r : ins)
+    if (overlap(ro, r) || overlap(rl, r)) return FA2_ERR_ALIAS;
+  if (overlap(ro, rl)) return FA2_ERR_ALIAS;
+
+  FwdProblem p{};
+  p.RH = H;
+  p.M = max_seqlen_q;
+  p.Nq = max_seqlen_q;
+  p.Nk = max_seqlen_k;
+  p.kvdiv = H / H_kv;
+  p.splits = 1;
+  p.tiles_per_split = (max_seqlen_k + kRowsPerTile - 1) / kRowsPerTile;
+  p.o = o;
+  p.lse = lse;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.batches = B;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  if (max_seqlen_q == 0) return FA2_OK;  // every sequence is empty
+  TmapSet tm;
+  // With no keys at all the K/V maps are never read; they describe q instead.
+  const void* kb_ptr = total_k > 0 ? k : q;
+  const void* vb_ptr = total_k > 0 ? v : q;
+  const int tk = total_k > 0 ? total_k : 1;
+  if (!make_tmap_packed(&tm.q, q, H, total_q, d) || !make_tmap_packed(&tm.k, kb_ptr, H_kv, tk, d) ||
+      !make_tmap_packed(&tm.v, vb_ptr, H_kv, tk, d))
+    return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
+  if (int e = launch_fwd(tm, p, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
+    return cuda_fail(e, "varlen fwd launch");
+  return FA2_OK;
+}
+
+size_t fa2_bwd_varlen_workspace_bytes(int H, int total_q, int d) {
+  if (H < 1 || total_q < 0 || total_q > (1 << 30)) return 0;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
+  return varlen_bwd_workspace(H, total_q, d);
+}
+
+int fa2_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                   int H_kv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, float scale,
+                   int causal, void* workspace, size_t workspace_bytes_given, void* stream) {
+  if (int rc = check_varlen_sizes(B, H, H_kv, total_q, total_k, max_seqlen_q, max_seqlen_k, d)) return rc;
+  if (int rc = check_scale(scale)) return rc;
+  const bool has_q = total_q > 0, has_k = total_k > 0;
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA2_ERR_NULL;
+  if (has_q && (!q || !o || !dO || !lse || !dq)) return FA2_ERR_NULL;
+  if (has_k && (!k || !v || !dk || !dv)) return FA2_ERR_NULL;
+  if ((has_q && (!aligned(q, 16) || !aligned(o, 16) || !aligned(dO, 16) || !aligned(dq, 16) || !aligned(lse, 4))) ||
+      (has_k && (!aligned(k, 16) || !aligned(v, 16) || !aligned(dk, 16) || !aligned(dv, 16))))
+    return FA2_ERR_ALIGN;
+  const size_t qb = static_cast<size_t>(total_q) * H * d * 2;
+  const size_t kb = static_cast<size_t>(total_k) * H_kv * d * 2;
+  const size_t lb = static_cast<size_t>(total_q) * H * 4;
+  const size_t cb = static_cast<size_t>(B + 1) * 4;
+  const Range outs[] = {range_of(dq, qb), range_of(dk, kb), range_of(dv, kb)};
+  const Range ins[] = {range_of(q, qb), range_of(k, kb), range_of(v, kb), range_of(o, qb), range_of(dO, qb),
+                       range_of(lse, lb), range_of(cu_seqlens_q, cb), range_of(cu_seqlens_k, cb)};
+  for (int a = 0; a < 3; ++a) {
+    for (const Range& r : ins)
+      if (overlap(outs[a], r)) return FA2_ERR_ALIAS;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlap(outs[a], outs[b])) return FA2_ERR_ALIAS;
+  }
+  const size_t need = varlen_bwd_workspace(H, total_q, d);
+  if (has_q && has_k && (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < need))
+    return FA2_ERR_WORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Degenerate batches: no queries means dK = dV = 0, no keys means dQ = 0.
+  if (!has_q || !has_k) {
+    if (has_k) {
+      if (cudaError_t e = cudaMemsetAsync(dk, 0, kb, st)) return cuda_fail(static_cast<int>(e), "memset dk");
+      if (cudaError_t e = cudaMemsetAsync(dv, 0, kb, st)) return cuda_fail(static_cast<int>(e), "memset dv");
+    }
+    if (has_q)
+      if (cudaError_t e = cudaMemsetAsync(dq, 0, qb, st)) return cuda_fail(static_cast<int>(e), "memset dq");
+    return FA2_OK;
+  }
+  float* Dvec = static_cast<float*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           round_up(static_cast<size_t>(total_q) * H * sizeof(float)));
+  TmapSet tm;
+  if (!make_tmap_packed(&tm.q, q, H, total_q, d) || !make_tmap_packed(&tm.k, k, H_kv, total_k, d) ||
+      !make_tmap_packed(&tm.v, v, H_kv, total_k, d) || !make_tmap_packed(&tm.dO, dO, H, total_q, d) ||
+      !encode_rows(&tm.dqacc, dq_acc, true, H, total_q, d, static_cast<long long>(H) * d, d))
+    return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
+  // D and the zeroed accumulator in the packed row order ([total_q, H]).
+  if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, H, total_q, d, st)) return cuda_fail(e, "bwd preprocess launch");
+  BwdProblem p{};
+  p.lse = lse;
+  p.Dvec = Dvec;
+  p.dk = dk;
+  p.dv = dv;
+  p.BH = H;
+  p.N = 0;
+  p.group = H / H_kv;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.batches = B;
+  p.H = H;
+  p.Hkv = H_kv;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.max_q = max_seqlen_q;
+  p.max_k = max_seqlen_k;
+  if (max_seqlen_k > 0)
+    if (int e = launch_bwd_main(tm, p, d, scale, causal != 0, st)) return cuda_fail(e, "varlen bwd main launch");
+  if (int e = launch_bwd_dq_convert(dq_acc, dq, H, total_q, d, scale, st)) return cuda_fail(e, "dq convert launch");
   return FA2_OK;
 }
 

@@ -165,15 +165,20 @@ __global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __rest
 }
 
 // ---------------------------------------------------------------- main
-template <int D, bool CAUSAL>
+// VARLEN = true: packed variable-length batch (per-sequence lengths from
+// p.cu_q / p.cu_k); otherwise the square [B * H, N, d] problem.
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(512, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const __grid_constant__ CUtensorMap tm_dqacc, const float* __restrict__ lse,
-                   const float* __restrict__ Dvec, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                   int BH, int N, int group, int heads_per_group, float scale, float scale_log2) {
+                   const __grid_constant__ CUtensorMap tm_dqacc, const BwdProblem p, float scale, float scale_log2) {
   using T = HeadDim<D>;
   using C = BwdCfg<D>;
+  const float* __restrict__ lse = p.lse;
+  const float* __restrict__ Dvec = p.Dvec;
+  __nv_bfloat16* __restrict__ dk = static_cast<__nv_bfloat16*>(p.dk);
+  __nv_bfloat16* __restrict__ dv = static_cast<__nv_bfloat16*>(p.dv);
+  const int group = p.group;
   constexpr int SQ = C::kQStages, SD = C::kDoStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -193,26 +198,58 @@ __global__ void __launch_bounds__(512, 1)
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int num_tiles = (N + kTileRows - 1) / kTileRows;
-  // One CTA per (key/value tile, K/V head); it visits the query tiles of all
-  // `group` query heads that share the K/V head, so dK and dV accumulate the
-  // group sum in TMEM.  Iteration it covers query head g = it / n_q, query
-  // tile i = i_begin + it % n_q.
+  // One CTA per (key/value tile, K/V head) (per sequence when VARLEN); it
+  // visits the query tiles of all `group` query heads that share the K/V
+  // head, so dK and dV accumulate the group sum in TMEM.  Iteration it covers
+  // query head g = it / n_q, query tile i = i_begin + it % n_q.
   // CTAs come in groups of `heads_per_group` K/V heads, so that the group's
   // Q, dO and fp32 dQ rows stay in L2 while its CTAs run; inside a group the
   // key/value tile index is the slow one (causal work shrinks with jt, so
   // heavy tiles go first).
-  const int BHkv = BH / group;
-  const int per_group = heads_per_group * num_tiles;
-  const int hg0 = static_cast<int>(blockIdx.x / per_group) * heads_per_group;
-  const int within = static_cast<int>(blockIdx.x % per_group);
-  const int hg = min(heads_per_group, BHkv - hg0);
+  const int kv_tiles_grid = ((VARLEN ? p.max_k : p.N) + kTileRows - 1) / kTileRows;
+  const int BHkv = VARLEN ? p.Hkv : p.BH / group;
+  const int per_batch = BHkv * kv_tiles_grid;
+  const int local = VARLEN ? static_cast<int>(blockIdx.x % per_batch) : static_cast<int>(blockIdx.x);
+  const int per_group = p.heads_per_group * kv_tiles_grid;
+  const int hg0 = local / per_group * p.heads_per_group;
+  const int within = local % per_group;
+  const int hg = min(p.heads_per_group, BHkv - hg0);
   const int jt = within / hg;  // key/value tile
   const int bh_kv = hg0 + within % hg;
   const int kv0 = jt * kTileRows;
-  const int i_begin = CAUSAL ? jt : 0;
-  const int n_q = num_tiles - i_begin;
+  // Query rows, key rows, causal offset (query i sees key j iff j <= i + off)
+  // and the first TMA row of the sequence's queries and keys.
+  int Nq = p.N, Nk = p.N, off = 0, q_base = 0, k_base = 0;
+  if constexpr (VARLEN) {
+    const int b = static_cast<int>(blockIdx.x / per_batch);
+    const int sq = p.cu_q[b], eq = p.cu_q[b + 1], sk = p.cu_k[b], ek = p.cu_k[b + 1];
+    if (!(0 <= sq && sq <= eq && eq <= p.total_q && eq - sq <= p.max_q && 0 <= sk && sk <= ek &&
+          ek <= p.total_k && ek - sk <= p.max_k)) {
+      if (threadIdx.x == 0) atomicCAS(status, kDevOk, kDevBadSeqlens);
+      return;
+    }
+    Nq = eq - sq;
+    Nk = ek - sk;
+    off = Nk - Nq;
+    q_base = sq;
+    k_base = sk;
+    if (kv0 >= Nk) return;  // the tile lies past this sequence's keys
+  }
+  const int num_q_tiles = (Nq + kTileRows - 1) / kTileRows;
+  // First query tile that can see a key of this tile (causal): i >= kv0 - off.
+  const int i_begin = !CAUSAL ? 0 : (VARLEN ? (kv0 - off > 0 ? (kv0 - off) / kTileRows : 0) : jt);
+  const int n_q = num_q_tiles - i_begin;
   const int n_iter = n_q * group;
+  if (VARLEN && n_q <= 0) {
+    // No query of the sequence sees these keys (Lq = 0): dK = dV = 0.
+    const int rows = min(kTileRows, Nk - kv0);
+    for (int e = threadIdx.x; e < rows * (D / 8); e += blockDim.x) {
+      const size_t at = (static_cast<size_t>(k_base + kv0 + e / (D / 8)) * BHkv + bh_kv) * D + (e % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(dk + at) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(dv + at) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
 
   if (threadIdx.x == kWarpProducer * 32) {
     mbar_init(&bars[kBarKV], 1);
@@ -259,8 +296,8 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars[kBarKV], 2 * T::kTileBytes);
       for (int b = 0; b < T::kNumBoxes; ++b) {
-        tma_load_3d(smem + C::kK + b * T::kBoxBytes, &tm_k, &bars[kBarKV], b * T::kBoxCols, kv0, bh_kv);
-        tma_load_3d(smem + C::kV + b * T::kBoxBytes, &tm_v, &bars[kBarKV], b * T::kBoxCols, kv0, bh_kv);
+        tma_load_3d(smem + C::kK + b * T::kBoxBytes, &tm_k, &bars[kBarKV], b * T::kBoxCols, k_base + kv0, bh_kv);
+        tma_load_3d(smem + C::kV + b * T::kBoxBytes, &tm_v, &bars[kBarKV], b * T::kBoxCols, k_base + kv0, bh_kv);
       }
     }
     int last_q0 = -1, last_q1 = -1, last_do0 = -1, last_do1 = -1;
@@ -276,16 +313,19 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int r = lane; r < 128; r += 32) {
           const int q = q0 + r;
-          const bool in = q < N;
-          stats[r] = in ? -__ldg(lse + static_cast<size_t>(bh) * N + q) * kLog2e : -INFINITY;
-          stats[128 + r] = in ? -__ldg(Dvec + static_cast<size_t>(bh) * N + q) : 0.f;
+          const bool in = q < Nq;
+          // lse [BH, N] and D [BH, N]; packed batches: lse [H, total_q], D [total_q, H]
+          const size_t li = VARLEN ? static_cast<size_t>(bh) * p.total_q + q_base + q : static_cast<size_t>(bh) * Nq + q;
+          const size_t di = VARLEN ? static_cast<size_t>(q_base + q) * p.H + bh : li;
+          stats[r] = in ? -__ldg(lse + li) * kLog2e : -INFINITY;
+          stats[128 + r] = in ? -__ldg(Dvec + di) : 0.f;
         }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars[kBarQFull + st], T::kTileBytes);
           for (int b = 0; b < T::kNumBoxes; ++b)
             tma_load_3d(smem + C::kQ + st * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQFull + st],
-                        b * T::kBoxCols, q0, bh);
+                        b * T::kBoxCols, q_base + q0, bh);
         }
         (st ? last_q1 : last_q0) = it;
       }
@@ -296,7 +336,7 @@ __global__ void __launch_bounds__(512, 1)
           mbar_arrive_expect_tx(&bars[kBarDoFull + st], T::kTileBytes);
           for (int b = 0; b < T::kNumBoxes; ++b)
             tma_load_3d(smem + C::kDo + st * T::kTileBytes + b * T::kBoxBytes, &tm_do, &bars[kBarDoFull + st],
-                        b * T::kBoxCols, q0, bh);
+                        b * T::kBoxCols, q_base + q0, bh);
         }
         (st ? last_do1 : last_do0) = it;
       }
@@ -411,8 +451,9 @@ __global__ void __launch_bounds__(512, 1)
       if (!(ok = mbar_wait(&bars[kBarSFull], it & 1, status))) break;
       tc_fence_after();
       uint32_t pk[32];  // this half's 64 weights as bf16 pairs
-      const bool row_dead = kv_row >= N;
-      const int first = (CAUSAL && i == jt) ? kv_row - q0 : 0;  // queries q0 + c with c < first cannot see this key
+      const bool row_dead = kv_row >= Nk;
+      // queries q0 + c with c < first cannot see this key
+      const int first = !CAUSAL ? 0 : (VARLEN ? kv_row - off - q0 : (i == jt ? kv_row - q0 : 0));
       // P^T goes back to TMEM as bf16 pairs inside this warpgroup's own S^T
       // columns (the other warpgroup may still be reading its half): the 64
       // weights of columns [64 hh, 64 hh + 64) land in TMEM columns
@@ -527,7 +568,7 @@ __global__ void __launch_bounds__(512, 1)
         if (lane == 0) mbar_arrive(&bars[kBarStageFull + bsel]);
         if (issuer) {
           if ((ok = mbar_wait(&bars[kBarStageFull + bsel], u & 1, status))) {
-            tma_reduce_add_3d(&tm_dqacc, sb, c * C::kChunk, q0, bh);
+            tma_reduce_add_3d(&tm_dqacc, sb, c * C::kChunk, q_base + q0, bh);
             bulk_commit_group();
             // The previous chunk's reduce (other buffer) has read its source
             // once at most this one is still pending: release that buffer.
@@ -547,8 +588,10 @@ __global__ void __launch_bounds__(512, 1)
     if (ok && mbar_wait_sleep(&bars[kBarAccFull], 0, status)) {
       tc_fence_after();
       const int kv_row = kv0 + t;
-      const bool valid = kv_row < N;
-      const size_t off = (static_cast<size_t>(bh_kv) * N + (valid ? kv_row : 0)) * D;
+      const bool valid = kv_row < Nk;
+      const int vrow = valid ? kv_row : 0;
+      const size_t off = VARLEN ? (static_cast<size_t>(k_base + vrow) * BHkv + bh_kv) * D
+                                : (static_cast<size_t>(bh_kv) * Nk + vrow) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
@@ -606,20 +649,21 @@ int launch_preprocess_t(const void* o, const void* dO, float* Dvec, float* dq_ac
 }
 
 template <int D, bool CAUSAL>
-int launch_bwd_main_t(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N,
-                      int group, float scale, cudaStream_t stream) {
+int launch_bwd_main_t(const TmapSet& tm, BwdProblem p, float scale, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  auto kern = fa2_bwd_kernel<D, CAUSAL>;
+  const bool varlen = p.cu_q != nullptr;
+  auto kern = varlen ? fa2_bwd_kernel<D, CAUSAL, true> : fa2_bwd_kernel<D, CAUSAL, false>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
-  const int num_tiles = (N + kTileRows - 1) / kTileRows;
-  const dim3 grid(static_cast<unsigned>(num_tiles) * static_cast<unsigned>(BH / group));
+  const int rows_q = varlen ? p.max_q : p.N;
+  const int num_kv_tiles = ((varlen ? p.max_k : p.N) + kTileRows - 1) / kTileRows;
+  const int kv_heads = varlen ? p.Hkv : p.BH / p.group;
+  const dim3 grid(static_cast<unsigned>(num_kv_tiles) * static_cast<unsigned>(kv_heads) *
+                  static_cast<unsigned>(varlen ? p.batches : 1));
   // Bytes one K/V head's CTAs keep re-reading: Q, dO (bf16), the fp32 dQ
   // accumulator and LSE, D of its `group` query heads.
-  const size_t per_head = static_cast<size_t>(group) * N * (static_cast<size_t>(D) * 8 + 8);
-  const int hpg = heads_per_l2_group(per_head, BH / group);
-  kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, tm.dqacc, lse, Dvec,
-                                                  static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-                                                  BH, N, group, hpg, scale, scale * kLog2e);
+  const size_t per_head = static_cast<size_t>(p.group) * rows_q * (static_cast<size_t>(D) * 8 + 8);
+  p.heads_per_group = heads_per_l2_group(per_head, kv_heads);
+  kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, tm.dqacc, p, scale, scale * kLog2e);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -647,17 +691,13 @@ int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_
   }
 }
 
-int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N, int d,
-                    int group, float scale, bool causal, cudaStream_t stream) {
+int launch_bwd_main(const TmapSet& tm, const BwdProblem& p, int d, float scale, bool causal, cudaStream_t stream) {
   switch (d) {
-    case 16: return causal ? launch_bwd_main_t<16, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
-                           : launch_bwd_main_t<16, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
-    case 32: return causal ? launch_bwd_main_t<32, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
-                           : launch_bwd_main_t<32, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
-    case 64: return causal ? launch_bwd_main_t<64, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
-                           : launch_bwd_main_t<64, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
-    case 128: return causal ? launch_bwd_main_t<128, true>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream)
-                            : launch_bwd_main_t<128, false>(tm, lse, Dvec, dk, dv, BH, N, group, scale, stream);
+    case 16: return causal ? launch_bwd_main_t<16, true>(tm, p, scale, stream) : launch_bwd_main_t<16, false>(tm, p, scale, stream);
+    case 32: return causal ? launch_bwd_main_t<32, true>(tm, p, scale, stream) : launch_bwd_main_t<32, false>(tm, p, scale, stream);
+    case 64: return causal ? launch_bwd_main_t<64, true>(tm, p, scale, stream) : launch_bwd_main_t<64, false>(tm, p, scale, stream);
+    case 128:
+      return causal ? launch_bwd_main_t<128, true>(tm, p, scale, stream) : launch_bwd_main_t<128, false>(tm, p, scale, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

@@ -76,9 +76,13 @@ struct FwdCfg {
   static constexpr int kBytes = (kUsed + 1024) > 116 * 1024 ? (kUsed + 1024) : 116 * 1024;
 };
 
-// GENERAL = false compiles the plain prefill case (M = Nq = Nk, one split),
-// where a row's query index is the row itself and the causal offset is 0.
-template <int D, bool CAUSAL, bool GENERAL>
+// kSquare: the plain prefill case (M = Nq = Nk, one split), where a row's
+// query index is the row itself and the causal offset is 0.  kGeneral:
+// row-head form with Nq != Nk and key splits.  kVarlen: packed
+// variable-length batch (per-sequence lengths from cu_q / cu_k).
+enum FwdMode : int { kSquare = 0, kGeneral = 1, kVarlen = 2 };
+
+template <int D, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdProblem p, float scale_log2) {
@@ -93,16 +97,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // CTA = (key split, group of heads_per_group row-heads, pair of 128-row
-  // tiles, row-head), slowest first: a group's K/V rows stay in L2 while its
-  // CTAs run, and inside a group the heaviest pairs go first (causal work
-  // grows with the pair index).  Row r of row-head rh is query r % Nq; the
-  // row-head reads K/V head rh / kvdiv.
+  // CTA = (key split or sequence, group of heads_per_group row-heads, pair
+  // of 128-row tiles, row-head), slowest first: a group's K/V rows stay in L2
+  // while its CTAs run, and inside a group the heaviest pairs go first
+  // (causal work grows with the pair index).  Row r of row-head rh is query
+  // r % Nq; the row-head reads K/V head rh / kvdiv.
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
-  const int num_kv_tiles = (p.Nk + kTileRows - 1) / kTileRows;
   const int per_split = num_pairs * p.RH;
-  const int split = static_cast<int>(blockIdx.x / per_split);
+  const int split = MODE == kVarlen ? 0 : static_cast<int>(blockIdx.x / per_split);
   const int local = static_cast<int>(blockIdx.x % per_split);
   const int per_group = p.heads_per_group * num_pairs;
   const int hg0 = local / per_group * p.heads_per_group;
@@ -111,13 +114,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int rh = hg0 + (local % per_group) % hg;
   const int rh_kv = rh / p.kvdiv;
   const int q0 = pair * 2 * kTileRows;
-  const int off = GENERAL ? p.Nk - p.Nq : 0;  // causal: query i sees key j iff j <= i + off
+  // Rows and keys of this CTA's problem, the causal offset (query i sees key
+  // j iff j <= i + off) and the first TMA row of its queries and keys.
+  int M = p.M, Nk = p.Nk, off = MODE == kGeneral ? p.Nk - p.Nq : 0, q_base = 0, k_base = 0;
+  if constexpr (MODE == kVarlen) {
+    const int b = static_cast<int>(blockIdx.x / per_split);
+    const int sq = p.cu_q[b], eq = p.cu_q[b + 1], sk = p.cu_k[b], ek = p.cu_k[b + 1];
+    if (!(0 <= sq && sq <= eq && eq <= p.total_q && eq - sq <= p.M && 0 <= sk && sk <= ek && ek <= p.total_k &&
+          ek - sk <= p.Nk)) {
+      if (threadIdx.x == 0) atomicCAS(status, kDevOk, kDevBadSeqlens);
+      return;
+    }
+    M = eq - sq;
+    Nk = ek - sk;
+    off = Nk - M;
+    q_base = sq;
+    k_base = sk;
+    if (q0 >= M) return;  // the whole CTA lies past this sequence's queries
+  }
+  const int num_kv_tiles = (Nk + kTileRows - 1) / kTileRows;
   const int jb = split * p.tiles_per_split;
   const int je = min(num_kv_tiles, jb + p.tiles_per_split);
   // Local K/V tiles (from jb) each row tile visits, and the smallest query
   // index among its rows (for the causal-mask test).
   int cnt[2], imin[2];
-  if constexpr (!GENERAL) {
+  if constexpr (MODE == kSquare) {
     // Square problem: tile A sees tiles 0..2*pair (causal), tile B one more.
     cnt[0] = CAUSAL ? 2 * pair + 1 : num_kv_tiles;
     cnt[1] = 2 * pair + 1 >= num_row_tiles ? 0 : (CAUSAL ? 2 * pair + 2 : num_kv_tiles);
@@ -129,12 +150,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int rx0 = q0 + x * kTileRows;
       cnt[x] = 0;
       imin[x] = 0;
-      if (rx0 < p.M) {
-        const int rlast = min(rx0 + kTileRows - 1, p.M - 1);
-        const bool one_head = rx0 / p.Nq == rlast / p.Nq;
-        const int i_max = one_head ? rlast % p.Nq : p.Nq - 1;
-        imin[x] = one_head ? rx0 % p.Nq : 0;
-        const int kv_end = CAUSAL ? min(num_kv_tiles, (i_max + off) / kTileRows + 1) : num_kv_tiles;
+      if (rx0 < M) {
+        const int rlast = min(rx0 + kTileRows - 1, M - 1);
+        const bool one_head = MODE == kVarlen || rx0 / p.Nq == rlast / p.Nq;
+        const int i_max = MODE == kVarlen ? rlast : (one_head ? rlast % p.Nq : p.Nq - 1);
+        imin[x] = MODE == kVarlen ? rx0 : (one_head ? rx0 % p.Nq : 0);
+        // causal: the last key any row of the tile sees is i_max + off (< 0: none)
+        const int kv_end = !CAUSAL ? num_kv_tiles
+                                   : (i_max + off < 0 ? 0 : min(num_kv_tiles, (i_max + off) / kTileRows + 1));
         cnt[x] = max(0, min(je, kv_end) - jb);
       }
     }
@@ -177,7 +200,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (cnt[x] > 0)
           for (int b = 0; b < T::kNumBoxes; ++b)
             tma_load_3d(smem + C::kQ + x * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQ],
-                        b * T::kBoxCols, q0 + x * kTileRows, rh);
+                        b * T::kBoxCols, q_base + q0 + x * kTileRows, rh);
       int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;
 #pragma unroll 1
       for (int j = 0; j < n_kv; ++j) {
@@ -186,13 +209,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
-                      b * T::kBoxCols, (jb + j) * kTileRows, rh_kv);
+                      b * T::kBoxCols, k_base + (jb + j) * kTileRows, rh_kv);
         (st ? last_k1 : last_k0) = j;
         if (j >= 2 && !mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
         mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
         for (int b = 0; b < T::kNumBoxes; ++b)
           tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
-                      b * T::kBoxCols, (jb + j) * kTileRows, rh_kv);
+                      b * T::kBoxCols, k_base + (jb + j) * kTileRows, rh_kv);
         (st ? last_v1 : last_v0) = j;
       }
       // Never leave the CTA with a TMA write still landing in shared memory.
@@ -276,7 +299,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int x = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
     const int q_row = q0 + x * kTileRows + r;  // row in the row-head
-    const int qi = GENERAL ? q_row % p.Nq : q_row;  // its query index
+    const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
     const int imin_x = x ? imin[1] : imin[0];
     const int nx = x == 0 ? nA : nB;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -298,8 +321,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_wait_ld();
 
       const int kv0 = (jb + j) * kTileRows;
-      if ((CAUSAL && (GENERAL ? kv0 + kTileRows - 1 > imin_x + off : j == nx - 1)) || kv0 + kTileRows > p.Nk) {
-        int lim = p.Nk - kv0;                                // keys >= Nk do not exist
+      if ((CAUSAL && (MODE != kSquare ? kv0 + kTileRows - 1 > imin_x + off : j == nx - 1)) || kv0 + kTileRows > Nk) {
+        int lim = Nk - kv0;                                  // keys >= Nk do not exist
         if (CAUSAL) lim = min(lim, qi + off - kv0 + 1);      // key j visible iff j <= query + off
 #pragma unroll
         for (int e = 0; e < 128; ++e)
@@ -376,18 +399,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     // ------------------------------------------------------------ epilogue
     // One split: O / l in bf16 and LSE.  Several splits: this split's O / l
-    // and LSE in fp32 for the combine kernel (a split that sees no key of a
-    // row leaves O = 0, LSE = -inf there).
-    const bool valid = q_row < p.M;
-    const bool partial = GENERAL && p.splits > 1;
-    const size_t row_idx = (partial ? static_cast<size_t>(split) * p.RH + rh : static_cast<size_t>(rh)) * p.M +
-                           (valid ? q_row : 0);
-    if (GENERAL && nx == 0) {
-      if (partial && valid && ok) {
-        float4* dst = reinterpret_cast<float4*>(p.o_part + row_idx * D);
+    // and LSE in fp32 for the combine kernel.  A row that sees no key gets
+    // O = 0, LSE = -inf.
+    const bool valid = q_row < M;
+    const bool partial = MODE == kGeneral && p.splits > 1;
+    const int vrow = valid ? q_row : 0;
+    // o_row: row of o (or o_part) in units of D elements; lse_idx: index into lse.
+    size_t o_row, lse_idx;
+    if constexpr (MODE == kVarlen) {
+      o_row = static_cast<size_t>(q_base + vrow) * p.RH + rh;
+      lse_idx = static_cast<size_t>(rh) * p.total_q + q_base + vrow;
+    } else {
+      o_row = (partial ? static_cast<size_t>(split) * p.RH + rh : static_cast<size_t>(rh)) * p.M + vrow;
+      lse_idx = o_row;
+    }
+    if (MODE != kSquare && nx == 0) {
+      if (valid && ok) {
+        if (partial) {
+          float4* dst = reinterpret_cast<float4*>(p.o_part + o_row * D);
 #pragma unroll
-        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.lse_part[row_idx] = -INFINITY;
+          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.lse_part[o_row] = -INFINITY;
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_row * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[lse_idx] = -INFINITY;
+        }
       }
     } else if (ok && mbar_wait(&bars[kBarPVDone + x], (nx - 1) & 1, status)) {
       tc_fence_after();
@@ -402,13 +440,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_ld16(tO, o);
         tmem_wait_ld();
         if (valid) {
-          if (GENERAL && partial) {
-            float4* dst = reinterpret_cast<float4*>(p.o_part + row_idx * D + c * kC);
+          if (partial) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + o_row * D + c * kC);
 #pragma unroll
             for (int q = 0; q < kC / 4; ++q)
               dst[q] = make_float4(o[4 * q] * inv_l, o[4 * q + 1] * inv_l, o[4 * q + 2] * inv_l, o[4 * q + 3] * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + row_idx * D + c * kC);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_row * D + c * kC);
 #pragma unroll
             for (int q = 0; q < kC / 8; ++q)
               dst[q] = make_uint4(pack_bf16x2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l),
@@ -419,7 +457,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       // LSE in natural log of the scaled scores: ln 2 * (m + log2 l).
-      if (valid) (partial ? p.lse_part : p.lse)[row_idx] = (m + log2f(l)) * 0.69314718055994531f;
+      if (valid) {
+        const float lse_row = (m + log2f(l)) * 0.69314718055994531f;
+        if (partial)
+          p.lse_part[o_row] = lse_row;
+        else
+          p.lse[lse_idx] = lse_row;
+      }
     }
     tc_fence_before();
   }
@@ -434,15 +478,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int D, bool CAUSAL>
 int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stream) {
   using C = FwdCfg<D>;
+  const bool varlen = p.cu_q != nullptr;
   const bool general = p.splits > 1 || p.M != p.Nq || p.Nq != p.Nk;
   // Every row-head re-reads the K and V rows of its split.
   const int kv_rows = min(p.Nk, p.tiles_per_split * kTileRows);
   p.heads_per_group = heads_per_l2_group(static_cast<size_t>(kv_rows) * D * 4 / p.kvdiv, p.RH);
-  auto kern = general ? fa2_fwd_kernel<D, CAUSAL, true> : fa2_fwd_kernel<D, CAUSAL, false>;
+  auto kern = varlen    ? fa2_fwd_kernel<D, CAUSAL, kVarlen>
+              : general ? fa2_fwd_kernel<D, CAUSAL, kGeneral>
+                        : fa2_fwd_kernel<D, CAUSAL, kSquare>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
-  const dim3 grid(static_cast<unsigned>(num_pairs) * static_cast<unsigned>(p.RH) * static_cast<unsigned>(p.splits));
+  const unsigned outer = static_cast<unsigned>(varlen ? p.batches : p.splits);  // sequences or key splits
+  const dim3 grid(static_cast<unsigned>(num_pairs) * static_cast<unsigned>(p.RH) * outer);
   const float scale_log2 = scale * 1.44269504088896341f;
   kern<<<grid, kFwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, p, scale_log2);
   return static_cast<int>(cudaGetLastError());

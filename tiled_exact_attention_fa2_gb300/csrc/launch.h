@@ -40,6 +40,13 @@ inline int heads_per_l2_group(size_t bytes_per_head, int heads) {
 // kernel writes bf16 o and lse, with more it writes per-split fp32 results
 // to o_part [splits, RH, M, d] / lse_part [splits, RH, M] for
 // launch_splitkv_combine.
+//
+// Variable-length batch (cu_q != nullptr): q, o are packed [total_q, RH, d]
+// (RH = H query heads), k, v [total_k, H_kv, d], lse [RH, total_q];
+// sequence b owns query rows cu_q[b] .. cu_q[b+1] - 1 and key rows
+// cu_k[b] .. cu_k[b+1] - 1 (device arrays of batches + 1 ints), M = max
+// query length, Nk = max key length, one split.  Query i of a sequence with
+// Lq queries and Lk keys sees key j iff j <= i + Lk - Lq when causal.
 struct FwdProblem {
   int RH, M, Nq, Nk, kvdiv, splits, tiles_per_split;
   int heads_per_group;  // row-heads per CTA group (set by launch_fwd)
@@ -47,17 +54,37 @@ struct FwdProblem {
   float* lse;
   float* o_part;
   float* lse_part;
+  const int* cu_q;
+  const int* cu_k;
+  int batches, total_q, total_k;
 };
 
 int launch_fwd(const TmapSet& tm, const FwdProblem& p, int d, float scale, bool causal, cudaStream_t stream);
 int launch_splitkv_combine(const FwdProblem& p, int d, cudaStream_t stream);
 int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int BH, int N, int d,
                           cudaStream_t stream);
-// BH counts query heads; one CTA per (key/value tile, K/V head) loops over the
-// `group` query heads that share it, so dk / dv ([B * H / group, N, d]) hold
-// the group sums.
-int launch_bwd_main(const TmapSet& tm, const float* lse, const float* Dvec, void* dk, void* dv, int BH, int N, int d,
-                    int group, float scale, bool causal, cudaStream_t stream);
+// Backward main-kernel problem.  Square form: BH query heads ([B * H, N, d]
+// views, lse and D [B * H, N]); one CTA per (key/value tile, K/V head) loops
+// over the `group` query heads that share it, so dk / dv ([B * H / group, N,
+// d]) hold the group sums.
+//
+// Variable-length batch (cu_q != nullptr): q, dO packed [total_q, H, d], k,
+// v, dk, dv [total_k, Hkv, d], lse [H, total_q], D [total_q, H] (the
+// preprocess kernel's row order); sequence b owns query rows cu_q[b] ..
+// cu_q[b+1] - 1 and key rows cu_k[b] .. cu_k[b+1] - 1, at most max_q / max_k
+// of each; causal: query i sees key j iff j <= i + Lk - Lq.
+struct BwdProblem {
+  const float* lse;
+  const float* Dvec;
+  void* dk;
+  void* dv;
+  int BH, N, group;
+  int heads_per_group;  // K/V heads per CTA group (set by launch_bwd_main)
+  const int* cu_q;
+  const int* cu_k;
+  int batches, H, Hkv, total_q, total_k, max_q, max_k;
+};
+int launch_bwd_main(const TmapSet& tm, const BwdProblem& p, int d, float scale, bool causal, cudaStream_t stream);
 int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, float scale, cudaStream_t stream);
 
 int read_fwd_status(int* value, bool reset);

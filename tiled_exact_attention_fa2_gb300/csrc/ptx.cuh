@@ -21,6 +21,7 @@ enum DeviceStatus : int {
   kDevOk = 0,
   kDevWaitTimeout = 1,
   kDevSmemMisaligned = 2,
+  kDevBadSeqlens = 3,  // cu_seqlens not non-decreasing within [0, total] or a length above the stated maximum
 };
 
 // ---------------------------------------------------------------- generic
