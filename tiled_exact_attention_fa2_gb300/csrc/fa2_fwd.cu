@@ -44,19 +44,25 @@ __device__ int g_fwd_status;
 namespace {
 
 constexpr int kFwdThreads = 352;
+// Readers of each scheduler response: the producer, the two MMA issuers and
+// the eight softmax warps.
+constexpr int kSchedReaders = 11;
 constexpr uint32_t kTmemCols = 512;
 
 enum FwdBar {
-  kBarQ = 0,
-  kBarKFull = 1,    // +stage (2)
-  kBarKEmpty = 3,   // +stage
-  kBarVFull = 5,    // +stage
-  kBarVEmpty = 7,   // +stage
-  kBarSFull = 9,    // +tile (A, B)
-  kBarPFull = 11,   // +tile, 4 warp arrivals
-  kBarPVDone = 13,  // +tile
-  kBarDrain = 15,   // +tile
-  kNumFwdBars = 17,
+  kBarQFull = 0,    // +tile (A, B)
+  kBarKFull = 2,    // +stage (2)
+  kBarKEmpty = 4,   // +stage
+  kBarVFull = 6,    // +stage
+  kBarVEmpty = 8,   // +stage
+  kBarSFull = 10,   // +tile
+  kBarPFull = 12,   // +tile, 4 warp arrivals
+  kBarPVDone = 14,  // +tile
+  kBarDrain = 16,   // +tile
+  kBarQEmpty = 18,      // +tile: the tile's issuer is done with its Q tile of a unit
+  kBarSchedFull = 20,   // +slot (2): scheduler response landed (16 transaction bytes)
+  kBarSchedEmpty = 22,  // +slot: every role has read the response (kSchedReaders arrivals)
+  kNumFwdBars = 24,
 };
 
 template <int D>
@@ -69,7 +75,8 @@ struct FwdCfg {
   static constexpr int kK = kQ + 2 * T::kTileBytes;
   static constexpr int kV = kK + 2 * T::kTileBytes;
   static constexpr int kBars = kV + 2 * T::kTileBytes;
-  static constexpr int kTmemSlot = kBars + kNumFwdBars * 8;
+  static constexpr int kSched = (kBars + kNumFwdBars * 8 + 15) / 16 * 16;  // 2 x 16-byte responses
+  static constexpr int kTmemSlot = kSched + 32;
   static constexpr int kUsed = kTmemSlot + 16;
   // +1024 so the base can be rounded up to a 1024-byte boundary; at least
   // 116 KB so that a single CTA (and its 512 TMEM columns) occupies an SM.
@@ -82,6 +89,111 @@ struct FwdCfg {
 // variable-length batch (per-sequence lengths from cu_q / cu_k).
 enum FwdMode : int { kSquare = 0, kGeneral = 1, kVarlen = 2 };
 
+// One work unit: a pair of 128-row query tiles of one row-head, for one key
+// split (or one sequence of a variable-length batch).
+struct FwdUnit {
+  bool valid;                // false: nothing to do (varlen: past the sequence, or bad offsets)
+  int rh, rh_kv, q0, split;  // row-head, its K/V head, first row of the pair, key split
+  int M, Nk, off;            // rows, keys, causal offset (query i sees key j iff j <= i + off)
+  int q_base, k_base;        // first TMA row of the unit's queries / keys (varlen offsets)
+  int jb;                    // first K/V tile of the split
+  int cnt[2], imin[2];       // K/V tiles each row tile visits; smallest query index of the tile
+};
+
+// Unit u, in the order CTAs take them: key split or sequence slowest, then
+// groups of heads_per_group row-heads (a group's K/V rows stay in L2 while it
+// runs), then pairs heaviest first (causal work grows with the pair index),
+// then row-heads.  Row r of row-head rh is query r % Nq; the row-head reads
+// K/V head rh / kvdiv.
+template <bool CAUSAL, int MODE>
+__device__ __forceinline__ FwdUnit fwd_unit(const FwdProblem& p, int u, int num_row_tiles, int num_pairs,
+                                            int* status) {
+  FwdUnit w;
+  const int per_split = num_pairs * p.RH;
+  const int outer = u / per_split;
+  const int local = u % per_split;
+  const int per_group = p.heads_per_group * num_pairs;
+  const int hg0 = local / per_group * p.heads_per_group;
+  const int hg = min(p.heads_per_group, p.RH - hg0);
+  const int pair = num_pairs - 1 - (local % per_group) / hg;
+  w.valid = true;
+  w.rh = hg0 + (local % per_group) % hg;
+  w.rh_kv = w.rh / p.kvdiv;
+  w.q0 = pair * 2 * kTileRows;
+  w.split = MODE == kVarlen ? 0 : outer;
+  w.M = p.M;
+  w.Nk = p.Nk;
+  w.off = MODE == kGeneral ? p.Nk - p.Nq : 0;
+  w.q_base = 0;
+  w.k_base = 0;
+  if constexpr (MODE == kVarlen) {
+    const int sq = p.cu_q[outer], eq = p.cu_q[outer + 1], sk = p.cu_k[outer], ek = p.cu_k[outer + 1];
+    if (!(0 <= sq && sq <= eq && eq <= p.total_q && eq - sq <= p.M && 0 <= sk && sk <= ek && ek <= p.total_k &&
+          ek - sk <= p.Nk)) {
+      if (threadIdx.x == 0) atomicCAS(status, kDevOk, kDevBadSeqlens);
+      w.valid = false;
+    }
+    w.M = eq - sq;
+    w.Nk = ek - sk;
+    w.off = w.Nk - w.M;
+    w.q_base = sq;
+    w.k_base = sk;
+    if (w.q0 >= w.M) w.valid = false;  // the pair lies past this sequence's queries
+  }
+  const int num_kv_tiles = (w.Nk + kTileRows - 1) / kTileRows;
+  w.jb = w.split * p.tiles_per_split;
+  const int je = min(num_kv_tiles, w.jb + p.tiles_per_split);
+  if constexpr (MODE == kSquare) {
+    // Square problem: tile A sees tiles 0..2*pair (causal), tile B one more.
+    w.cnt[0] = CAUSAL ? 2 * pair + 1 : num_kv_tiles;
+    w.cnt[1] = 2 * pair + 1 >= num_row_tiles ? 0 : (CAUSAL ? 2 * pair + 2 : num_kv_tiles);
+    w.imin[0] = w.q0;
+    w.imin[1] = w.q0 + kTileRows;
+  } else {
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int rx0 = w.q0 + x * kTileRows;
+      w.cnt[x] = 0;
+      w.imin[x] = 0;
+      if (w.valid && rx0 < w.M) {
+        const int rlast = min(rx0 + kTileRows - 1, w.M - 1);
+        const bool one_head = MODE == kVarlen || rx0 / p.Nq == rlast / p.Nq;
+        const int i_max = MODE == kVarlen ? rlast : (one_head ? rlast % p.Nq : p.Nq - 1);
+        w.imin[x] = MODE == kVarlen ? rx0 : (one_head ? rx0 % p.Nq : 0);
+        // causal: the last key any row of the tile sees is i_max + off (< 0: none)
+        const int kv_end = !CAUSAL ? num_kv_tiles
+                                   : (i_max + w.off < 0 ? 0 : min(num_kv_tiles, (i_max + w.off) / kTileRows + 1));
+        w.cnt[x] = max(0, min(je, kv_end) - w.jb);
+      }
+    }
+  }
+  return w;
+}
+
+// The unit after a CTA's n-th unit: wait for the n-th scheduler response
+// (slot n & 1), decode it (-1: no unit left) and, if `release`, mark the slot
+// read.  Every reader calls this once per unit, in unit order.
+__device__ __forceinline__ int next_unit(uint64_t* bars, const uint8_t* sched, int n, bool release, int* status,
+                                         bool& ok) {
+  const int slot = n & 1;
+  if (!(ok = mbar_wait(&bars[kBarSchedFull + slot], (n >> 1) & 1, status))) return -1;
+  int u = clc_cancelled_block_x(sched + 16 * slot);
+  if (u >= static_cast<int>(gridDim.x)) {  // never expected: refuse rather than index past the grid
+    atomicCAS(status, kDevOk, kDevBadSchedule);
+    u = -1;
+  }
+  if (release) mbar_arrive(&bars[kBarSchedEmpty + slot]);
+  return u;
+}
+
+// Persistent with the hardware's dynamic order: the grid has one CTA per
+// unit, but a running CTA takes over the next not-yet-started CTA's unit
+// (cluster launch control) instead of exiting, for as long as there is one.
+// Units still start in blockIdx order (heaviest first), and all barrier
+// phases run on across a CTA's units, so the producer loads the next unit's
+// Q / K / V and the issuers start its first S while the softmax warps are
+// still writing the previous unit's O.  The producer requests the next unit
+// once it has issued every load of the current one.
 template <int D, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -92,82 +204,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
+  uint8_t* sched = smem + C::kSched;
   int* status = &g_fwd_status;
 
   const int warp = warp_id();
   const int lane = lane_id();
-
-  // CTA = (key split or sequence, group of heads_per_group row-heads, pair
-  // of 128-row tiles, row-head), slowest first: a group's K/V rows stay in L2
-  // while its CTAs run, and inside a group the heaviest pairs go first
-  // (causal work grows with the pair index).  Row r of row-head rh is query
-  // r % Nq; the row-head reads K/V head rh / kvdiv.
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
-  const int per_split = num_pairs * p.RH;
-  const int split = MODE == kVarlen ? 0 : static_cast<int>(blockIdx.x / per_split);
-  const int local = static_cast<int>(blockIdx.x % per_split);
-  const int per_group = p.heads_per_group * num_pairs;
-  const int hg0 = local / per_group * p.heads_per_group;
-  const int hg = min(p.heads_per_group, p.RH - hg0);
-  const int pair = num_pairs - 1 - (local % per_group) / hg;
-  const int rh = hg0 + (local % per_group) % hg;
-  const int rh_kv = rh / p.kvdiv;
-  const int q0 = pair * 2 * kTileRows;
-  // Rows and keys of this CTA's problem, the causal offset (query i sees key
-  // j iff j <= i + off) and the first TMA row of its queries and keys.
-  int M = p.M, Nk = p.Nk, off = MODE == kGeneral ? p.Nk - p.Nq : 0, q_base = 0, k_base = 0;
-  if constexpr (MODE == kVarlen) {
-    const int b = static_cast<int>(blockIdx.x / per_split);
-    const int sq = p.cu_q[b], eq = p.cu_q[b + 1], sk = p.cu_k[b], ek = p.cu_k[b + 1];
-    if (!(0 <= sq && sq <= eq && eq <= p.total_q && eq - sq <= p.M && 0 <= sk && sk <= ek && ek <= p.total_k &&
-          ek - sk <= p.Nk)) {
-      if (threadIdx.x == 0) atomicCAS(status, kDevOk, kDevBadSeqlens);
-      return;
-    }
-    M = eq - sq;
-    Nk = ek - sk;
-    off = Nk - M;
-    q_base = sq;
-    k_base = sk;
-    if (q0 >= M) return;  // the whole CTA lies past this sequence's queries
-  }
-  const int num_kv_tiles = (Nk + kTileRows - 1) / kTileRows;
-  const int jb = split * p.tiles_per_split;
-  const int je = min(num_kv_tiles, jb + p.tiles_per_split);
-  // Local K/V tiles (from jb) each row tile visits, and the smallest query
-  // index among its rows (for the causal-mask test).
-  int cnt[2], imin[2];
-  if constexpr (MODE == kSquare) {
-    // Square problem: tile A sees tiles 0..2*pair (causal), tile B one more.
-    cnt[0] = CAUSAL ? 2 * pair + 1 : num_kv_tiles;
-    cnt[1] = 2 * pair + 1 >= num_row_tiles ? 0 : (CAUSAL ? 2 * pair + 2 : num_kv_tiles);
-    imin[0] = q0;
-    imin[1] = q0 + kTileRows;
-  } else {
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const int rx0 = q0 + x * kTileRows;
-      cnt[x] = 0;
-      imin[x] = 0;
-      if (rx0 < M) {
-        const int rlast = min(rx0 + kTileRows - 1, M - 1);
-        const bool one_head = MODE == kVarlen || rx0 / p.Nq == rlast / p.Nq;
-        const int i_max = MODE == kVarlen ? rlast : (one_head ? rlast % p.Nq : p.Nq - 1);
-        imin[x] = MODE == kVarlen ? rx0 : (one_head ? rx0 % p.Nq : 0);
-        // causal: the last key any row of the tile sees is i_max + off (< 0: none)
-        const int kv_end = !CAUSAL ? num_kv_tiles
-                                   : (i_max + off < 0 ? 0 : min(num_kv_tiles, (i_max + off) / kTileRows + 1));
-        cnt[x] = max(0, min(je, kv_end) - jb);
-      }
-    }
-  }
-  const int nA = cnt[0], nB = cnt[1];
-  const int n_kv = nA > nB ? nA : nB;
 
   if (threadIdx.x == 8 * 32) {
-    mbar_init(&bars[kBarQ], 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kBarQFull + s], 1);
+      mbar_init(&bars[kBarQEmpty + s], 1);
+      mbar_init(&bars[kBarSchedFull + s], 1);
+      mbar_init(&bars[kBarSchedEmpty + s], kSchedReaders);
       mbar_init(&bars[kBarKFull + s], 1);
       mbar_init(&bars[kBarKEmpty + s], 2);
       mbar_init(&bars[kBarVFull + s], 1);
@@ -194,32 +244,68 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int n_q_tiles = (nA > 0) + (nB > 0);
-      if (n_q_tiles > 0) mbar_arrive_expect_tx(&bars[kBarQ], n_q_tiles * T::kTileBytes);
-      for (int x = 0; x < 2; ++x)
-        if (cnt[x] > 0)
-          for (int b = 0; b < T::kNumBoxes; ++b)
-            tma_load_3d(smem + C::kQ + x * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQ],
-                        b * T::kBoxCols, q_base + q0 + x * kTileRows, rh);
-      int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;
+      int g = 0;   // K/V tiles loaded so far (stage g & 1, use g >> 1)
+      int qn0 = 0, qn1 = 0;  // Q_A / Q_B tiles loaded so far
+      int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;  // last tile armed per stage
+      bool ok = true;
+      int pending = -1;  // scheduler request issued but not yet read here
 #pragma unroll 1
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status)) break;
-        mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
-        for (int b = 0; b < T::kNumBoxes; ++b)
-          tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
-                      b * T::kBoxCols, k_base + (jb + j) * kTileRows, rh_kv);
-        (st ? last_k1 : last_k0) = j;
-        if (j >= 2 && !mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status)) break;
-        mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
-        for (int b = 0; b < T::kNumBoxes; ++b)
-          tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
-                      b * T::kBoxCols, k_base + (jb + j) * kTileRows, rh_kv);
-        (st ? last_v1 : last_v0) = j;
+      for (int n = 0, u = static_cast<int>(blockIdx.x); ok && u >= 0; ++n) {
+        do {
+        const FwdUnit w = fwd_unit<CAUSAL, MODE>(p, u, num_row_tiles, num_pairs, status);
+        const int n_kv = max(w.cnt[0], w.cnt[1]);
+        if (!w.valid || n_kv == 0) break;
+        // Q_x smem is free once issuer x's last S of its previous unit is
+        // done.  Order: Q_A, K/V tile 0, Q_B, then the other K/V tiles, so
+        // tile A can start the unit while tile B still finishes the last one.
+        auto load_q = [&](int x) -> bool {
+          int& qn = x ? qn1 : qn0;
+          if (qn >= 1 && !mbar_wait(&bars[kBarQEmpty + x], (qn - 1) & 1, status)) return false;
+          mbar_arrive_expect_tx(&bars[kBarQFull + x], T::kTileBytes);
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_load_3d(smem + C::kQ + x * T::kTileBytes + b * T::kBoxBytes, &tm_q, &bars[kBarQFull + x],
+                        b * T::kBoxCols, w.q_base + w.q0 + x * kTileRows, w.rh);
+          ++qn;
+          return true;
+        };
+        if (w.cnt[0] > 0 && !(ok = load_q(0))) break;
+#pragma unroll 1
+        for (int j = 0; j < n_kv; ++j, ++g) {
+          const int st = g & 1;
+          if (g >= 2 && !(ok = mbar_wait(&bars[kBarKEmpty + st], ((g >> 1) - 1) & 1, status))) break;
+          mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
+                        b * T::kBoxCols, w.k_base + (w.jb + j) * kTileRows, w.rh_kv);
+          (st ? last_k1 : last_k0) = g;
+          if (g >= 2 && !(ok = mbar_wait(&bars[kBarVEmpty + st], ((g >> 1) - 1) & 1, status))) break;
+          mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
+                        b * T::kBoxCols, w.k_base + (w.jb + j) * kTileRows, w.rh_kv);
+          (st ? last_v1 : last_v0) = g;
+          if (j == 0 && w.cnt[1] > 0 && !(ok = load_q(1))) break;
+        }
+        } while (false);
+        if (!ok) break;
+        // Every load of this unit is issued (about two K/V tiles ahead of the
+        // MMAs): ask for the next unit now, late enough that CTAs which
+        // finish first take the remaining units.  Slot n & 1 is free once
+        // every reader has taken request n - 2's answer.
+        if (n >= 2 && !(ok = mbar_wait(&bars[kBarSchedEmpty + (n & 1)], ((n >> 1) - 1) & 1, status))) break;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[kBarSchedFull + (n & 1)], 16);
+        clc_try_cancel(sched + 16 * (n & 1), &bars[kBarSchedFull + (n & 1)]);
+        pending = n;
+        u = next_unit(bars, sched, n, true, status, ok);
+        pending = -1;
       }
-      // Never leave the CTA with a TMA write still landing in shared memory.
-      if (n_q_tiles > 0) mbar_wait(&bars[kBarQ], 0, status);
+      // A scheduler response still on its way must land before the CTA exits.
+      if (pending >= 0) mbar_wait(&bars[kBarSchedFull + (pending & 1)], (pending >> 1) & 1, status);
+      // Never leave the CTA with a TMA write still landing in shared memory:
+      // wait for the last completion of every full barrier that was armed.
+      if (qn0 >= 1) mbar_wait(&bars[kBarQFull + 0], (qn0 - 1) & 1, status);
+      if (qn1 >= 1) mbar_wait(&bars[kBarQFull + 1], (qn1 - 1) & 1, status);
       if (last_k0 >= 0) mbar_wait(&bars[kBarKFull + 0], (last_k0 >> 1) & 1, status);
       if (last_k1 >= 0) mbar_wait(&bars[kBarKFull + 1], (last_k1 >> 1) & 1, status);
       if (last_v0 >= 0) mbar_wait(&bars[kBarVFull + 0], (last_v0 >> 1) & 1, status);
@@ -229,66 +315,78 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer of tile x
     if (lane == 0) {
       const int x = warp - 9;
-      const int nx = x == 0 ? nA : nB;
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q (K-major) x K (K-major)
       constexpr uint32_t kIdescO = make_idesc_bf16(128, D, false, true);     // P (TMEM) x V (MN-major)
       const uint32_t sQ0 = smem_u32(smem + C::kQ), sK0 = smem_u32(smem + C::kK), sV0 = smem_u32(smem + C::kV);
       const uint32_t tSx = tmem + (x ? C::kColS1 : C::kColS0), tOx = tmem + (x ? C::kColO1 : C::kColO0);
-      // S_x(j) = Q_x K_j^T into TMEM S_x.
-      auto issue_s = [&](int j) {
+      // S_x = Q_x K^T for the K/V tile in stage st, into TMEM S_x.
+      auto issue_s = [&](int st) {
         uint32_t sQ = sQ0, sK = sK0;
         opaque(sQ);
         opaque(sK);
-        const uint32_t qb = sQ + x * T::kTileBytes, kb = sK + (j & 1) * T::kTileBytes;
+        const uint32_t qb = sQ + x * T::kTileBytes, kb = sK + st * T::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ss(tSx, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kBarSFull + x]);
-        mma_commit(&bars[kBarKEmpty + (j & 1)]);
+        mma_commit(&bars[kBarKEmpty + st]);
       };
-      // O_x += P_x V_j with P_x read from the first 64 columns of S_x.
-      auto issue_pv = [&](int j) {
+      // O_x (+)= P_x V with P_x read from the first 64 columns of S_x.
+      auto issue_pv = [&](int st, bool first) {
         uint32_t sV = sV0;
         opaque(sV);
-        const uint32_t vb = sV + (j & 1) * T::kTileBytes;
+        const uint32_t vb = sV + st * T::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ts(tOx, tSx + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tOx, tSx + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarPVDone + x]);
-        mma_commit(&bars[kBarVEmpty + (j & 1)]);
+        mma_commit(&bars[kBarVEmpty + st]);
       };
+      int g = 0;   // K/V tiles of all units so far (same count as the producer's)
+      int k = 0;   // S_x / P_x / PV_x issued so far (phase k & 1)
+      int qn = 0;  // units whose Q_x tile was loaded so far
       bool ok = true;
-      if (nx > 0) {
-        ok = mbar_wait(&bars[kBarQ], 0, status) && mbar_wait(&bars[kBarKFull + 0], 0, status);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0);
-        }
-      }
 #pragma unroll 1
-      for (int j = 0; ok && j < nx; ++j) {
-        const int st = j & 1;
-        if (!(ok = mbar_wait(&bars[kBarVFull + st], (j >> 1) & 1, status))) break;
-        if (!(ok = mbar_wait(&bars[kBarPFull + x], j & 1, status))) break;
-        tc_fence_after();
-        issue_pv(j);
-        if (j + 1 < nx) {
-          // S_x(j+1) overwrites the P_x columns the MMA above reads.
-          if (!(ok = mbar_wait(&bars[kBarPVDone + x], j & 1, status))) break;
-          if (!(ok = mbar_wait(&bars[kBarKFull + (st ^ 1)], ((j + 1) >> 1) & 1, status))) break;
-          tc_fence_after();
-          issue_s(j + 1);
+      for (int n = 0, u = static_cast<int>(blockIdx.x); ok && u >= 0; ++n) {
+        do {
+        const FwdUnit w = fwd_unit<CAUSAL, MODE>(p, u, num_row_tiles, num_pairs, status);
+        const int n_kv = max(w.cnt[0], w.cnt[1]);
+        if (!w.valid || n_kv == 0) break;
+        const int nx = x ? w.cnt[1] : w.cnt[0];  // (selects keep the struct in registers)
+        if (nx > 0) {
+          if (!(ok = mbar_wait(&bars[kBarQFull + x], qn & 1, status))) break;
+          ++qn;
         }
-      }
-      // K/V tiles this query tile does not visit: release them once, in
-      // phase order (after the stage's previous use has been released).
 #pragma unroll 1
-      for (int j = nx; ok && j < n_kv; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !(ok = mbar_wait(&bars[kBarKEmpty + st], ((j >> 1) - 1) & 1, status))) break;
-        mbar_arrive(&bars[kBarKEmpty + st]);
-        if (j >= 2 && !(ok = mbar_wait(&bars[kBarVEmpty + st], ((j >> 1) - 1) & 1, status))) break;
-        mbar_arrive(&bars[kBarVEmpty + st]);
+        for (int j = 0; j < nx; ++j) {
+          const int gj = g + j, st = gj & 1;
+          // S_x overwrites the P_x columns the previous PV_x reads.
+          if (k >= 1 && !(ok = mbar_wait(&bars[kBarPVDone + x], (k - 1) & 1, status))) break;
+          if (!(ok = mbar_wait(&bars[kBarKFull + st], (gj >> 1) & 1, status))) break;
+          tc_fence_after();
+          issue_s(st);
+          if (j + 1 == nx) mma_commit(&bars[kBarQEmpty + x]);  // last use of Q_x in this unit
+          if (!(ok = mbar_wait(&bars[kBarVFull + st], (gj >> 1) & 1, status))) break;
+          if (!(ok = mbar_wait(&bars[kBarPFull + x], k & 1, status))) break;
+          tc_fence_after();
+          issue_pv(st, j == 0);
+          ++k;
+        }
+        if (!ok) break;
+        // K/V tiles this query tile does not visit: release them once, in
+        // phase order (after the stage's previous use has been released).
+#pragma unroll 1
+        for (int j = nx; j < n_kv; ++j) {
+          const int gj = g + j, st = gj & 1;
+          if (gj >= 2 && !(ok = mbar_wait(&bars[kBarKEmpty + st], ((gj >> 1) - 1) & 1, status))) break;
+          mbar_arrive(&bars[kBarKEmpty + st]);
+          if (gj >= 2 && !(ok = mbar_wait(&bars[kBarVEmpty + st], ((gj >> 1) - 1) & 1, status))) break;
+          mbar_arrive(&bars[kBarVEmpty + st]);
+        }
+        g += n_kv;
+        } while (false);
+        if (!ok) break;
+        u = next_unit(bars, sched, n, true, status, ok);
       }
       // Wait for every MMA this thread issued before TMEM can be released.
       mma_commit(&bars[kBarDrain + x]);
@@ -298,123 +396,131 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------ softmax (tile x)
     const int x = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
-    const int q_row = q0 + x * kTileRows + r;  // row in the row-head
-    const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
-    const int imin_x = x ? imin[1] : imin[0];
-    const int nx = x == 0 ? nA : nB;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_base + (x ? C::kColO1 : C::kColO0);
-    float m = -INFINITY;  // running row max, log2 units (scores * scale * log2 e)
-    float l = 0.f;        // running sum of 2^(x - m)
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+    int k = 0;  // S_x tiles consumed so far (phase k & 1)
     bool ok = true;
 #pragma unroll 1
-    for (int j = 0; j < nx; ++j) {
-      // S_x(j) was issued after O_x += P_x(j-1) V_{j-1} completed, so O_x is
-      // stable once S_x(j) has landed.
-      if (!(ok = mbar_wait(&bars[kBarSFull + x], j & 1, status))) break;
-      tc_fence_after();
-      float s[128];
+    for (int n = 0, u = static_cast<int>(blockIdx.x); ok && u >= 0; ++n) {
+      do {
+      const FwdUnit w = fwd_unit<CAUSAL, MODE>(p, u, num_row_tiles, num_pairs, status);
+      if (!w.valid) break;
+      const int nx = x ? w.cnt[1] : w.cnt[0];  // (selects keep the struct in registers)
+      const int q_row = w.q0 + x * kTileRows + r;              // row in the row-head
+      const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
+      const int imin_x = x ? w.imin[1] : w.imin[0];
+      const int off = w.off, Nk = w.Nk;
+      float m = -INFINITY;  // running row max, log2 units (scores * scale * log2 e)
+      float l = 0.f;        // running sum of 2^(x - m)
+#pragma unroll 1
+      for (int j = 0; j < nx; ++j, ++k) {
+        // S_x(j) was issued after O_x += P_x(j-1) V_{j-1} completed, so O_x is
+        // stable once S_x(j) has landed.
+        if (!(ok = mbar_wait(&bars[kBarSFull + x], k & 1, status))) break;
+        tc_fence_after();
+        float s[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + 32 * c));
-      tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + 32 * c));
+        tmem_wait_ld();
 
-      const int kv0 = (jb + j) * kTileRows;
-      if ((CAUSAL && (MODE != kSquare ? kv0 + kTileRows - 1 > imin_x + off : j == nx - 1)) || kv0 + kTileRows > Nk) {
-        int lim = Nk - kv0;                                  // keys >= Nk do not exist
-        if (CAUSAL) lim = min(lim, qi + off - kv0 + 1);      // key j visible iff j <= query + off
+        const int kv0 = (w.jb + j) * kTileRows;
+        if ((CAUSAL && (MODE != kSquare ? kv0 + kTileRows - 1 > imin_x + off : j == nx - 1)) || kv0 + kTileRows > Nk) {
+          int lim = Nk - kv0;                                  // keys >= Nk do not exist
+          if (CAUSAL) lim = min(lim, qi + off - kv0 + 1);      // key j visible iff j <= query + off
 #pragma unroll
-        for (int e = 0; e < 128; ++e)
-          if (e >= lim) s[e] = -INFINITY;
-      }
-      // Row max: 8 independent chains of 3-input max.
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        // chain k covers columns k, k + 8, ..., k + 120
-        float v = fmax3(s[k], s[k + 8], s[k + 16]);
-#pragma unroll
-        for (int i = 24; i <= 104; i += 16) v = fmax3(v, s[k + i], s[k + i + 8]);
-        mx8[k] = fmaxf(v, s[k + 120]);
-      }
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      const float m_new = fmaxf(m, mx * scale_log2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const bool grow = m_use > m;  // always true on the first tile
-      const float alpha = ex2_approx(m - m_use);
-
-      // P = 2^(s * scale_log2 - m) on packed pairs; 4 independent pair sums.
-      const uint64_t negm2 = f2_pack(-m_use, -m_use);
-      // P goes to TMEM (bf16 pairs over the first 64 S columns, all of which
-      // are already in registers) 16 columns at a time.
-      uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = 32 * c + 2 * i;
-          const float2 xx = f2_unpack(ffma2(f2_pack(s[e], s[e + 1]), scale2, negm2));
-          const float p0 = ex2_approx(xx.x), p1 = ex2_approx(xx.y);
-          acc[i & 3] = fadd2(acc[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 128; ++e)
+            if (e >= lim) s[e] = -INFINITY;
         }
-        tmem_st16u(tS + 16 * c, pk);
-      }
-      const float2 a01 = f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])));
-      const float rs = a01.x + a01.y;
-
-      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
-        const uint64_t alpha2 = f2_pack(alpha, alpha);
-        if constexpr (D >= 32) {
+        // Row max: 8 independent chains of 3-input max.
+        float mx8[8];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(tO + c * 32, o);
+        for (int c = 0; c < 8; ++c) {
+          // chain c covers columns c, c + 8, ..., c + 120
+          float v = fmax3(s[c], s[c + 8], s[c + 16]);
+#pragma unroll
+          for (int i = 24; i <= 104; i += 16) v = fmax3(v, s[c + i], s[c + i + 8]);
+          mx8[c] = fmaxf(v, s[c + 120]);
+        }
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        const float m_new = fmaxf(m, mx * scale_log2);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const bool grow = m_use > m;  // always true on the first tile
+        const float alpha = ex2_approx(m - m_use);
+
+        // P = 2^(s * scale_log2 - m) on packed pairs; 4 independent pair sums.
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        // P goes to TMEM (bf16 pairs over the first 64 S columns, all of which
+        // are already in registers) 16 columns at a time.
+        uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int e = 32 * c + 2 * i;
+            const float2 xx = f2_unpack(ffma2(f2_pack(s[e], s[e + 1]), scale2, negm2));
+            const float p0 = ex2_approx(xx.x), p1 = ex2_approx(xx.y);
+            acc[i & 3] = fadd2(acc[i & 3], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16u(tS + 16 * c, pk);
+        }
+        const float2 a01 = f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])));
+        const float rs = a01.x + a01.y;
+
+        if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+          const uint64_t alpha2 = f2_pack(alpha, alpha);
+          if constexpr (D >= 32) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                const float2 rr = f2_unpack(fmul2(f2_pack(o[e], o[e + 1]), alpha2));
+                o[e] = rr.x;
+                o[e + 1] = rr.y;
+              }
+              tmem_st32(tO + c * 32, o);
+            }
+          } else {
+            float o[16];
+            tmem_ld16(tO, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 r = f2_unpack(fmul2(f2_pack(o[e], o[e + 1]), alpha2));
-              o[e] = r.x;
-              o[e + 1] = r.y;
-            }
-            tmem_st32(tO + c * 32, o);
+            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+            tmem_st16(tO, o);
           }
-        } else {
-          float o[16];
-          tmem_ld16(tO, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] *= alpha;
-          tmem_st16(tO, o);
         }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarPFull + x]);
+        l = l * alpha + rs;
+        m = m_use;
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarPFull + x]);
-      l = l * alpha + rs;
-      m = m_use;
-    }
-    // ------------------------------------------------------------ epilogue
-    // One split: O / l in bf16 and LSE.  Several splits: this split's O / l
-    // and LSE in fp32 for the combine kernel.  A row that sees no key gets
-    // O = 0, LSE = -inf.
-    const bool valid = q_row < M;
-    const bool partial = MODE == kGeneral && p.splits > 1;
-    const int vrow = valid ? q_row : 0;
-    // o_row: row of o (or o_part) in units of D elements; lse_idx: index into lse.
-    size_t o_row, lse_idx;
-    if constexpr (MODE == kVarlen) {
-      o_row = static_cast<size_t>(q_base + vrow) * p.RH + rh;
-      lse_idx = static_cast<size_t>(rh) * p.total_q + q_base + vrow;
-    } else {
-      o_row = (partial ? static_cast<size_t>(split) * p.RH + rh : static_cast<size_t>(rh)) * p.M + vrow;
-      lse_idx = o_row;
-    }
-    if (MODE != kSquare && nx == 0) {
-      if (valid && ok) {
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      // One split: O / l in bf16 and LSE.  Several splits: this split's O / l
+      // and LSE in fp32 for the combine kernel.  A row that sees no key gets
+      // O = 0, LSE = -inf.
+      const bool valid = q_row < w.M;
+      const bool partial = MODE == kGeneral && p.splits > 1;
+      const int vrow = valid ? q_row : 0;
+      // o_row: row of o (or o_part) in units of D elements; lse_idx: index into lse.
+      size_t o_row, lse_idx;
+      if constexpr (MODE == kVarlen) {
+        o_row = static_cast<size_t>(w.q_base + vrow) * p.RH + w.rh;
+        lse_idx = static_cast<size_t>(w.rh) * p.total_q + w.q_base + vrow;
+      } else {
+        o_row = (partial ? static_cast<size_t>(w.split) * p.RH + w.rh : static_cast<size_t>(w.rh)) * p.M + vrow;
+        lse_idx = o_row;
+      }
+      if (nx == 0) {
+        if (!valid) break;
         if (partial) {
           float4* dst = reinterpret_cast<float4*>(p.o_part + o_row * D);
 #pragma unroll
@@ -426,8 +532,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
           p.lse[lse_idx] = -INFINITY;
         }
+        break;
       }
-    } else if (ok && mbar_wait(&bars[kBarPVDone + x], (nx - 1) & 1, status)) {
+      // The warp reads O (all lanes: tcgen05.ld is warp-wide) only after its
+      // unit's last PV_x has completed; the next unit's first PV_x (which
+      // overwrites O_x) waits for this warp's next P_x, so the read-out cannot
+      // race it.
+      if (!(ok = mbar_wait(&bars[kBarPVDone + x], (k - 1) & 1, status))) break;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       constexpr int kC = D >= 32 ? 32 : 16;
@@ -464,6 +575,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         else
           p.lse[lse_idx] = lse_row;
       }
+      } while (false);
+      if (!ok) break;
+      u = next_unit(bars, sched, n, false, status, ok);
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&bars[kBarSchedEmpty + (n & 1)]);
     }
     tc_fence_before();
   }
@@ -489,8 +605,10 @@ int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stre
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
-  const unsigned outer = static_cast<unsigned>(varlen ? p.batches : p.splits);  // sequences or key splits
-  const dim3 grid(static_cast<unsigned>(num_pairs) * static_cast<unsigned>(p.RH) * outer);
+  // One CTA per unit; running CTAs take over the units of CTAs that have
+  // not started (cluster launch control), so at most one CTA per SM ever runs.
+  const long long units = static_cast<long long>(num_pairs) * p.RH * (varlen ? p.batches : p.splits);
+  const dim3 grid(static_cast<unsigned>(units > 0 ? units : 1));
   const float scale_log2 = scale * 1.44269504088896341f;
   kern<<<grid, kFwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, p, scale_log2);
   return static_cast<int>(cudaGetLastError());

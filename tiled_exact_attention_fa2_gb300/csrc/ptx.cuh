@@ -22,6 +22,7 @@ enum DeviceStatus : int {
   kDevWaitTimeout = 1,
   kDevSmemMisaligned = 2,
   kDevBadSeqlens = 3,  // cu_seqlens not non-decreasing within [0, total] or a length above the stated maximum
+  kDevBadSchedule = 4,  // the hardware scheduler returned a block index outside the grid
 };
 
 // ---------------------------------------------------------------- generic
@@ -172,6 +173,39 @@ __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk
 // proxy (tcgen05.mma operand reads, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Dynamic persistent scheduling with the hardware's own queue: a running CTA
+// asks the scheduler to cancel one CTA of the same grid that has not started
+// yet and then does that CTA's work itself.  The 16-byte response is written
+// (asynchronously) to `resp` in shared memory, 16-byte aligned, and completes
+// 16 transaction bytes on `bar`.  After a failed request (nothing left to
+// cancel) a CTA must not issue another.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Decode a completed response: the x block index of the cancelled CTA, or
+// -1 if the request failed.
+__device__ __forceinline__ int clc_cancelled_block_x(const void* resp) {
+  uint32_t canceled, bx;
+  asm volatile(
+      "{\n\t.reg .b64 lo, hi;\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.v2.b64 {lo, hi}, [%2];\n\t"
+      "mov.b128 r, {lo, hi};\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t"
+      "mov.b32 %1, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(canceled), "=r"(bx)
+      : "r"(smem_u32(resp))
+      : "memory");
+  return canceled ? static_cast<int>(bx) : -1;
 }
 
 // ---------------------------------------------------------------- tcgen05
