@@ -16,6 +16,7 @@ every rank runs its own batch of the same shape; no data-path collective.
 from __future__ import annotations
 
 import argparse
+import itertools
 import json
 import os
 import statistics
@@ -227,6 +228,96 @@ def run_reference(args, w, causal):
 
 
 # --------------------------------------------------------------------------- GPU arm
+def _stats(xs):
+    xs = sorted(xs)
+    return {"mean": statistics.mean(xs), "median": statistics.median(xs), "min": xs[0],
+            "p90": xs[min(len(xs) - 1, int(round(0.9 * (len(xs) - 1))))]}
+
+
+def _time_ms(fn, stream, iters=10, warm=3):
+    """Mean milliseconds of fn() over `iters` calls, CUDA events on `stream`."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def measure_rows(fa2, dev, stream, peaks):
+    """Throughput of the widened rows (grouped-query prefill, split-KV decoding,
+    variable-length batch) on synthetic device-generated inputs."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2024)
+
+    def rnd(*shape):
+        return torch.randn(*shape, device=dev, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+    out = {}
+    tf = lambda fl, ms: fl / (ms * 1e-3) / 1e12
+    # Grouped-query prefill: 32 query heads over 8 K/V heads.
+    B, H, Hkv, N, d = 1, 32, 8, 16384, 128
+    q, dO = rnd(B, H, N, d), rnd(B, H, N, d)
+    k, v = rnd(B, Hkv, N, d), rnd(B, Hkv, N, d)
+    o, lse = fa2.fa2_fwd_gqa(q, k, v, causal=True, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    f_ms = _time_ms(lambda: fa2.fa2_fwd_gqa(q, k, v, o=o, lse=lse, causal=True, stream=stream), stream)
+    b_ms = _time_ms(lambda: fa2.fa2_bwd_gqa(q, k, v, o, dO, lse, dq=dq, dk=dk, dv=dv, causal=True, stream=stream),
+                    stream)
+    ff, bf = 2.0 * B * H * N * N * d, 5.0 * B * H * N * N * d
+    out["gqa_prefill"] = {"workload": f"B={B} H={H} H_kv={Hkv} N={N} d={d} causal",
+                          "fwd_ms": f_ms, "fwd_tflops": tf(ff, f_ms), "bwd_ms": b_ms, "bwd_tflops": tf(bf, b_ms),
+                          "fwd_pct_of_peak_burst": 100 * tf(ff, f_ms) / peaks["bf16_tflops"],
+                          "bwd_pct_of_peak_burst": 100 * tf(bf, b_ms) / peaks["bf16_tflops"]}
+    del q, dO, k, v, o, lse, dq, dk, dv
+    # Split-KV decoding: one query per sequence against a 16K key-value cache.
+    B, H, Hkv, Nq, Nk, d, splits = 8, 32, 8, 1, 16384, 128, 16
+    q, k, v = rnd(B, H, Nq, d), rnd(B, Hkv, Nk, d), rnd(B, Hkv, Nk, d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, fa2.load_library().fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, splits)),
+                     dtype=torch.uint8, device=dev)
+    ms = _time_ms(lambda: fa2.fa2_fwd_splitkv(q, k, v, splits, o=o, lse=lse, workspace=ws, causal=True,
+                                              stream=stream), stream, iters=50)
+    nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["decode_splitkv"] = {"workload": f"B={B} H={H} H_kv={Hkv} Nq={Nq} Nk={Nk} d={d} causal, {splits} splits",
+                             "ms": ms, "algorithmic_bytes": nbytes,
+                             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                          "frac": gbs / peaks["hbm_gbs"]},
+                             "note": "K and V read once per K/V head (query heads of a group share the tile); "
+                                     "launches: split kernel + combine kernel"}
+    del q, k, v, o, lse, ws
+    # Variable-length batch: 16 packed sequences of 1..8192 tokens.
+    lens = workloads.varlen_lengths(16, 8192, seed=7)
+    H, d = 32, 128
+    T = sum(lens)
+    q, k, v, dO = rnd(T, H, d), rnd(T, H, d), rnd(T, H, d), rnd(T, H, d)
+    cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device=dev)
+    mx = max(lens)
+    o, lse = fa2.fa2_fwd_varlen(q, k, v, cu, cu, mx, mx, causal=True, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa2.load_library().fa2_bwd_varlen_workspace_bytes(H, T, d), dtype=torch.uint8, device=dev)
+    f_ms = _time_ms(lambda: fa2.fa2_fwd_varlen(q, k, v, cu, cu, mx, mx, o=o, lse=lse, causal=True, stream=stream),
+                    stream)
+    b_ms = _time_ms(lambda: fa2.fa2_bwd_varlen(q, k, v, o, dO, lse, cu, cu, mx, mx, dq=dq, dk=dk, dv=dv,
+                                               workspace=ws, causal=True, stream=stream), stream)
+    sq = sum(L * L for L in lens)
+    ff, bf = 2.0 * H * sq * d, 5.0 * H * sq * d
+    out["varlen"] = {"workload": f"16 packed sequences, lengths {lens}, H={H} d={d} causal",
+                     "fwd_ms": f_ms, "fwd_tflops": tf(ff, f_ms), "bwd_ms": b_ms, "bwd_tflops": tf(bf, b_ms),
+                     "fwd_pct_of_peak_burst": 100 * tf(ff, f_ms) / peaks["bf16_tflops"],
+                     "bwd_pct_of_peak_burst": 100 * tf(bf, b_ms) / peaks["bf16_tflops"]}
+    torch.cuda.synchronize()
+    if fa2.fa2_device_status(reset=True) != 0:
+        raise RuntimeError("a kernel reported a device status during the row measurements")
+    return out
+
+
 def run_gpu(args, w, causal):
     world, rank, local = _dist()
     import tiled_exact_attention_fa2_gb300 as fa2
@@ -279,9 +370,11 @@ def run_gpu(args, w, causal):
     total_ms = _max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
     timed = ev[args.warmup:]
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in timed)
+    fwd_list = [e[0].elapsed_time(e[1]) for e in timed]
+    main_list = [e[2].elapsed_time(e[3]) for e in timed]
+    fwd_ms = statistics.mean(fwd_list)
     pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in timed)
-    main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in timed)
+    main_ms = statistics.mean(main_list)
     conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in timed)
     bwd_ms = pre_ms + main_ms + conv_ms
 
@@ -339,11 +432,15 @@ def run_gpu(args, w, causal):
                      "algorithmic_bytes": algorithmic_bytes(dominant, B, H, N, d),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
                      "frac_of_burst": dom_tf / peaks["bf16_tflops"]},
+        "timing": {"fwd_ms": _stats(fwd_list), "bwd_main_ms": _stats(main_list),
+                   "method": "CUDA events on the launching stream around each kernel of every timed step"},
         "gpu_launches": 4 * args.steps,
         "device_status": status,
         "clocks": clocks,
         "e2e": e2e,
     }
+    if world == 1 and not args.no_rows:
+        line["rows"] = measure_rows(fa2, dev, stream, peaks)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, causal)
     print(json.dumps(line), flush=True)
@@ -363,6 +460,7 @@ def main():
     ap.add_argument("--noncausal", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the GQA / decoding / varlen measurements")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
