@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(256) fa2_bwd_preprocess_kernel(const __nv_bflo
                                                                  float* __restrict__ Dvec,
                                                                  float* __restrict__ dq_acc, long long rows) {
   constexpr int kTpr = D / 8;  // threads per row, 16 bytes each
+  griddep_wait();
+  griddep_launch_dependents();
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / kTpr;
   const int sub = threadIdx.x % kTpr;
   float acc = 0.f;
@@ -154,6 +156,8 @@ __global__ void __launch_bounds__(256) fa2_bwd_preprocess_kernel(const __nv_bflo
 __global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __restrict__ dq_acc,
                                                              __nv_bfloat16* __restrict__ dq, long long n8,
                                                              float scale) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(dq_acc) + 2 * i);
@@ -206,6 +210,7 @@ __global__ void __launch_bounds__(512, 1)
   // Q, dO and fp32 dQ rows stay in L2 while its CTAs run; inside a group the
   // key/value tile index is the slow one (causal work shrinks with jt, so
   // heavy tiles go first).
+  if constexpr (VARLEN) griddep_wait();  // the geometry below reads cu_seqlens
   const int kv_tiles_grid = ((VARLEN ? p.max_k : p.N) + kTileRows - 1) / kTileRows;
   const int BHkv = VARLEN ? p.Hkv : p.BH / group;
   const int per_batch = BHkv * kv_tiles_grid;
@@ -283,6 +288,8 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if constexpr (!VARLEN) griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
@@ -643,9 +650,8 @@ int launch_preprocess_t(const void* o, const void* dO, float* Dvec, float* dq_ac
   constexpr int kTpr = D / 8;
   const long long threads = rows * kTpr;
   const long long blocks = (threads + 255) / 256;
-  fa2_bwd_preprocess_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, rows);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(fa2_bwd_preprocess_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                    static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, rows);
 }
 
 template <int D, bool CAUSAL>
@@ -663,8 +669,8 @@ int launch_bwd_main_t(const TmapSet& tm, BwdProblem p, float scale, cudaStream_t
   // accumulator and LSE, D of its `group` query heads.
   const size_t per_head = static_cast<size_t>(p.group) * rows_q * (static_cast<size_t>(D) * 8 + 8);
   p.heads_per_group = heads_per_l2_group(per_head, kv_heads);
-  kern<<<grid, kBwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, tm.dqacc, p, scale, scale * kLog2e);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(kern, grid, dim3(kBwdThreads), C::kBytes, stream, tm.q, tm.k, tm.v, tm.dO, tm.dqacc, p, scale,
+                    scale * kLog2e);
 }
 
 int launch_dq_convert(const float* dq_acc, void* dq, long long elems, float scale, cudaStream_t stream) {
@@ -672,9 +678,8 @@ int launch_dq_convert(const float* dq_acc, void* dq, long long elems, float scal
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  fa2_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(fa2_dq_convert_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, dq_acc,
+                    static_cast<__nv_bfloat16*>(dq), n8, scale);
 }
 
 }  // namespace

@@ -237,6 +237,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -610,8 +612,7 @@ int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stre
   const long long units = static_cast<long long>(num_pairs) * p.RH * (varlen ? p.batches : p.splits);
   const dim3 grid(static_cast<unsigned>(units > 0 ? units : 1));
   const float scale_log2 = scale * 1.44269504088896341f;
-  kern<<<grid, kFwdThreads, C::kBytes, stream>>>(tm.q, tm.k, tm.v, p, scale_log2);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(kern, grid, dim3(kFwdThreads), C::kBytes, stream, tm.q, tm.k, tm.v, p, scale_log2);
 }
 
 // Merge per-split results: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
@@ -623,6 +624,8 @@ __global__ void __launch_bounds__(256) fa2_splitkv_combine_kernel(const float* _
                                                                   float* __restrict__ lse, long long rows,
                                                                   int splits) {
   constexpr int kPer = D >= 32 ? D / 32 : 1;  // columns per lane
+  griddep_wait();
+  griddep_launch_dependents();
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -671,13 +674,12 @@ int launch_splitkv_combine(const FwdProblem& p, int d, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
   auto o = static_cast<__nv_bfloat16*>(p.o);
   switch (d) {
-    case 16: fa2_splitkv_combine_kernel<16><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
-    case 32: fa2_splitkv_combine_kernel<32><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
-    case 64: fa2_splitkv_combine_kernel<64><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
-    case 128: fa2_splitkv_combine_kernel<128><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o, p.lse, rows, p.splits); break;
+    case 16: return launch_pdl(fa2_splitkv_combine_kernel<16>, dim3(blocks), dim3(256), 0, stream, p.o_part, p.lse_part, o, p.lse, rows, p.splits);
+    case 32: return launch_pdl(fa2_splitkv_combine_kernel<32>, dim3(blocks), dim3(256), 0, stream, p.o_part, p.lse_part, o, p.lse, rows, p.splits);
+    case 64: return launch_pdl(fa2_splitkv_combine_kernel<64>, dim3(blocks), dim3(256), 0, stream, p.o_part, p.lse_part, o, p.lse, rows, p.splits);
+    case 128: return launch_pdl(fa2_splitkv_combine_kernel<128>, dim3(blocks), dim3(256), 0, stream, p.o_part, p.lse_part, o, p.lse, rows, p.splits);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
-  return static_cast<int>(cudaGetLastError());
 }
 
 int read_fwd_status(int* value, bool reset) {

@@ -12,6 +12,23 @@ struct TmapSet {
   CUtensorMap q, k, v, dO, dqacc;
 };
 
+// Launch `kern` on `stream` with programmatic stream serialisation (the
+// kernel calls griddep_wait() before its first global memory access).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...));
+}
+
 // Every function below returns 0 or the cudaError_t value of the failure.
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).

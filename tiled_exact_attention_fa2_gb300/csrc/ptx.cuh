@@ -175,6 +175,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of this library is launched with programmatic stream
+// serialisation: it may be scheduled while the previous kernel in the stream
+// is still finishing, and runs its prologue (barrier setup, TMEM allocation)
+// meanwhile.  griddep_wait() blocks until the previous kernel has completed
+// and its memory writes are visible; it must come before the first global
+// memory access.  griddep_launch_dependents() lets the next kernel in the
+// stream be scheduled early in the same way.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster launch control
 // Dynamic persistent scheduling with the hardware's own queue: a running CTA
 // asks the scheduler to cancel one CTA of the same grid that has not started
