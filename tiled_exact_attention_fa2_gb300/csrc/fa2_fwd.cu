@@ -211,6 +211,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int lane = lane_id();
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
+  // Decoding (split-KV with at most 128 packed rows per row-head): tile B
+  // never has rows, so tile A double-buffers S over both S column ranges
+  // (and uses tile B's S-full / P-full / PV-done barriers for the second
+  // buffer): S(j+1) is computed while the softmax of tile j runs.
+  const bool dual = MODE == kGeneral && num_row_tiles == 1;
 
   if (threadIdx.x == 8 * 32) {
     for (int s = 0; s < 2; ++s) {
@@ -320,29 +325,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q (K-major) x K (K-major)
       constexpr uint32_t kIdescO = make_idesc_bf16(128, D, false, true);     // P (TMEM) x V (MN-major)
       const uint32_t sQ0 = smem_u32(smem + C::kQ), sK0 = smem_u32(smem + C::kK), sV0 = smem_u32(smem + C::kV);
-      const uint32_t tSx = tmem + (x ? C::kColS1 : C::kColS0), tOx = tmem + (x ? C::kColO1 : C::kColO0);
-      // S_x = Q_x K^T for the K/V tile in stage st, into TMEM S_x.
-      auto issue_s = [&](int st) {
+      const uint32_t tOx = tmem + (x ? C::kColO1 : C::kColO0);
+      // S buffer of the tile's k-th S: S_x, or S_A / S_B alternately when dual.
+      auto sbuf = [&](int kk) { return dual ? (kk & 1) : x; };
+      auto sphase = [&](int kk) { return dual ? (kk >> 1) & 1 : kk & 1; };
+      // S = Q_x K^T for the K/V tile in stage st, into S buffer b.
+      auto issue_s = [&](int st, int b) {
         uint32_t sQ = sQ0, sK = sK0;
         opaque(sQ);
         opaque(sK);
         const uint32_t qb = sQ + x * T::kTileBytes, kb = sK + st * T::kTileBytes;
+        const uint32_t tS = tmem + (b ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tSx, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
-        mma_commit(&bars[kBarSFull + x]);
+          mma_bf16_ss(tS, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kBarSFull + b]);
         mma_commit(&bars[kBarKEmpty + st]);
       };
-      // O_x (+)= P_x V with P_x read from the first 64 columns of S_x.
-      auto issue_pv = [&](int st, bool first) {
+      // O_x (+)= P V with P read from the first 64 columns of S buffer b.
+      auto issue_pv = [&](int st, bool first, int b) {
         uint32_t sV = sV0;
         opaque(sV);
         const uint32_t vb = sV + st * T::kTileBytes;
+        const uint32_t tP = tmem + (b ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ts(tOx, tSx + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (!first || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarPVDone + x]);
+          mma_bf16_ts(tOx, tP + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarPVDone + b]);
         mma_commit(&bars[kBarVEmpty + st]);
+      };
+      // S number kk may overwrite its buffer once the PV that last read it
+      // (number kk - 2 when dual, kk - 1 otherwise) has completed.
+      auto s_ready = [&](int kk) -> bool {
+        const int prev = dual ? kk - 2 : kk - 1;
+        return prev < 0 || mbar_wait(&bars[kBarPVDone + sbuf(prev)], sphase(prev), status);
       };
       int g = 0;   // K/V tiles of all units so far (same count as the producer's)
       int k = 0;   // S_x / P_x / PV_x issued so far (phase k & 1)
@@ -359,20 +375,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!(ok = mbar_wait(&bars[kBarQFull + x], qn & 1, status))) break;
           ++qn;
         }
+        // Order: S(0); then per tile j: [dual: S(j+1)], PV(j), [else: S(j+1)].
+        if (nx > 0) {
+          const int st = g & 1;
+          if (!(ok = s_ready(k) && mbar_wait(&bars[kBarKFull + st], (g >> 1) & 1, status))) break;
+          tc_fence_after();
+          issue_s(st, sbuf(k));
+          if (nx == 1) mma_commit(&bars[kBarQEmpty + x]);  // last use of Q_x in this unit
+        }
 #pragma unroll 1
         for (int j = 0; j < nx; ++j) {
-          const int gj = g + j, st = gj & 1;
-          // S_x overwrites the P_x columns the previous PV_x reads.
-          if (k >= 1 && !(ok = mbar_wait(&bars[kBarPVDone + x], (k - 1) & 1, status))) break;
-          if (!(ok = mbar_wait(&bars[kBarKFull + st], (gj >> 1) & 1, status))) break;
-          tc_fence_after();
-          issue_s(st);
-          if (j + 1 == nx) mma_commit(&bars[kBarQEmpty + x]);  // last use of Q_x in this unit
+          const int gj = g + j, st = gj & 1, st1 = st ^ 1;
+          if (dual && j + 1 < nx) {
+            if (!(ok = s_ready(k + 1) && mbar_wait(&bars[kBarKFull + st1], ((gj + 1) >> 1) & 1, status))) break;
+            tc_fence_after();
+            issue_s(st1, sbuf(k + 1));
+            if (j + 2 == nx) mma_commit(&bars[kBarQEmpty + x]);
+          }
           if (!(ok = mbar_wait(&bars[kBarVFull + st], (gj >> 1) & 1, status))) break;
-          if (!(ok = mbar_wait(&bars[kBarPFull + x], k & 1, status))) break;
+          // (P-full barriers are per S buffer too: with S(j+1) already issued
+          // the softmax can finish P(j+1) before this wait, and one barrier
+          // would then be two phases ahead.)
+          if (!(ok = mbar_wait(&bars[kBarPFull + sbuf(k)], sphase(k), status))) break;
           tc_fence_after();
-          issue_pv(st, j == 0);
+          issue_pv(st, j == 0, sbuf(k));
           ++k;
+          if (!dual && j + 1 < nx) {
+            // S_x(j+1) overwrites the P_x columns the PV above reads.
+            if (!(ok = s_ready(k) && mbar_wait(&bars[kBarKFull + st1], ((gj + 1) >> 1) & 1, status))) break;
+            tc_fence_after();
+            issue_s(st1, sbuf(k));
+            if (j + 2 == nx) mma_commit(&bars[kBarQEmpty + x]);
+          }
         }
         if (!ok) break;
         // K/V tiles this query tile does not visit: release them once, in
@@ -399,10 +433,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int x = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + (x ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_base + (x ? C::kColO1 : C::kColO0);
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-    int k = 0;  // S_x tiles consumed so far (phase k & 1)
+    // S buffer / barrier phase of the tile's kk-th S (see the issuer).
+    auto sbuf = [&](int kk) { return dual ? (kk & 1) : x; };
+    auto sphase = [&](int kk) { return dual ? (kk >> 1) & 1 : kk & 1; };
+    int k = 0;  // S_x tiles consumed so far
     bool ok = true;
 #pragma unroll 1
     for (int n = 0, u = static_cast<int>(blockIdx.x); ok && u >= 0; ++n) {
@@ -418,10 +454,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float l = 0.f;        // running sum of 2^(x - m)
 #pragma unroll 1
       for (int j = 0; j < nx; ++j, ++k) {
-        // S_x(j) was issued after O_x += P_x(j-1) V_{j-1} completed, so O_x is
-        // stable once S_x(j) has landed.
-        if (!(ok = mbar_wait(&bars[kBarSFull + x], k & 1, status))) break;
+        // Without dual buffering S_x(j) was issued after O_x += P_x(j-1)
+        // V_{j-1} completed, so O_x is stable once S_x(j) has landed; with it,
+        // the O rescale below waits for that PV first.
+        const int b = sbuf(k);
+        if (!(ok = mbar_wait(&bars[kBarSFull + b], sphase(k), status))) break;
         tc_fence_after();
+        const uint32_t tS = tmem + lane_base + (b ? C::kColS1 : C::kColS0);
         float s[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + 32 * c));
@@ -473,6 +512,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float rs = a01.x + a01.y;
 
         if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+          if (dual) {
+            if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
+            tc_fence_after();
+          }
           const uint64_t alpha2 = f2_pack(alpha, alpha);
           if constexpr (D >= 32) {
 #pragma unroll
@@ -500,7 +543,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarPFull + x]);
+        if (lane == 0) mbar_arrive(&bars[kBarPFull + b]);
         l = l * alpha + rs;
         m = m_use;
       }
@@ -540,7 +583,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // unit's last PV_x has completed; the next unit's first PV_x (which
       // overwrites O_x) waits for this warp's next P_x, so the read-out cannot
       // race it.
-      if (!(ok = mbar_wait(&bars[kBarPVDone + x], (k - 1) & 1, status))) break;
+      if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       constexpr int kC = D >= 32 ? 32 : 16;
