@@ -126,3 +126,30 @@ def test_nonzero_stream_and_invalid_args_raise():
         fa2.fa2_fwd(g["q"], g["k"], g["v"], scale=-1.0)
     with pytest.raises(fa2.FA2Error):  # output aliasing an input
         fa2.fa2_fwd(g["q"], g["k"], g["v"], o=g["q"])
+
+
+def test_host_step_pipeline_matches_device_calls():
+    # attention_step_from_host pipelines host<->device copies with the
+    # kernels over groups of heads; its results must be those of plain
+    # fa2_fwd / fa2_bwd on the same inputs (bit-identical except dQ, whose
+    # fp32 reduction order varies between runs).
+    import tiled_exact_attention_fa2_gb300 as fa2
+    from parity_util import check_grad, to_np
+    w = workloads.WORKLOADS["small"]
+    x = workloads.workload_inputs(w)
+    g = {k: t.to(DEV) for k, t in x.items()}
+    o, lse = fa2.fa2_fwd(g["q"], g["k"], g["v"], causal=True)
+    dq, dk, dv = fa2.fa2_bwd(g["q"], g["k"], g["v"], o, g["dO"], lse, causal=True)
+    host = {k: x[k].pin_memory() for k in ("q", "k", "v", "dO")}
+    host.update({k: torch.zeros_like(host["q"]).pin_memory() for k in ("o", "dq", "dk", "dv")})
+    host["lse"] = torch.zeros((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    devb = {k: torch.empty_like(t) for k, t in g.items()}
+    devb.update({k: torch.empty_like(g["q"]) for k in ("o", "dq", "dk", "dv")})
+    devb["lse"] = torch.empty_like(lse)
+    for chunks in (1, 3):
+        fa2.attention_step_from_host(host, devb, True, None, None, chunks=chunks)
+        torch.cuda.synchronize()
+        assert fa2.fa2_device_status(reset=True) == 0
+        assert torch.equal(host["o"], o.cpu()) and torch.equal(host["lse"], lse.cpu())
+        assert torch.equal(host["dk"], dk.cpu()) and torch.equal(host["dv"], dv.cpu())
+        check_grad(to_np(host["dq"]), to_np(dq), "dQ")

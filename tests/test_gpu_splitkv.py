@@ -24,6 +24,11 @@ CASES = [
     (1, 4, 2, 64, 64, 32, True, 1),        # one split == plain forward
     (1, 2, 1, 3, 300, 16, False, 5),
     (1, 8, 4, 1, 130, 128, True, 64),      # more splits requested than key tiles
+    # long caches: many key tiles per split and several units per CTA, so the
+    # decode path's double-buffered S runs ahead of slow K/V loads
+    (4, 16, 4, 1, 16384, 128, True, 16),
+    (1, 8, 2, 1, 65536, 128, True, 16),
+    (2, 8, 8, 3, 20000, 64, True, 8),      # several queries per sequence, ragged cache
 ]
 
 

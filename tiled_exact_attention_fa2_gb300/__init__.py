@@ -397,23 +397,69 @@ def fa2_bwd_stages(q, k, v, o, dO, lse, Dvec, dq_acc, dq, dk, dv, scale: Optiona
     return dq, dk, dv
 
 
+_COPY_STREAMS = {}
+
+
+def _copy_streams(device):
+    """Two side streams per device: host->device and device->host copies."""
+    key = torch.device(device).index
+    if key not in _COPY_STREAMS:
+        _COPY_STREAMS[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    return _COPY_STREAMS[key]
+
+
 def attention_step_from_host(host: dict, dev: dict, causal: bool = True, scale: Optional[float] = None,
-                             stream=None) -> dict:
+                             stream=None, chunks: Optional[int] = None) -> dict:
     """One forward + backward pass starting from pinned host tensors.
 
     ``host`` holds pinned CPU bf16 tensors q, k, v, dO and pinned outputs
-    o, lse, dq, dk, dv; ``dev`` holds device buffers of the same names.
-    Copies the inputs host->device, runs fa2_fwd and fa2_bwd, copies every
-    result device->host, all on one stream (asynchronously; synchronise the
-    stream before reading ``host``).
+    o, lse, dq, dk, dv; ``dev`` holds device buffers of the same names
+    ([B, H, N, d]; lse [B, H, N]).  Every (batch, head) is an independent
+    problem, so the B * H heads are processed in ``chunks`` groups (default:
+    up to 4) as a pipeline over three streams: the host->device copy of group
+    c + 1 and the device->host copy of group c - 1 run while fa2_fwd and
+    fa2_bwd of group c run on ``stream``.  Everything is enqueued
+    asynchronously and ``stream`` waits for the last copy: synchronise it
+    before reading ``host``.
     """
     s = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(s):
-        for name in ("q", "k", "v", "dO"):
-            dev[name].copy_(host[name], non_blocking=True)
-        fa2_fwd(dev["q"], dev["k"], dev["v"], dev["o"], dev["lse"], scale, causal, s)
-        fa2_bwd(dev["q"], dev["k"], dev["v"], dev["o"], dev["dO"], dev["lse"], dev["dq"], dev["dk"], dev["dv"],
-                scale, causal, s)
-        for name in ("o", "lse", "dq", "dk", "dv"):
-            host[name].copy_(dev[name], non_blocking=True)
+    device = dev["q"].device
+    B, H, N, d = dev["q"].shape
+    BH = B * H
+    n = max(1, min(BH, chunks if chunks is not None else 4))
+    bounds = [BH * i // n for i in range(n + 1)]
+    cin, cout = _copy_streams(device)
+    flat = {k: (t.view(BH, N, d) if k != "lse" else t.view(BH, N)) for k, t in dev.items()}
+    hflat = {k: (t.view(BH, N, d) if k != "lse" else t.view(BH, N)) for k, t in host.items()}
+    start = torch.cuda.Event()
+    start.record(s)
+    cin.wait_event(start)  # the device buffers are free once earlier work on `stream` is done
+    loaded, computed = [], []
+    for c in range(n):
+        a, b = bounds[c], bounds[c + 1]
+        with torch.cuda.stream(cin):
+            for name in ("q", "k", "v", "dO"):
+                flat[name][a:b].copy_(hflat[name][a:b], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(cin)
+            loaded.append(e)
+    for c in range(n):
+        a, b = bounds[c], bounds[c + 1]
+        s.wait_event(loaded[c])
+        view = {k: flat[k][a:b].unsqueeze(0) for k in flat}
+        fa2_fwd(view["q"], view["k"], view["v"], view["o"], view["lse"], scale, causal, s)
+        fa2_bwd(view["q"], view["k"], view["v"], view["o"], view["dO"], view["lse"], view["dq"], view["dk"],
+                view["dv"], scale, causal, s)
+        e = torch.cuda.Event()
+        e.record(s)
+        computed.append(e)
+    for c in range(n):
+        a, b = bounds[c], bounds[c + 1]
+        cout.wait_event(computed[c])
+        with torch.cuda.stream(cout):
+            for name in ("o", "lse", "dq", "dk", "dv"):
+                hflat[name][a:b].copy_(flat[name][a:b], non_blocking=True)
+    done = torch.cuda.Event()
+    done.record(cout)
+    s.wait_event(done)
     return host
