@@ -154,12 +154,24 @@ def _barrier(world):
 
 
 def _max_over_ranks(x: float, world: int) -> float:
+    """Slowest rank's value (timing is max over ranks)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(w, rank: int) -> int:
+    """Weak scaling: every rank runs the same shape on its own inputs."""
+    return w.seed + rank
+
+
+def job_tflops(world: int, flops_per_rank: float, max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * flops_per_rank / (max_ms * 1e-3) / 1e12
 
 
 # --------------------------------------------------------------------------- CPU oracle legs
@@ -327,7 +339,7 @@ def run_gpu(args, w, causal):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     B, H, N, d = w.B, w.H, w.N, w.d
-    x = workloads.make_inputs(B, H, N, d, seed=w.seed + rank, qk_mult=w.qk_mult)
+    x = workloads.make_inputs(B, H, N, d, seed=rank_seed(w, rank), qk_mult=w.qk_mult)
     g = {k: t.to(dev) for k, t in x.items()}
     o = torch.empty_like(g["q"])
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -399,11 +411,11 @@ def run_gpu(args, w, causal):
         e2e_ms = _max_over_ranks(a.elapsed_time(b), world) / args.steps
         h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "dO"))
         d2h = sum(host[k].numel() * host[k].element_size() for k in ("o", "lse", "dq", "dk", "dv"))
-        e2e = {"value": world * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+        e2e = {"value": job_tflops(world, fwd_flops + bwd_flops, e2e_ms), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     peaks = _peaks()
-    value = world * (fwd_flops + bwd_flops) / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, fwd_flops + bwd_flops, ms_step)
     fwd_tf = fwd_flops / (fwd_ms * 1e-3) / 1e12
     bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
     main_tf = bwd_flops / (main_ms * 1e-3) / 1e12
