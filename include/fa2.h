@@ -178,9 +178,10 @@ int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const
  *   the standard FA2 backward identity (the pages do not state it).
  * fa2_bwd_main: recomputes P from q, k and lse tile by tile (the article's
  *   backward-pass bullet), writes dk and dv (bf16) and ADDS the unscaled
- *   dS K into dq_acc with fp32 atomics (the order of that sum varies from run
- *   to run; the article's "Numerical Stability and Loss Drift" section notes
- *   atomic reductions as a rounding source).
+ *   dS K into dq_acc with fp32 reduce-adds performed in L2 (TMA bulk
+ *   reduce; the order of that sum varies from run to run; the article's
+ *   "Numerical Stability and Loss Drift" section notes atomic reductions as
+ *   a rounding source).
  * fa2_bwd_dq_convert: dq = bf16(scale * dq_acc).
  * Same pointer, alignment and error rules as above; Dvec and dq_acc are
  * device pointers owned by the caller.

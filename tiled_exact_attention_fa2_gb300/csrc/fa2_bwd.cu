@@ -6,32 +6,33 @@
 // attention weights are recomputed tile by tile from the saved Q, K and the
 // per-row log-sum-exp instead of being read back from a stored matrix.  The
 // same article's section "Numerical Stability and Loss Drift" names atomic
-// reductions as a rounding source; dQ here is such a reduction (fp32 atomics
-// into a zeroed accumulator), the only step whose summation order varies
-// between runs.
+// reductions as a rounding source; dQ here is such a reduction (fp32 adds
+// into a zeroed accumulator, performed in L2 by TMA reduce-add), the only
+// step whose summation order varies between runs.
 //
-// Three kernels, enqueued in this order on the caller's stream:
+// Three kernels, enqueued in this order on the caller's stream (each
+// launched with programmatic stream serialisation):
 //   1. preprocess: D = rowsum(dO * O) (fp32) and zero the fp32 dQ accumulator
 //      (HBM-bound, 16-byte coalesced loads).
-//   2. main: one CTA per (128-row key/value tile, head); loops over the query
-//      tiles that can see it (all of them, or those at or after the diagonal
-//      when causal):
+//   2. main: one CTA per (128-row key/value tile, K/V head); loops over the
+//      query tiles that can see it (all of them, or those at or after the
+//      diagonal when causal) of every query head that shares the K/V head:
 //         S^T  = K Q_i^T                   (TMEM)
-//         P^T  = exp(scale S^T - LSE_i)    (registers -> bf16 smem)
+//         P^T  = exp(scale S^T - LSE_i)    (registers -> bf16 pairs in TMEM)
 //         dP^T = V dO_i^T                  (TMEM)
-//         dV  += P^T dO_i                  (TMEM accumulator)
+//         dV  += P^T dO_i                  (TMEM accumulator, P^T from TMEM)
 //         dS^T = P^T * (dP^T - D_i)        (registers -> bf16 smem)
 //         dK  += dS^T Q_i                  (TMEM accumulator)
-//         dQ_i = dS K                      (TMEM) -> fp32 atomics into dQacc
+//         dQ_i = dS K                      (TMEM) -> TMA reduce-add into dQacc
 //      then writes dK * scale and dV as bf16.
 //   3. convert: dQ = bf16(scale * dQacc).
 //
-// Warp roles of the main kernel (192 threads): warps 0-3 compute (thread t
-// owns key row t of the tile for P/dS and query row t for the dQ drain),
-// warp 4 TMA producer, warp 5 MMA issuer and TMEM owner.
-// TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK after dV;
-// dQ gets its own D columns after dK when they fit (D <= 64) and otherwise
-// reuses the S^T columns, which are free once P^T has been read out.
+// Warp roles of the main kernel (448 threads, see kBwdThreads): two P/dS
+// warpgroups (query columns 0-63 and 64-127 of every tile; thread t owns key
+// row t = TMEM lane t), the dQ drain / epilogue warpgroup, the TMA producer
+// warp and the MMA issuer warp (also TMEM owner).
+// TMEM columns: S^T [0,128) (P^T as bf16 pairs inside each warpgroup's half),
+// dP^T [128,256) (reused by dQ_i once dS^T is formed), dV and dK after them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

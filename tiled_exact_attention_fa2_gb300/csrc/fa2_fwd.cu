@@ -1,6 +1,7 @@
 // FlashAttention-2 forward on sm_103a: TMA-fed tiles, tcgen05 MMAs with TMEM
-// accumulators and an online softmax.  One CTA per (pair of 128-row query
-// tiles, head).
+// accumulators and an online softmax.  Work unit = (pair of 128-row query
+// tiles, head [, key split or sequence]); CTAs are persistent and take units
+// from the hardware scheduler (cluster launch control).
 //
 // Method: "Revolutionizing Web-Based AI: How a Plain JavaScript Prototype
 // Paved the Way for High-Performance WebGPU Flash Attention 2", section
@@ -16,7 +17,7 @@
 // other tile's softmax runs:
 //   warps 0-3  softmax of tile A   (thread t owns row t = TMEM lane t)
 //   warps 4-7  softmax of tile B
-//   warp  8    TMA producer: Q_A, Q_B once, then K_j / V_j into 2-stage rings
+//   warp  8    TMA producer: Q_A, Q_B per unit, then K_j / V_j into 2-stage rings
 //   warp  9    MMA issuer for tile A (one thread) + TMEM owner
 //   warp 10    MMA issuer for tile B (one thread)
 // One issuer per tile, so that waiting on one tile's MMA never delays the
@@ -25,11 +26,12 @@
 // softmax overwrites the first 64 columns of S_X with P_X (bf16 pairs) and
 // O_X += P_X V_j reads P_X straight from TMEM (A operand in TMEM), so P never
 // touches shared memory.  S_X(j+1) is issued only after P_X(j) V_j has
-// completed, because it overwrites the columns that MMA reads.
+// completed, because it overwrites the columns that MMA reads (decoding,
+// where tile B is empty, double-buffers S over both ranges instead).
 // O is rescaled in TMEM only when some row of the warp sees its max grow, so
 // every row's largest weight is exactly 1.  The softmax arithmetic runs on
 // packed fp32 pairs (f32x2 FMA/ADD/MUL) and 3-input max to halve its
-// instruction count, which bounds this kernel.
+// instruction count.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

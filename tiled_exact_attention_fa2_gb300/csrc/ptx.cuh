@@ -43,21 +43,6 @@ __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 // hoisted out of a loop (keeps register pressure low in issue loops).
 __device__ __forceinline__ void opaque(uint32_t& v) { asm volatile("" : "+r"(v)); }
 
-// Named barrier over a subset of warps (id 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Per-warpgroup register reallocation (all four warps of a warpgroup execute it).
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
