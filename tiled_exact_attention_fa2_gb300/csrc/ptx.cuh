@@ -419,24 +419,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// 2^x on the FMA/ALU pipes (no MUFU), for x <= 64.  Cody-Waite reduction
-// x = j + f, j = round(x), f in [-1/2, 1/2], then 2^f by a degree-4
-// polynomial whose coefficients minimise the maximum relative error on
-// [-1/2, 1/2] (Remez exchange, constant term pinned to 1; fitted by
-// csrc/exp2_poly_fit.py), and 2^j added into the exponent field.  Maximum
-// relative error 3.7e-6 in fp32; inputs below -125 return 0.
-__device__ __forceinline__ float exp2_poly(float x) {
-  const float xc = fmaxf(x, -125.f);
-  const float t = xc + 12582912.f;  // 1.5 * 2^23: round-to-nearest integer in the low mantissa bits
-  const float j = t - 12582912.f;
-  const float f = xc - j;
-  float p = fmaf(0.009782912209630013f, f, 0.055976882576942444f);
-  p = fmaf(p, f, 0.24020710587501526f);
-  p = fmaf(p, f, 0.6931136250495911f);
-  p = fmaf(p, f, 1.f);
-  const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-  return x < -125.f ? 0.f : r;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;  // round-to-nearest-even; `lo` lands in the low half
