@@ -260,9 +260,10 @@ def _time_ms(fn, stream, iters=10, warm=3):
     return a.elapsed_time(b) / iters
 
 
-def measure_rows(fa2, dev, stream, peaks):
+def measure_rows(fa2, dev, stream, peaks, only=None):
     """Throughput of the widened rows (grouped-query prefill, split-KV decoding,
-    variable-length batch) on synthetic device-generated inputs."""
+    variable-length batch) on synthetic device-generated inputs; `only` picks
+    one of "gqa", "decode", "varlen"."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(2024)
 
@@ -271,41 +272,46 @@ def measure_rows(fa2, dev, stream, peaks):
 
     out = {}
     tf = lambda fl, ms: fl / (ms * 1e-3) / 1e12
+    want = lambda name: only is None or only == name
     # Grouped-query prefill: 32 query heads over 8 K/V heads.
     B, H, Hkv, N, d = 1, 32, 8, 16384, 128
-    q, dO = rnd(B, H, N, d), rnd(B, H, N, d)
-    k, v = rnd(B, Hkv, N, d), rnd(B, Hkv, N, d)
-    o, lse = fa2.fa2_fwd_gqa(q, k, v, causal=True, stream=stream)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    f_ms = _time_ms(lambda: fa2.fa2_fwd_gqa(q, k, v, o=o, lse=lse, causal=True, stream=stream), stream)
-    b_ms = _time_ms(lambda: fa2.fa2_bwd_gqa(q, k, v, o, dO, lse, dq=dq, dk=dk, dv=dv, causal=True, stream=stream),
-                    stream)
-    ff, bf = 2.0 * B * H * N * N * d, 5.0 * B * H * N * N * d
-    out["gqa_prefill"] = {"workload": f"B={B} H={H} H_kv={Hkv} N={N} d={d} causal",
-                          "fwd_ms": f_ms, "fwd_tflops": tf(ff, f_ms), "bwd_ms": b_ms, "bwd_tflops": tf(bf, b_ms),
-                          "fwd_pct_of_peak_burst": 100 * tf(ff, f_ms) / peaks["bf16_tflops"],
-                          "bwd_pct_of_peak_burst": 100 * tf(bf, b_ms) / peaks["bf16_tflops"]}
-    del q, dO, k, v, o, lse, dq, dk, dv
+    if want("gqa"):
+        q, dO = rnd(B, H, N, d), rnd(B, H, N, d)
+        k, v = rnd(B, Hkv, N, d), rnd(B, Hkv, N, d)
+        o, lse = fa2.fa2_fwd_gqa(q, k, v, causal=True, stream=stream)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        f_ms = _time_ms(lambda: fa2.fa2_fwd_gqa(q, k, v, o=o, lse=lse, causal=True, stream=stream), stream)
+        b_ms = _time_ms(lambda: fa2.fa2_bwd_gqa(q, k, v, o, dO, lse, dq=dq, dk=dk, dv=dv, causal=True, stream=stream),
+                        stream)
+        ff, bf = 2.0 * B * H * N * N * d, 5.0 * B * H * N * N * d
+        out["gqa_prefill"] = {"workload": f"B={B} H={H} H_kv={Hkv} N={N} d={d} causal",
+                              "fwd_ms": f_ms, "fwd_tflops": tf(ff, f_ms), "bwd_ms": b_ms, "bwd_tflops": tf(bf, b_ms),
+                              "fwd_pct_of_peak_burst": 100 * tf(ff, f_ms) / peaks["bf16_tflops"],
+                              "bwd_pct_of_peak_burst": 100 * tf(bf, b_ms) / peaks["bf16_tflops"]}
+        del q, dO, k, v, o, lse, dq, dk, dv
     # Split-KV decoding: one query per sequence against a 16K key-value cache.
     B, H, Hkv, Nq, Nk, d, splits = 8, 32, 8, 1, 16384, 128, 16
-    q, k, v = rnd(B, H, Nq, d), rnd(B, Hkv, Nk, d), rnd(B, Hkv, Nk, d)
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(1, fa2.load_library().fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, splits)),
-                     dtype=torch.uint8, device=dev)
-    ms = _time_ms(lambda: fa2.fa2_fwd_splitkv(q, k, v, splits, o=o, lse=lse, workspace=ws, causal=True,
-                                              stream=stream), stream, iters=50)
-    nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    out["decode_splitkv"] = {"workload": f"B={B} H={H} H_kv={Hkv} Nq={Nq} Nk={Nk} d={d} causal, {splits} splits",
-                             "ms": ms, "algorithmic_bytes": nbytes,
-                             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                          "frac": gbs / peaks["hbm_gbs"]},
-                             "note": "K and V read once per K/V head (query heads of a group share the tile); "
-                                     "launches: split kernel + combine kernel"}
-    del q, k, v, o, lse, ws
+    if want("decode"):
+        q, k, v = rnd(B, H, Nq, d), rnd(B, Hkv, Nk, d), rnd(B, Hkv, Nk, d)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(1, fa2.load_library().fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, splits)),
+                         dtype=torch.uint8, device=dev)
+        ms = _time_ms(lambda: fa2.fa2_fwd_splitkv(q, k, v, splits, o=o, lse=lse, workspace=ws, causal=True,
+                                                  stream=stream), stream, iters=50)
+        nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["decode_splitkv"] = {"workload": f"B={B} H={H} H_kv={Hkv} Nq={Nq} Nk={Nk} d={d} causal, {splits} splits",
+                                 "ms": ms, "algorithmic_bytes": nbytes,
+                                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                              "frac": gbs / peaks["hbm_gbs"]},
+                                 "note": "K and V read once per K/V head (query heads of a group share the tile); "
+                                         "launches: split kernel + combine kernel"}
+        del q, k, v, o, lse, ws
     # Variable-length batch: 16 packed sequences of 1..8192 tokens.
     lens = workloads.varlen_lengths(16, 8192, seed=7)
+    if not want("varlen"):
+        return _checked(fa2, out)
     H, d = 32, 128
     T = sum(lens)
     q, k, v, dO = rnd(T, H, d), rnd(T, H, d), rnd(T, H, d), rnd(T, H, d)
@@ -324,6 +330,10 @@ def measure_rows(fa2, dev, stream, peaks):
                      "fwd_ms": f_ms, "fwd_tflops": tf(ff, f_ms), "bwd_ms": b_ms, "bwd_tflops": tf(bf, b_ms),
                      "fwd_pct_of_peak_burst": 100 * tf(ff, f_ms) / peaks["bf16_tflops"],
                      "bwd_pct_of_peak_burst": 100 * tf(bf, b_ms) / peaks["bf16_tflops"]}
+    return _checked(fa2, out)
+
+
+def _checked(fa2, out):
     torch.cuda.synchronize()
     if fa2.fa2_device_status(reset=True) != 0:
         raise RuntimeError("a kernel reported a device status during the row measurements")
@@ -473,6 +483,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the GQA / decoding / varlen measurements")
+    ap.add_argument("--row", choices=["gqa", "decode", "varlen"],
+                    help="measure only this widened row and print it (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -480,6 +492,14 @@ def main():
     causal = not args.noncausal
     if args.impl == "reference":
         return run_reference(args, w, causal)
+    if args.row:
+        import tiled_exact_attention_fa2_gb300 as fa2
+        from tiled_exact_attention_fa2_gb300 import _build
+        _build.build()
+        dev = torch.device("cuda:0")
+        stream = torch.cuda.Stream(device=dev)
+        print(json.dumps({"row": args.row, **measure_rows(fa2, dev, stream, _peaks(), only=args.row)}), flush=True)
+        return 0
     return run_gpu(args, w, causal)
 
 

@@ -661,7 +661,10 @@ int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stre
 }
 
 // Merge per-split results: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
-// One warp per row; lane l holds columns [l * D / 32, (l + 1) * D / 32).
+// One warp per row; lane l holds columns [l * D / 32, (l + 1) * D / 32).  The
+// split LSEs are read by the lanes in parallel (lane l: splits l, l + 32, ...)
+// and combined with warp shuffles; the weights are then broadcast one split at
+// a time while every lane accumulates its columns.
 template <int D>
 __global__ void __launch_bounds__(256) fa2_splitkv_combine_kernel(const float* __restrict__ o_part,
                                                                   const float* __restrict__ lse_part,
@@ -675,22 +678,32 @@ __global__ void __launch_bounds__(256) fa2_splitkv_combine_kernel(const float* _
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, lse_part[static_cast<size_t>(s) * rows + row]);
+  for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, lse_part[static_cast<size_t>(s) * rows + row]);
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
   float acc[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
   float total = -INFINITY;
   if (mx != -INFINITY) {
     float sum = 0.f;
-    for (int s = 0; s < splits; ++s) sum += expf(lse_part[static_cast<size_t>(s) * rows + row] - mx);
+    for (int s = lane; s < splits; s += 32) sum += expf(lse_part[static_cast<size_t>(s) * rows + row] - mx);
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
     total = mx + logf(sum);
     const bool active = D >= 32 || lane < D;
-    for (int s = 0; s < splits; ++s) {
-      const float w = expf(lse_part[static_cast<size_t>(s) * rows + row] - total);
-      if (w == 0.f || !active) continue;
-      const float* src = o_part + (static_cast<size_t>(s) * rows + row) * D + lane * kPer;
+    for (int base = 0; base < splits; base += 32) {
+      const int s_l = base + lane;
+      const float w_l = s_l < splits ? expf(lse_part[static_cast<size_t>(s_l) * rows + row] - total) : 0.f;
+      const int n = min(32, splits - base);
+#pragma unroll 4
+      for (int i = 0; i < n; ++i) {
+        const float w = __shfl_sync(0xffffffffu, w_l, i);
+        if (w == 0.f || !active) continue;
+        const float* src = o_part + (static_cast<size_t>(base + i) * rows + row) * D + lane * kPer;
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) acc[k] = fmaf(w, src[k], acc[k]);
+        for (int k = 0; k < kPer; ++k) acc[k] = fmaf(w, src[k], acc[k]);
+      }
     }
   }
   if (D >= 32 || lane < D) {
