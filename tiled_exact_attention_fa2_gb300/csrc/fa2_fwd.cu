@@ -28,8 +28,11 @@
 // touches shared memory.  S_X(j+1) is issued only after P_X(j) V_j has
 // completed, because it overwrites the columns that MMA reads (decoding,
 // where tile B is empty, double-buffers S over both ranges instead).
-// O is rescaled in TMEM only when some row of the warp sees its max grow, so
-// every row's largest weight is exactly 1.  The softmax arithmetic runs on
+// The reference value m that the exponentials subtract is raised only when a
+// tile's row max exceeds it by more than kRescaleSlack (log2 units), so the
+// weights stay below 2^kRescaleSlack and O is rescaled in TMEM (for the whole
+// warp) only on those rare tiles; softmax warps w and w + 4, which share an
+// SMSP, take turns at the exponentials.  The softmax arithmetic runs on
 // packed fp32 pairs (f32x2 FMA/ADD/MUL) and 3-input max to halve its
 // instruction count.
 #include <cuda.h>
@@ -50,6 +53,10 @@ constexpr int kFwdThreads = 352;
 // the eight softmax warps.
 constexpr int kSchedReaders = 11;
 constexpr uint32_t kTmemCols = 512;
+// A row's reference max is raised only when a tile's max exceeds it by more
+// than this (log2 units): weights 2^(s - m) then stay below 2^8, well inside
+// bf16 and fp32 range, and the result is the same softmax up to rounding.
+constexpr float kRescaleSlack = 8.f;
 
 enum FwdBar {
   kBarQFull = 0,    // +tile (A, B)
@@ -64,7 +71,9 @@ enum FwdBar {
   kBarQEmpty = 18,      // +tile: the tile's issuer is done with its Q tile of a unit
   kBarSchedFull = 20,   // +slot (2): scheduler response landed (16 transaction bytes)
   kBarSchedEmpty = 22,  // +slot: every role has read the response (kSchedReaders arrivals)
-  kNumFwdBars = 24,
+  kBarTokA = 24,        // +SMSP slot (4): softmax warp of tile A may start its exponentials
+  kBarTokB = 28,        // +SMSP slot (4): softmax warp of tile B may start its exponentials
+  kNumFwdBars = 32,
 };
 
 template <int D>
@@ -233,6 +242,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars[kBarPFull + s], 4);
       mbar_init(&bars[kBarPVDone + s], 1);
       mbar_init(&bars[kBarDrain + s], 1);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars[kBarTokA + s], 1);
+      mbar_init(&bars[kBarTokB + s], 1);
     }
     fence_mbar_init();
   }
@@ -416,6 +429,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll 1
         for (int j = nx; j < n_kv; ++j) {
           const int gj = g + j, st = gj & 1;
+          // Take the tile's full phases too, so that this issuer's next wait
+          // on the stage is never two phases ahead of the loads.
+          if (!(ok = mbar_wait(&bars[kBarKFull + st], (gj >> 1) & 1, status) &&
+                     mbar_wait(&bars[kBarVFull + st], (gj >> 1) & 1, status)))
+            break;
           if (gj >= 2 && !(ok = mbar_wait(&bars[kBarKEmpty + st], ((gj >> 1) - 1) & 1, status))) break;
           mbar_arrive(&bars[kBarKEmpty + st]);
           if (gj >= 2 && !(ok = mbar_wait(&bars[kBarVEmpty + st], ((gj >> 1) - 1) & 1, status))) break;
@@ -441,6 +459,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     auto sbuf = [&](int kk) { return dual ? (kk & 1) : x; };
     auto sphase = [&](int kk) { return dual ? (kk >> 1) & 1 : kk & 1; };
     int k = 0;  // S_x tiles consumed so far
+    // Softmax warps w (tile A) and w + 4 (tile B) share an SMSP and take
+    // turns at the exponentials, so that the two never contend for its MUFU
+    // and issue slots: per unit, turn j of tile A, then turn j of tile B,
+    // for every K/V tile j of the unit (a tile the warp does not visit is a
+    // turn it passes on at once).  Tile A's turn t waits for B's turn t - 1;
+    // B's turn t waits for A's turn t.  Each waiter is exactly one phase
+    // behind the token barrier it waits on.
+    int tn = 0;  // turns this warp has taken
+    uint64_t* tok_wait = &bars[(x ? kBarTokB : kBarTokA) + (warp & 3)];
+    uint64_t* tok_pass = &bars[(x ? kBarTokA : kBarTokB) + (warp & 3)];
+    auto take_turn = [&]() -> bool {
+      const int t = x ? tn : tn - 1;
+      return t < 0 || mbar_wait(tok_wait, t & 1, status);
+    };
+    auto pass_turn = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tok_pass);
+      ++tn;
+    };
     bool ok = true;
 #pragma unroll 1
     for (int n = 0, u = static_cast<int>(blockIdx.x); ok && u >= 0; ++n) {
@@ -448,12 +485,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const FwdUnit w = fwd_unit<CAUSAL, MODE>(p, u, num_row_tiles, num_pairs, status);
       if (!w.valid) break;
       const int nx = x ? w.cnt[1] : w.cnt[0];  // (selects keep the struct in registers)
+      // Turns are taken only in units where both tiles have K/V tiles.
+      const int turns = (!dual && w.cnt[0] > 0 && w.cnt[1] > 0) ? max(w.cnt[0], w.cnt[1]) : 0;
       const int q_row = w.q0 + x * kTileRows + r;              // row in the row-head
       const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
       const int imin_x = x ? w.imin[1] : w.imin[0];
       const int off = w.off, Nk = w.Nk;
-      float m = -INFINITY;  // running row max, log2 units (scores * scale * log2 e)
-      float l = 0.f;        // running sum of 2^(x - m)
+      float m = -INFINITY;  // reference max, log2 units (scores * scale * log2 e); row max - m <= slack
+      float l = 0.f;        // running sum of 2^(x - m) (fp32 weights: the LSE)
+      float lo = 0.f;       // the same with each tile's largest weight as bf16 (normalises O)
 #pragma unroll 1
       for (int j = 0; j < nx; ++j, ++k) {
         // Without dual buffering S_x(j) was issued after O_x += P_x(j-1)
@@ -487,10 +527,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mx8[c] = fmaxf(v, s[c + 120]);
         }
         const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-        const float m_new = fmaxf(m, mx * scale_log2);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const bool grow = m_use > m;  // always true on the first tile
+        // Raise m to this tile's max only when that exceeds it by more than
+        // the slack (always on the first tile that sees a key).
+        const float mt = mx * scale_log2;
+        const bool grow = mt > m + kRescaleSlack;
+        const float m_new = grow ? mt : m;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // (no key seen yet)
         const float alpha = ex2_approx(m - m_use);
+        // The tile's largest weight (computed exactly as the loop below does)
+        // and its bf16 rounding error.  With the reference max lagging the
+        // row max, that weight is not a power of two, and the PV MMA sees it
+        // rounded to bf16; normalising O by a sum that carries the same
+        // rounding keeps O the weighted mean of V that the MMA computed.
+        const float pmax = ex2_approx(fmaf(mx, scale_log2, -m_use));
+        const float dpmax = unpack_bf16x2(pack_bf16x2(pmax, 0.f)).x - pmax;
+        if (j < turns && !(ok = take_turn())) break;
 
         // P = 2^(s * scale_log2 - m) on packed pairs; 4 independent pair sums.
         const uint64_t negm2 = f2_pack(-m_use, -m_use);
@@ -512,6 +563,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         const float2 a01 = f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])));
         const float rs = a01.x + a01.y;
+        if (j < turns) pass_turn();
 
         if (j >= 1 && __any_sync(0xffffffffu, grow)) {
           if (dual) {
@@ -547,7 +599,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarPFull + b]);
         l = l * alpha + rs;
-        m = m_use;
+        lo = lo * alpha + (rs + dpmax);
+        m = m_new;
+      }
+      if (!ok) break;
+      // Turns of the K/V tiles this warp does not visit.
+#pragma unroll 1
+      for (int j = nx; j < turns; ++j) {
+        if (!(ok = take_turn())) break;
+        pass_turn();
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -587,7 +647,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // race it.
       if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = lo > 0.f ? 1.f / lo : 0.f;
       constexpr int kC = D >= 32 ? 32 : 16;
 #pragma unroll
       for (int c = 0; c < D / kC; ++c) {
