@@ -75,6 +75,31 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int, qk_mult: float = 1.0,
     return out
 
 
+def make_profile_inputs(B: int, H: int, N: int, d: int, profile: str, strength: float, seed: int):
+    """make_inputs with K reshaped so that the largest scores of a query row
+    come late in the key sequence (CPU bf16 tensors, with dO).
+
+    'ramp'  scales key row j by 1 + strength * j / N, so score magnitudes, and
+            with them each row's running maximum, grow along the keys;
+    'spike' replaces key row i - 3 by strength * (query row i) for every
+            eighth query row i >= 8, which gives row i one very large score
+            just before its own position (a causal row sees it).
+    """
+    x = make_inputs(B, H, N, d, seed)
+    k = x["k"].float()
+    if profile == "ramp":
+        ramp = 1.0 + strength * torch.arange(N, dtype=torch.float32) / N
+        k = k * ramp[None, None, :, None]
+    elif profile == "spike":
+        q = x["q"].float()
+        for i in range(8, N, 8):
+            k[:, :, i - 3] = strength * q[:, :, i]
+    else:
+        raise ValueError(profile)
+    x["k"] = k.to(torch.bfloat16).contiguous()
+    return x
+
+
 def workload_inputs(w: Workload, with_grad: bool = True):
     return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, with_grad)
 
