@@ -539,35 +539,43 @@ __global__ void __launch_bounds__(512, 1)
       const int bh = bh_kv * group + it / n_q;
       if (!(ok = mbar_wait_sleep(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
-      // Pieces are read from TMEM two at a time (64 registers); the columns
-      // are released right after the last read, before the staging of the
-      // last two pieces can wait on earlier reduces.
-      float g[2][C::kChunk];
+      // The first three pieces are read from TMEM at once (96 registers),
+      // the fourth as soon as the first is staged, and the columns are
+      // released right after that read: dP^T(i+1) reuses them, so only one
+      // piece's staging lies between dQ landing and the release.
+      constexpr int kFirst = C::kChunks < 3 ? C::kChunks : 3;
+      float g[3][C::kChunk];
+#pragma unroll
+      for (int k = 0; k < kFirst; ++k) {
+        if constexpr (C::kChunk == 32)
+          tmem_ld32(tmem + lane_base + C::kColDQ + k * 32, g[k]);
+        else
+          tmem_ld16(tmem + lane_base + C::kColDQ, g[k]);
+      }
+      tmem_wait_ld();
+      if (C::kChunks == kFirst) {  // every dQ column has been read: release the TMEM columns
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+      }
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
         const int gi = it * C::kChunks + c, bsel = gi & 1, u = gi >> 1;
-        if ((c & 1) == 0) {
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            if (c + k < C::kChunks) {
-              if constexpr (C::kChunk == 32)
-                tmem_ld32(tmem + lane_base + C::kColDQ + (c + k) * 32, g[k]);
-              else
-                tmem_ld16(tmem + lane_base + C::kColDQ, g[k]);
-            }
-          }
-          tmem_wait_ld();
-          if (c + 2 >= C::kChunks) {  // every dQ column has been read: release the TMEM columns
+        if constexpr (C::kChunks == 4) {
+          if (c == 1) {  // piece 3 into piece 0's registers, then release
+            tmem_ld32(tmem + lane_base + C::kColDQ + 3 * 32, g[0]);
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
           }
         }
+        const int slot = c == 3 ? 0 : c;
         if (gi >= 2 && !(ok = mbar_wait_sleep(&bars[kBarStageFree + bsel], (u - 1) & 1, status))) break;
         const uint32_t sb = sStage + bsel * C::kStageBytes;
 #pragma unroll
         for (int j = 0; j < C::kChunk / 4; ++j) {
-          const float* v4 = g[c & 1] + 4 * j;
+          const float* v4 = g[slot] + 4 * j;
           st_shared_v4(sb + swizzle_offset<C::kChunk * 4>(t, j), __float_as_uint(v4[0]), __float_as_uint(v4[1]),
                        __float_as_uint(v4[2]), __float_as_uint(v4[3]));
         }
