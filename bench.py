@@ -44,11 +44,11 @@ METRIC = "causal bf16 FA2 fwd / bwd TFLOPS and % of GB300 dense bf16 peak (1 GPU
 # the current kernel exists.  The profile summary under profiles/ names the
 # command that produced the figure.
 DOMINANT_KERNEL_TRAFFIC = {
-    # profiles/dram_traffic_long_causal.md: dram__bytes_read.sum 809.68 MB +
-    # dram__bytes_write.sum 485.76 MB for one fa2_bwd_kernel<128, causal> launch.
-    ("fa2_bwd_kernel", "long", True): 809.68e6 + 485.76e6,
-    # same capture: 406.67 MB + 115.54 MB for one fa2_fwd_kernel<128, causal> launch.
-    ("fa2_fwd_kernel", "long", True): 406.67e6 + 115.54e6,
+    # profiles/dram_traffic_long_causal.md: dram__bytes_read.sum 810.72 MB +
+    # dram__bytes_write.sum 486.32 MB for one fa2_bwd_kernel<128, causal> launch.
+    ("fa2_bwd_kernel", "long", True): 810.72e6 + 486.32e6,
+    # same capture: 406.53 MB + 115.63 MB for one fa2_fwd_kernel<128, causal> launch.
+    ("fa2_fwd_kernel", "long", True): 406.53e6 + 115.63e6,
 }
 
 
