@@ -1,0 +1,136 @@
+"""CPU model of the backward main kernel's mbarrier protocol (no GPU).
+
+`fa2_bwd_kernel` runs a TMA producer, one MMA issuer, two P/dS warpgroups
+and a dQ drain warpgroup (whose first lane also issues the TMA reduces)
+over the query tiles of one key/value tile.  This model replays each
+role's waits, arrivals, loads, MMA commits and bulk reduces with the
+kernel's barrier counts (BwdBar enum) and stage counts (two Q stages, one
+or two dO stages, dQ in 1, 2 or 4 pieces of at most 32 columns), lets loads
+land and reduces finish reading in any order, and checks that no wait is
+two phases away from its barrier and that every run ends
+(`protocol_model.Engine`).
+"""
+import random
+
+import pytest
+
+from protocol_model import Engine
+
+SQ = 2  # Q stages
+
+
+def backward_roles(e, n_iter, sd, pieces, early_release=False):
+    e.bar("KV", 1)
+    for s in range(2):
+        for name in ("QFull", "QEmpty", "DoFull", "DoEmpty"):
+            e.bar((name, s), 1, f"{name}[{s}]")
+        e.bar(("StageFull", s), 4, f"StageFull[{s}]")
+        e.bar(("StageFree", s), 1, f"StageFree[{s}]")
+    for name, count in (("SFull", 1), ("DpFull", 1), ("PFull", 8), ("DvDone", 1), ("DsFull", 8), ("DsEmpty", 1),
+                        ("DqFull", 1), ("DqDrained", 4), ("AccFull", 1), ("Drain", 1)):
+        e.bar(name, count)
+
+    def load(key):
+        e.unordered(lambda: e.arrive(key))
+
+    def commit(*keys):
+        for key in keys:
+            e.ordered("mma", lambda key=key: e.arrive(key))
+
+    def producer():
+        load("KV")
+        for it in range(n_iter):
+            st, u = it % SQ, it // SQ
+            if it >= SQ:
+                yield ("QEmpty", st), u - 1
+            load(("QFull", st))
+            st, u = it % sd, it // sd
+            if it >= sd:
+                yield ("DoEmpty", st), u - 1
+            load(("DoFull", st))
+
+    def issuer():
+        yield "KV", 0
+        yield ("QFull", 0), 0
+        commit("SFull")
+        for it in range(n_iter):
+            qs, ds, du = it % SQ, it % sd, it // sd
+            yield ("DoFull", ds), du
+            if it >= 1:
+                yield "DqDrained", it - 1
+            commit("DpFull")
+            yield "PFull", it
+            commit(("DoEmpty", ds), "DvDone")
+            if it + 1 < n_iter:
+                yield "DvDone", it
+                yield ("QFull", (it + 1) % SQ), (it + 1) // SQ
+                commit("SFull")
+            yield "DsFull", it
+            commit("DqFull", ("QEmpty", qs), "DsEmpty")
+        commit("AccFull", "Drain")
+        yield "Drain", 0
+
+    def p_ds():
+        for it in range(n_iter):
+            yield ("QFull", it % SQ), it // SQ
+            yield "SFull", it
+            e.arrive("PFull")
+            yield "DpFull", it
+            if it >= 1:
+                yield "DsEmpty", it - 1
+            e.arrive("DsFull")
+
+    read_done, issued = set(), []
+
+    def drain(w):
+        for it in range(n_iter):
+            yield "DqFull", it
+            if pieces <= 3 or early_release:
+                e.arrive("DqDrained")
+            for c in range(pieces):
+                if pieces == 4 and c == 1:
+                    e.arrive("DqDrained")
+                gi = it * pieces + c
+                bsel, u = gi & 1, gi >> 1
+                if gi >= 2:
+                    yield ("StageFree", bsel), u - 1
+                e.arrive(("StageFull", bsel))
+                if w == 0:  # lane 0 of the first drain warp issues the reduce
+                    yield ("StageFull", bsel), u
+                    issued.append(gi)
+                    e.unordered(lambda gi=gi: read_done.add(gi))
+                    if gi >= 1:
+                        older = list(issued[:-1])
+                        yield ("cond", lambda older=older: all(g in read_done for g in older),
+                               "bulk reads of the older reduces")
+                        e.arrive(("StageFree", bsel ^ 1))
+        yield "AccFull", 0
+
+    roles = {"producer": producer(), "issuer": issuer()}
+    for w in range(8):
+        roles[f"P/dS {w}"] = p_ds()
+    for w in range(4):
+        roles[f"drain {w}"] = drain(w)
+    return roles
+
+
+@pytest.mark.parametrize("sd,pieces", [(1, 4), (2, 2), (2, 1)], ids=["d128", "d64", "d32_d16"])
+def test_backward_protocol_has_no_deadlock_or_parity_aliasing(sd, pieces):
+    for seed in range(300):
+        n_iter = random.Random(seed).randint(1, 12)
+        e = Engine(seed)
+        result = e.run(backward_roles(e, n_iter, sd, pieces))
+        assert result is None, f"seed {seed}, {n_iter} query tiles: {result}"
+
+
+def test_model_catches_a_second_release_of_the_dq_columns():
+    # A drain that also released the dQ columns right after its first read
+    # (as well as after the fourth piece) would run the barrier two phases
+    # past the MMA issuer's wait.
+    found = None
+    for seed in range(300):
+        e = Engine(seed)
+        found = e.run(backward_roles(e, random.Random(seed).randint(2, 12), 1, 4, early_release=True))
+        if found:
+            break
+    assert found and "DqDrained" in found

@@ -1,72 +1,46 @@
 """CPU model of the forward kernel's mbarrier protocol (no GPU).
 
 `fa2_fwd_kernel` coordinates its roles (TMA producer, two MMA issuers, two
-groups of four softmax warps) through mbarriers that are waited on by
-phase parity.  A parity wait cannot tell phase t from phase t + 2 or t - 2:
-a waiter that falls two phases behind a barrier blocks forever, and one
-that runs a phase ahead of it passes on the parity of an older phase.  This
-model replays the kernel's sequence of waits and arrivals for each role as
-a coroutine, lets TMA loads land and MMA groups complete at random times
-(loads in any order, MMAs of one issuer in order), and checks on every
-wait that the barrier is at most one phase away, and that the whole run
-ends (no deadlock).  Barrier names and counts follow the kernel's FwdBar
-enum; units are (K/V tiles of tile A, K/V tiles of tile B) pairs as
-`fwd_unit` produces them.  The scheduler barriers (one response per unit,
-read by all eleven roles) are part of the model.
+groups of four softmax warps) through mbarriers waited on by phase parity.
+This model replays each role's sequence of waits, arrivals, TMA loads and
+MMA commits (`protocol_model.Engine`: loads land in any order, one issuer's
+commits in issue order) and checks that no wait is ever two phases away
+from its barrier and that every run ends.  Barrier names and counts follow
+the kernel's FwdBar enum; a unit is the pair (K/V tiles of query tile A,
+K/V tiles of query tile B) that `fwd_unit` computes.  The scheduler
+barriers (one response per unit, read by all eleven roles) are included.
 """
 import random
 
 import pytest
 
-
-class Bar:
-    def __init__(self, name, count):
-        self.name, self.count, self.pending, self.done = name, count, 0, 0
-
-    def arrive(self):
-        self.pending += 1
-        assert self.pending <= self.count
-        if self.pending == self.count:
-            self.pending, self.done = 0, self.done + 1
+from protocol_model import Engine
 
 
-class Model:
-    def __init__(self, units, seed, skip_full_waits=True, turns=True):
-        self.units, self.rng = units, random.Random(seed)
-        self.skip_full_waits, self.turns = skip_full_waits, turns
-        self.bars = {}
-        for s in range(2):
-            for name, count in (("QFull", 1), ("QEmpty", 1), ("KFull", 1), ("KEmpty", 2), ("VFull", 1),
-                                ("VEmpty", 2), ("SFull", 1), ("PFull", 4), ("PVDone", 1), ("SchedFull", 1),
-                                ("SchedEmpty", 11)):
-                self.bars[(name, s)] = Bar(f"{name}[{s}]", count)
-        for w in range(4):
-            self.bars[("TokA", w)] = Bar(f"TokA[{w}]", 1)
-            self.bars[("TokB", w)] = Bar(f"TokB[{w}]", 1)
-        self.mma = {0: [], 1: []}  # per issuer: commits in issue order
-        self.loads = []            # TMA loads in flight (land in any order)
-        self.error = None
+def forward_roles(e, units, skip_full_waits=True, turns=True):
+    for s in range(2):
+        for name, count in (("QFull", 1), ("QEmpty", 1), ("KFull", 1), ("KEmpty", 2), ("VFull", 1),
+                            ("VEmpty", 2), ("SFull", 1), ("PFull", 4), ("PVDone", 1), ("SchedFull", 1),
+                            ("SchedEmpty", 11)):
+            e.bar((name, s), count, f"{name}[{s}]")
+    for w in range(4):
+        e.bar(("TokA", w), 1, f"TokA[{w}]")
+        e.bar(("TokB", w), 1, f"TokB[{w}]")
 
-    def ready(self, key, t):
-        """Wait for completion number t (0-based) of a barrier, with parity semantics checked."""
-        b = self.bars[key]
-        if b.done >= t + 2:
-            self.error = f"{b.name}: waiter two phases behind (done {b.done}, waits #{t})"
-        elif b.done <= t - 1 and (t - b.done) % 2 == 1:
-            self.error = f"{b.name}: parity wait passes early (done {b.done}, waits #{t})"
-        return b.done >= t + 1
+    def load(key):
+        e.unordered(lambda: e.arrive(key))
 
-    def arrive(self, key):
-        self.bars[key].arrive()
+    def commit(x, *keys):
+        for key in keys:
+            e.ordered(("mma", x), lambda key=key: e.arrive(key))
 
-    # ---------------------------------------------------------------- roles
-    def producer(self):
+    def producer():
         g, qn = 0, [0, 0]
-        for n, (na, nb) in enumerate(self.units):
+        for n, (na, nb) in enumerate(units):
             def load_q(x):
                 if qn[x] >= 1:
                     yield ("QEmpty", x), qn[x] - 1
-                self.loads.append(("QFull", x))
+                load(("QFull", x))
                 qn[x] += 1
 
             if na > 0:
@@ -75,22 +49,22 @@ class Model:
                 st = g & 1
                 if g >= 2:
                     yield ("KEmpty", st), (g >> 1) - 1
-                self.loads.append(("KFull", st))
+                load(("KFull", st))
                 if g >= 2:
                     yield ("VEmpty", st), (g >> 1) - 1
-                self.loads.append(("VFull", st))
+                load(("VFull", st))
                 if j == 0 and nb > 0:
                     yield from load_q(1)
                 g += 1
             if n >= 2:
                 yield ("SchedEmpty", n & 1), (n >> 1) - 1
-            self.loads.append(("SchedFull", n & 1))
+            load(("SchedFull", n & 1))
             yield ("SchedFull", n & 1), n >> 1
-            self.arrive(("SchedEmpty", n & 1))
+            e.arrive(("SchedEmpty", n & 1))
 
-    def issuer(self, x):
+    def issuer(x):
         g = k = qn = 0
-        for n, cnt in enumerate(self.units):
+        for n, cnt in enumerate(units):
             n_kv, nx = max(cnt), cnt[x]
             if n_kv > 0:
                 if nx > 0:
@@ -99,94 +73,62 @@ class Model:
                     if k >= 1:
                         yield ("PVDone", x), k - 1
                     yield ("KFull", g & 1), g >> 1
-                    self.mma[x] += [("SFull", x), ("KEmpty", g & 1)] + ([("QEmpty", x)] if nx == 1 else [])
+                    commit(x, ("SFull", x), ("KEmpty", g & 1), *([("QEmpty", x)] if nx == 1 else []))
                 for j in range(nx):
                     gj = g + j
                     st = gj & 1
                     yield ("VFull", st), gj >> 1
                     yield ("PFull", x), k
-                    self.mma[x] += [("PVDone", x), ("VEmpty", st)]
+                    commit(x, ("PVDone", x), ("VEmpty", st))
                     k += 1
                     if j + 1 < nx:
                         yield ("PVDone", x), k - 1
                         yield ("KFull", st ^ 1), (gj + 1) >> 1
-                        self.mma[x] += [("SFull", x), ("KEmpty", st ^ 1)] + ([("QEmpty", x)] if j + 2 == nx else [])
-                for j in range(nx, n_kv):  # tiles this issuer does not visit
+                        commit(x, ("SFull", x), ("KEmpty", st ^ 1), *([("QEmpty", x)] if j + 2 == nx else []))
+                for j in range(nx, n_kv):  # K/V tiles this issuer does not visit
                     gj = g + j
                     st = gj & 1
-                    if self.skip_full_waits:
+                    if skip_full_waits:
                         yield ("KFull", st), gj >> 1
                         yield ("VFull", st), gj >> 1
                     if gj >= 2:
                         yield ("KEmpty", st), (gj >> 1) - 1
-                    self.arrive(("KEmpty", st))
+                    e.arrive(("KEmpty", st))
                     if gj >= 2:
                         yield ("VEmpty", st), (gj >> 1) - 1
-                    self.arrive(("VEmpty", st))
+                    e.arrive(("VEmpty", st))
                 g += n_kv
             yield ("SchedFull", n & 1), n >> 1
-            self.arrive(("SchedEmpty", n & 1))
+            e.arrive(("SchedEmpty", n & 1))
 
-    def softmax(self, x, w):
+    def softmax(x, w):
         k = tn = 0
         tok_wait, tok_pass = (("TokB", w), ("TokA", w)) if x else (("TokA", w), ("TokB", w))
-        for n, cnt in enumerate(self.units):
+        for n, cnt in enumerate(units):
             nx = cnt[x]
-            turns = max(cnt) if (self.turns and min(cnt) > 0) else 0
-            for j in range(max(nx, turns)):
+            n_turns = max(cnt) if (turns and min(cnt) > 0) else 0
+            for j in range(max(nx, n_turns)):
                 if j < nx:
                     yield ("SFull", x), k
-                if j < turns:
+                if j < n_turns:
                     t = tn if x else tn - 1
                     if t >= 0:
                         yield tok_wait, t
-                    self.arrive(tok_pass)
+                    e.arrive(tok_pass)
                     tn += 1
                 if j < nx:
-                    self.arrive(("PFull", x))
+                    e.arrive(("PFull", x))
                     k += 1
             if nx > 0:
                 yield ("PVDone", x), k - 1
             yield ("SchedFull", n & 1), n >> 1
-            self.arrive(("SchedEmpty", n & 1))
+            e.arrive(("SchedEmpty", n & 1))
 
-    # ---------------------------------------------------------------- run
-    def run(self, max_steps=500000):
-        roles = {"producer": self.producer(), "issuer A": self.issuer(0), "issuer B": self.issuer(1)}
-        for x in range(2):
-            for w in range(4):
-                roles[f"softmax {'AB'[x]}{w}"] = self.softmax(x, w)
-        waiting = dict.fromkeys(roles)
-        for _ in range(max_steps):
-            moves = [("role", r) for r, wt in waiting.items() if wt is None or self.ready(*wt)]
-            moves += [("mma", x) for x in (0, 1) if self.mma[x]]
-            moves += [("load", None)] if self.loads else []
-            if self.error:
-                return self.error
-            if not moves:
-                if not waiting:
-                    return None
-                return "deadlock: " + "; ".join(f"{r} waits {self.bars[wt[0]].name} #{wt[1]}"
-                                                for r, wt in waiting.items() if wt)
-            kind, who = self.rng.choice(moves)
-            if kind == "mma":
-                self.arrive(self.mma[who].pop(0))
-            elif kind == "load":
-                self.arrive(self.loads.pop(self.rng.randrange(len(self.loads))))
-            else:
-                waiting[who] = None
-                try:
-                    while True:
-                        wt = next(roles[who])
-                        if not self.ready(*wt):
-                            waiting[who] = wt
-                            break
-                        if self.error:
-                            return self.error
-                except StopIteration:
-                    del waiting[who]
-                    del roles[who]
-        return "step limit"
+    roles = {"producer": producer(), "issuer A": issuer(0), "issuer B": issuer(1)}
+    for x in range(2):
+        for w in range(4):
+            roles[f"softmax {'AB'[x]}{w}"] = softmax(x, w)
+    return roles
 
 
 def _units(rng, kind):
@@ -207,11 +149,16 @@ def _units(rng, kind):
     return out
 
 
+def _run(units, seed, **kw):
+    e = Engine(seed)
+    return e.run(forward_roles(e, units, **kw))
+
+
 @pytest.mark.parametrize("kind", ["causal", "mixed"])
 def test_forward_protocol_has_no_deadlock_or_parity_aliasing(kind):
     for seed in range(400):
         units = _units(random.Random(seed), kind)
-        result = Model(units, seed).run()
+        result = _run(units, seed)
         assert result is None, f"seed {seed}, units {units}: {result}"
 
 
@@ -221,7 +168,7 @@ def test_model_catches_a_release_without_the_full_waits():
     found = None
     for seed in range(3000):
         units = _units(random.Random(seed), "mixed")
-        found = Model(units, seed, skip_full_waits=False).run()
+        found = _run(units, seed, skip_full_waits=False)
         if found:
             break
     assert found and "parity wait passes early" in found
