@@ -17,7 +17,21 @@ import pytest
 from protocol_model import Engine
 
 
-def forward_roles(e, units, skip_full_waits=True, turns=True):
+def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0, one_p_full=False):
+    """Roles of one CTA.  ``dual``: decoding (tile B never has rows), where
+    tile A alternates its S / P / PV barriers between the two S buffers and
+    issues S(j+1) before PV(j)."""
+    rng = random.Random(seed + 7)
+
+    def buf(x, k):  # S buffer (and barrier index) of a tile's k-th S, and its use count
+        return (k & 1, k >> 1) if dual else (x, k)
+
+    def p_full(x, k):  # P-full barrier and completion number of a tile's k-th P
+        if one_p_full:  # (one barrier per tile even when S is double-buffered)
+            return ("PFull", x), k
+        b, i = buf(x, k)
+        return ("PFull", b), i
+
     for s in range(2):
         for name, count in (("QFull", 1), ("QEmpty", 1), ("KFull", 1), ("KEmpty", 2), ("VFull", 1),
                             ("VEmpty", 2), ("SFull", 1), ("PFull", 4), ("PVDone", 1), ("SchedFull", 1),
@@ -67,24 +81,38 @@ def forward_roles(e, units, skip_full_waits=True, turns=True):
         for n, cnt in enumerate(units):
             n_kv, nx = max(cnt), cnt[x]
             if n_kv > 0:
+                def s_ready(kk):  # S number kk may overwrite its buffer
+                    prev = kk - 2 if dual else kk - 1
+                    if prev >= 0:
+                        b, i = buf(x, prev)
+                        yield ("PVDone", b), i
+
+                def issue_s(kk, st, last):
+                    b, _ = buf(x, kk)
+                    commit(x, ("SFull", b), ("KEmpty", st), *([("QEmpty", x)] if last else []))
+
                 if nx > 0:
                     yield ("QFull", x), qn
                     qn += 1
-                    if k >= 1:
-                        yield ("PVDone", x), k - 1
+                    yield from s_ready(k)
                     yield ("KFull", g & 1), g >> 1
-                    commit(x, ("SFull", x), ("KEmpty", g & 1), *([("QEmpty", x)] if nx == 1 else []))
+                    issue_s(k, g & 1, nx == 1)
                 for j in range(nx):
                     gj = g + j
                     st = gj & 1
-                    yield ("VFull", st), gj >> 1
-                    yield ("PFull", x), k
-                    commit(x, ("PVDone", x), ("VEmpty", st))
-                    k += 1
-                    if j + 1 < nx:
-                        yield ("PVDone", x), k - 1
+                    if dual and j + 1 < nx:
+                        yield from s_ready(k + 1)
                         yield ("KFull", st ^ 1), (gj + 1) >> 1
-                        commit(x, ("SFull", x), ("KEmpty", st ^ 1), *([("QEmpty", x)] if j + 2 == nx else []))
+                        issue_s(k + 1, st ^ 1, j + 2 == nx)
+                    yield ("VFull", st), gj >> 1
+                    yield p_full(x, k)
+                    b, _ = buf(x, k)
+                    commit(x, ("PVDone", b), ("VEmpty", st))
+                    k += 1
+                    if not dual and j + 1 < nx:
+                        yield from s_ready(k)
+                        yield ("KFull", st ^ 1), (gj + 1) >> 1
+                        issue_s(k, st ^ 1, j + 2 == nx)
                 for j in range(nx, n_kv):  # K/V tiles this issuer does not visit
                     gj = g + j
                     st = gj & 1
@@ -106,10 +134,11 @@ def forward_roles(e, units, skip_full_waits=True, turns=True):
         tok_wait, tok_pass = (("TokB", w), ("TokA", w)) if x else (("TokA", w), ("TokB", w))
         for n, cnt in enumerate(units):
             nx = cnt[x]
-            n_turns = max(cnt) if (turns and min(cnt) > 0) else 0
+            n_turns = max(cnt) if (turns and not dual and min(cnt) > 0) else 0
             for j in range(max(nx, n_turns)):
                 if j < nx:
-                    yield ("SFull", x), k
+                    b, i = buf(x, k)
+                    yield ("SFull", b), i
                 if j < n_turns:
                     t = tn if x else tn - 1
                     if t >= 0:
@@ -117,10 +146,14 @@ def forward_roles(e, units, skip_full_waits=True, turns=True):
                     e.arrive(tok_pass)
                     tn += 1
                 if j < nx:
-                    e.arrive(("PFull", x))
+                    if dual and j >= 1 and rng.random() < 0.5:  # O rescale waits for PV(k - 1)
+                        pb, pi = buf(x, k - 1)
+                        yield ("PVDone", pb), pi
+                    e.arrive(p_full(x, k)[0])
                     k += 1
             if nx > 0:
-                yield ("PVDone", x), k - 1
+                pb, pi = buf(x, k - 1)
+                yield ("PVDone", pb), pi
             yield ("SchedFull", n & 1), n >> 1
             e.arrive(("SchedEmpty", n & 1))
 
@@ -151,7 +184,7 @@ def _units(rng, kind):
 
 def _run(units, seed, **kw):
     e = Engine(seed)
-    return e.run(forward_roles(e, units, **kw))
+    return e.run(forward_roles(e, units, seed=seed, **kw))
 
 
 @pytest.mark.parametrize("kind", ["causal", "mixed"])
@@ -172,3 +205,28 @@ def test_model_catches_a_release_without_the_full_waits():
         if found:
             break
     assert found and "parity wait passes early" in found
+
+
+def test_decode_protocol_has_no_deadlock_or_parity_aliasing():
+    # Decoding: every unit is (K/V tiles of its split, 0).
+    for seed in range(400):
+        rng = random.Random(seed)
+        units = [(rng.randint(1, 9), 0) for _ in range(rng.randint(1, 5))]
+        result = _run(units, seed, dual=True)
+        assert result is None, f"seed {seed}, units {units}: {result}"
+
+
+def test_model_catches_a_single_p_full_barrier_in_decode():
+    # One P-full barrier per tile while S is double-buffered lets a fast
+    # softmax warp arrive for P(j+1) before a slow one has arrived for P(j):
+    # the phase completes with arrivals of two tiles, PV(j) and S(j+2) go
+    # out early, and the slow warp ends up two phases behind.
+    found = None
+    for seed in range(2000):
+        rng = random.Random(seed)
+        units = [(rng.randint(2, 9), 0) for _ in range(rng.randint(1, 3))]
+        e = Engine(seed)
+        found = e.run(forward_roles(e, units, dual=True, seed=seed, one_p_full=True))
+        if found:
+            break
+    assert found and "two phases" in found
