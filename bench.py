@@ -289,11 +289,13 @@ def measure_rows(fa2, dev, stream, peaks, only=None):
                               "fwd_pct_of_peak_burst": 100 * tf(ff, f_ms) / peaks["bf16_tflops"],
                               "bwd_pct_of_peak_burst": 100 * tf(bf, b_ms) / peaks["bf16_tflops"]}
         del q, dO, k, v, o, lse, dq, dk, dv
-    # Split-KV decoding: one query per sequence against a 16K key-value cache.
-    # Two splits (128 CTAs, each streaming 8K keys of K and V) measured best:
-    # 5.7 TB/s against 5.2 (4 splits), 5.0 (16) and 3.0 (64).
-    B, H, Hkv, Nq, Nk, d, splits = 8, 32, 8, 1, 16384, 128, 2
+    # Split-KV decoding: one query per sequence against a 16K key-value cache,
+    # with the library's suggested split count (2 on a 152-SM GB300: 128 CTAs
+    # each streaming 8K keys of K and V, 5.7 TB/s against 5.0 with 16 splits).
+    B, H, Hkv, Nq, Nk, d = 8, 32, 8, 1, 16384, 128
     if want("decode"):
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        splits = max(1, fa2.load_library().fa2_fwd_splitkv_suggest_splits(sms, B, H, Hkv, Nq, Nk))
         q, k, v = rnd(B, H, Nq, d), rnd(B, Hkv, Nk, d), rnd(B, Hkv, Nk, d)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)

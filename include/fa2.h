@@ -116,6 +116,17 @@ int fa2_bwd_gqa_ws(const void* q, const void* k, const void* v, const void* o, c
  * split).  Other rules as fa2_fwd.
  */
 size_t fa2_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+/*
+ * A split count for fa2_fwd_splitkv on a GPU with sm_count SMs: the
+ * smallest that gives at least 0.8 * sm_count work units (a unit is one
+ * 256-row pair of packed query rows of one K/V head, for one key range), at
+ * most one per 128-key tile.  Fewer, longer key ranges stream the cache
+ * more efficiently than many short ones once the SMs are busy (measured on
+ * GB300, 8 sequences x 8 K/V heads x 16K keys: 2 splits 5.7 TB/s, 4: 5.2,
+ * 16: 5.0, 64: 3.0).  Pure arithmetic, no device access.  Returns 0 for
+ * invalid arguments (any size < 1, H not a multiple of H_kv).
+ */
+int fa2_fwd_splitkv_suggest_splits(int sm_count, int B, int H, int H_kv, int Nq, int Nk);
 int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
                     int Nk, int d, float scale, int causal, int num_splits, void* workspace, size_t workspace_bytes,
                     void* stream);

@@ -56,6 +56,27 @@ def test_workspace_bytes(lib):
     assert fa2.fa2_bwd_workspace_bytes(1, 1, 1, 48) == 0
 
 
+def test_splitkv_suggested_splits(lib):
+    f = lib.fa2_fwd_splitkv_suggest_splits
+    # 8 sequences x 8 K/V heads (4 query heads each, one query): 64 units per
+    # key range, so two ranges reach 0.8 x 152 SMs
+    assert f(152, 8, 32, 8, 1, 16384) == 2
+    # one sequence x 8 K/V heads against 128K keys: 8 units per range -> 16
+    assert f(152, 1, 32, 8, 1, 131072) == 16
+    # at most one range per 128-key tile
+    assert f(152, 1, 8, 8, 1, 256) == 2
+    assert f(152, 1, 8, 8, 1, 1) == 1
+    # enough units without splitting
+    assert f(152, 64, 64, 32, 1, 16384) == 1
+    # up to 256 packed rows per K/V head are one pair of 128-row tiles; 300 rows are two
+    assert f(152, 2, 200, 1, 1, 65536) == f(152, 2, 1, 1, 1, 65536) == 61
+    assert f(152, 2, 300, 1, 1, 65536) == 31
+    # invalid arguments
+    for args in ((0, 1, 1, 1, 1, 1), (152, 0, 1, 1, 1, 1), (152, 1, 6, 4, 1, 1), (152, 1, 1, 1, 0, 1),
+                 (152, 1, 1, 1, 1, 0)):
+        assert f(*args) == 0
+
+
 A = 1 << 20  # a fake, 16-byte aligned "device" address; never dereferenced
 
 

@@ -64,3 +64,23 @@ def test_splitkv_rejects_causal_with_more_queries_than_keys():
     kv = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(fa2.FA2Error):
         fa2.fa2_fwd_splitkv(q, kv, kv, 2, causal=True)
+
+
+def test_default_split_count_follows_the_suggestion():
+    # num_splits omitted: the binding asks fa2_fwd_splitkv_suggest_splits for
+    # this GPU's SM count; the result equals an explicit call with that count.
+    B, H, Hkv, Nq, Nk, d = 2, 16, 4, 1, 8192, 128
+    q = workloads.make_inputs(B, H, Nq, d, seed=611, with_grad=False)["q"].to(DEV)
+    kv = workloads.make_inputs(B, Hkv, Nk, d, seed=612, with_grad=False)
+    k, v = kv["k"].to(DEV), kv["v"].to(DEV)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    n = fa2.load_library().fa2_fwd_splitkv_suggest_splits(sms, B, H, Hkv, Nq, Nk)
+    assert n >= 1
+    o1, l1 = fa2.fa2_fwd_splitkv(q, k, v, causal=True)
+    o2, l2 = fa2.fa2_fwd_splitkv(q, k, v, n, causal=True)
+    torch.cuda.synchronize()
+    assert fa2.fa2_device_status(reset=True) == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ref_o, ref_l = oracle.attn_fwd_general(q.cpu(), kv["k"], kv["v"], 1.0 / np.sqrt(d), True)
+    check_o(to_np(o1), ref_o)
+    check_lse(to_np(l1), ref_l)

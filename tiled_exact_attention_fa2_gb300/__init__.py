@@ -54,6 +54,7 @@ _SIGNATURES = {
                             _vp]),
     "fa2_check_wait_timeout": (_i, [_i, ctypes.POINTER(_i)]),
     "fa2_fwd_splitkv_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "fa2_fwd_splitkv_suggest_splits": (_i, [_i, _i, _i, _i, _i, _i]),
     "fa2_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
     "fa2_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_varlen_workspace_bytes": (_sz, [_i, _i, _i]),
@@ -243,17 +244,21 @@ def fa2_bwd_gqa(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optional[
     return dq, dk, dv
 
 
-def fa2_fwd_splitkv(q, k, v, num_splits: int, o=None, lse=None, workspace=None, scale: Optional[float] = None,
-                    causal: bool = True, stream=None):
+def fa2_fwd_splitkv(q, k, v, num_splits: Optional[int] = None, o=None, lse=None, workspace=None,
+                    scale: Optional[float] = None, causal: bool = True, stream=None):
     """Split-KV forward for Nq <= Nk (decoding): q [B,H,Nq,d], k/v [B,H_kv,Nk,d].
 
-    Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32).  ``workspace`` (a CUDA
+    Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32).  ``num_splits`` defaults
+    to fa2_fwd_splitkv_suggest_splits for q's device.  ``workspace`` (a CUDA
     byte tensor) is allocated here when not given."""
     lib = load_library()
     B, H, Nq, d = _shape(q, "q")
     Bk, Hkv, Nk, dk_ = _shape(k, "k")
     if (Bk, dk_) != (B, d) or _shape(v, "v") != (B, Hkv, Nk, d):
         raise ValueError("k and v must be [B, H_kv, Nk, d] with q's B and d")
+    if num_splits is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        num_splits = max(1, lib.fa2_fwd_splitkv_suggest_splits(sms, B, H, Hkv, Nq, Nk))
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
     need = lib.fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)

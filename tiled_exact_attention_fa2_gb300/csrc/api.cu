@@ -271,6 +271,16 @@ int check_splitkv_sizes(int B, int H, int H_kv, int Nq, int Nk, int d, int causa
 
 extern "C" {
 
+int fa2_fwd_splitkv_suggest_splits(int sm_count, int B, int H, int H_kv, int Nq, int Nk) {
+  if (sm_count < 1 || B < 1 || H < 1 || H_kv < 1 || Nq < 1 || Nk < 1 || H % H_kv != 0) return 0;
+  const long long rows = static_cast<long long>(H / H_kv) * Nq;  // packed rows per K/V head
+  const long long pairs = ((rows + kRowsPerTile - 1) / kRowsPerTile + 1) / 2;
+  const long long units = static_cast<long long>(B) * H_kv * pairs;  // work units per key range
+  const long long tiles = (static_cast<long long>(Nk) + kRowsPerTile - 1) / kRowsPerTile;
+  const long long want = (4LL * sm_count + 5 * units - 1) / (5 * units);  // ceil(0.8 * sm_count / units)
+  return static_cast<int>(want < 1 ? 1 : (want > tiles ? tiles : want));
+}
+
 size_t fa2_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_splits < 1) return 0;
   if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
