@@ -466,14 +466,12 @@ __global__ void __launch_bounds__(512, 1)
       // columns (the other warpgroup may still be reading its half): the 64
       // weights of columns [64 hh, 64 hh + 64) land in TMEM columns
       // [64 hh, 64 hh + 32), 16 per 32 scores, over S columns already read.
-      float svv[2][32];
-      tmem_ld32(tmem + lane_base + C::kColS + 64 * hh, svv[0]);
-      tmem_ld32(tmem + lane_base + C::kColS + 64 * hh + 32, svv[1]);
-      tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int col0 = 64 * hh + 32 * c;
-        const float* sv = svv[c];
+        float sv[32];
+        tmem_ld32(tmem + lane_base + C::kColS + col0, sv);
+        tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = col0 + e;
