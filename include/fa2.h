@@ -209,17 +209,21 @@ int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d
  * exists for callers that may not allocate device memory themselves (a host
  * framework whose allocator owns all GPU memory, a plugin handed fixed
  * buffers, a latency-critical loop that cannot risk an allocation).  Same
- * arguments, results and errors as fa2_bwd; the backward scratch (D and the
- * fp32 dQ accumulator) lives in one statically allocated device array of
- * fa2_noalloc_scratch_capacity() bytes (64 MiB) that every GPU loading this
- * library holds until the process exits.  Problems needing more scratch than
- * that (fa2_bwd_workspace_bytes) return FA2_ERR_SCRATCH_CAPACITY before
- * anything is enqueued.  The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress, once per device, with that device
- * current), so make that first call before any stream capture.  Every call
- * shares the array: calls whose GPU work overlaps in time on one device race
- * and give wrong results.  Each call zeroes what must start at zero, so
- * nothing carries over between calls.
+ * arguments, results and errors as fa2_bwd, checked in the same order
+ * (pointers, sizes, scale, alignment, overlaps) before anything else; the
+ * backward scratch (D and the fp32 dQ accumulator) lives in one statically
+ * allocated device array of fa2_noalloc_scratch_capacity() bytes (64 MiB)
+ * that every GPU loading this library holds until the process exits.  Valid
+ * problems needing more scratch than that (fa2_bwd_workspace_bytes) return
+ * FA2_ERR_SCRATCH_CAPACITY before anything is enqueued.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current), so make that first call before any stream capture.
+ * The address belongs to the device's CUDA context: after cudaDeviceReset
+ * (or under another context) the next call sees the context change and
+ * looks the address up again, so that call too should come before any
+ * capture.  Every call shares the array: calls whose GPU work overlaps in
+ * time on one device race and give wrong results.  Each call zeroes what
+ * must start at zero, so nothing carries over between calls.
  */
 int fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                     void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,

@@ -25,3 +25,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print the worst error / bound of every parity check that ran."""
+    try:
+        import parity_util
+    except Exception:  # pragma: no cover
+        return
+    lines = parity_util.margin_report()
+    if lines:
+        terminalreporter.write_sep("-", "parity margins (error, bound, fraction of the bound)")
+        for ln in lines:
+            terminalreporter.write_line(ln)

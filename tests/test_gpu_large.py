@@ -3,7 +3,8 @@
 stress (B=2, H=16, N=4096, d=128, Q and K x3, causal): every output against
 the full fp64 oracle.  long (B=1, H=32, N=16384, d=128, causal and
 non-causal): O, LSE and dQ on 64 seeded query rows per head, which the
-oracle computes row by row; dK and dV against the full oracle on one head,
+oracle computes row by row; every output of head (0, 0) (O, LSE, dQ, dK, dV)
+element by element against the full oracle of that head, under both masks;
 and the gradient identities sum_j dK_j = 0, sum_j dV_j = sum_i dO_i on all
 heads.
 """
@@ -60,10 +61,16 @@ def test_long_sampled_rows_and_identities(causal):
     assert np.linalg.norm(dv_sum - do_sum) <= GRAD_REL_TOL * np.linalg.norm(do_sum)
 
 
-def test_long_one_head_full_gradients():
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+def test_long_one_head_full_gradients(causal):
+    # Head (0, 0) of the long workload in full: with causal=False every key
+    # tile of every query tile is visited (no causal skip), so this is the
+    # only element-wise check of dK and dV on the full-size non-causal path.
     w = workloads.WORKLOADS["long"]
     x = workloads.workload_inputs(w)
-    o, lse, dq, dk, dv = _gpu(x, w.scale, True)
-    ref = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dO"], w.scale, True, heads=[(0, 0)])
+    o, lse, dq, dk, dv = _gpu(x, w.scale, causal)
+    ref = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dO"], w.scale, causal, heads=[(0, 0)])
+    check_o(to_np(o[0, 0]), ref["O"][0, 0], "O head0")
+    check_lse(to_np(lse[0, 0]), ref["LSE"][0, 0], "LSE head0")
     for name, got in (("dQ", dq), ("dK", dk), ("dV", dv)):
-        check_grad(to_np(got[0, 0]), ref[name][0, 0], name)
+        check_grad(to_np(got[0, 0]), ref[name][0, 0], f"{name} head0")

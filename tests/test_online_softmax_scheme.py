@@ -11,11 +11,13 @@ its bf16 rounding (and keeps the fp32 sum for the LSE).
 This test replays that arithmetic tile by tile (fp32 accumulation, bf16
 weights, base-2 exponentials) on the large-logit stress distribution and
 checks it against the exact fp64 softmax: with the correction it meets the
-parity bound (|err| <= max(1e-2, one bf16 ulp)) with margin, without it
-the error is about twice as large.  It pins the numerical argument, not the
+parity bound (|err| <= 1e-2 where |O| < 4, one bf16 ulp of O above), without
+it the error is about twice as large.  It pins the numerical argument, not the
 GPU code, which the GPU parity tests check.
 """
 import numpy as np
+
+from parity_util import o_bound
 
 
 def _bf16(x):
@@ -58,11 +60,11 @@ def test_lagging_max_with_max_weight_correction_meets_the_bound():
     ref_o = (w @ v.astype(np.float64)) / w.sum(1, keepdims=True)
     ref_lse = np.log(w.sum(1)) + s64.max(1)
     s32 = s64.astype(np.float32)  # the MMA's fp32 scores
-    bound = np.maximum(1e-2, np.exp2(np.floor(np.log2(np.maximum(np.abs(ref_o), 1e-30))) - 7))
+    bound = o_bound(ref_o)
 
     o, lse = _emulate(s32, v, 8.0, True)
     worst = (np.abs(_bf16(o) - ref_o) / bound).max()
-    assert worst < 0.9, worst
+    assert worst < 0.95, worst
     assert np.abs(lse - ref_lse).max() < 2e-3
 
     # Without the correction the pre-store error of O is about twice as large

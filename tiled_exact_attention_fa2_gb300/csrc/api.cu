@@ -182,6 +182,13 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
 
 }  // namespace
 
+int validate_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, float scale) {
+  return validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale);
+}
+
+int record_cuda_failure(int cuda_code, const char* where) { return cuda_fail(cuda_code, where); }
+
 int ensure_max_smem(const void* kernel, int bytes) {
   static std::mutex mu;
   static std::set<std::pair<const void*, int>> done;

@@ -105,6 +105,13 @@ int launch_bwd_main(const TmapSet& tm, const BwdProblem& p, int d, float scale, 
 int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, float scale, cudaStream_t stream);
 
 int read_fwd_status(int* value, bool reset);
+
+// The argument checks of fa2_bwd_gqa_ws (pointers, sizes, head grouping,
+// scale, alignment, overlaps): FA2_OK or the fa2_status of the first failure.
+int validate_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, float scale);
+// Record a CUDA failure for fa2_last_error_detail; returns FA2_ERR_CUDA.
+int record_cuda_failure(int cuda_code, const char* where);
 int read_bwd_status(int* value, bool reset);
 
 }  // namespace fa2

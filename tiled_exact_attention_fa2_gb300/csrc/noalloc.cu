@@ -18,12 +18,14 @@
 // different host threads, on the same device) race on it and give wrong
 // results.  The dQ accumulator part is zeroed by the first kernel of every
 // call, and D is fully rewritten, so no state leaks from one call to the next.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "fa2.h"
+#include "launch.h"
 
 namespace {
 
@@ -39,24 +41,66 @@ static __device__ __align__(256) unsigned char g_fa2_noalloc_scratch[kNoAllocScr
 
 namespace {
 
-std::mutex g_setup_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Once per device, with that device current: look up the device address of
-// the scratch array.  Returns nullptr on failure.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
+// through the runtime so the library needs no link-time libcuda), or 0 when
+// there is none or it cannot be read.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+struct ScratchSlot {
+  void* ptr;                 // device address of the array in context ctx_id
+  unsigned long long ctx_id;  // 0: not looked up yet
+};
+std::mutex g_setup_mu;
+ScratchSlot g_slots[kMaxDevices] = {};
+
+// Set-up, with the device current: look up the device address of the
+// scratch array once per device and CUDA context (again after a device reset
+// or a context switch, which change the context id; on every call if the id
+// cannot be read).  Returns nullptr on failure.
 void* scratch_for_current_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_fa2_noalloc_scratch) != cudaSuccess || !ptr) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = ptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  ScratchSlot& slot = g_slots[dev];
+  const unsigned long long id = current_context_id();
+  if (slot.ptr && id != 0 && id == slot.ctx_id) return slot.ptr;
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_fa2_noalloc_scratch);
+  if (e != cudaSuccess || !ptr) {
+    cudaGetLastError();
+    slot = ScratchSlot{};
+    fa2::record_cuda_failure(static_cast<int>(e != cudaSuccess ? e : cudaErrorInvalidSymbol),
+                             "cudaGetSymbolAddress (noalloc scratch)");
+    return nullptr;
+  }
+  // The lookup makes the device's primary context current if no context was.
+  slot = ScratchSlot{ptr, current_context_id()};
+  return ptr;
 }
 
 }  // namespace
@@ -68,11 +112,12 @@ size_t fa2_noalloc_scratch_capacity(void) { return kNoAllocScratchBytes; }
 int fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                     void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                     void* stream) {
-  const size_t need = fa2_bwd_workspace_bytes(B, H, N, d);
-  if (need > kNoAllocScratchBytes) return FA2_ERR_SCRATCH_CAPACITY;
+  // The checks fa2_bwd makes, in its order, before the capacity check and
+  // before any CUDA call.
+  if (int rc = fa2::validate_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d, scale)) return rc;
+  if (fa2_bwd_workspace_bytes(B, H, N, d) > kNoAllocScratchBytes) return FA2_ERR_SCRATCH_CAPACITY;
   void* scratch = scratch_for_current_device();
   if (!scratch) return FA2_ERR_CUDA;
-  // need == 0 means the sizes are invalid; fa2_bwd_ws reports which check failed.
   return fa2_bwd_ws(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, scratch, kNoAllocScratchBytes,
                     stream);
 }
