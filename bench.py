@@ -1,9 +1,9 @@
 #!/usr/bin/env python
 """Throughput of the FA2 hot path (forward + backward) on GB300.
 
-One step = fa2_fwd followed by the three backward stages (D preprocess, main
-recompute kernel, dQ convert) on one batch of synthetic inputs already
-resident in HBM.  Default workload: the long-sequence configuration
+One step = the forward pass (fp16 copy of V, attention kernel) followed by
+the three backward stages (D preprocess, main recompute kernel, dQ convert)
+on one batch of synthetic inputs already resident in HBM.  Default workload: the long-sequence configuration
 B=1, H=32, N=16384, d=128, causal (Q, K, V, dO are 134 MB each, so the
 inputs of a step exceed the 129 MB L2 and no flush is needed).
 
@@ -398,8 +398,9 @@ def measure_square_rows(fa2, dev, stream, peaks, names=("stress", "b4h32n4096"))
         dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
         Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        fws = torch.empty(fa2.fa2_fwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
         sc = w.scale
-        f_ms = _time_ms(lambda: fa2.fa2_fwd(g["q"], g["k"], g["v"], o, lse, sc, True, stream), stream)
+        f_ms = _time_ms(lambda: fa2.fa2_fwd_ws(g["q"], g["k"], g["v"], fws, o, lse, sc, True, stream), stream)
         b_ms = _time_ms(lambda: fa2.fa2_bwd_stages(g["q"], g["k"], g["v"], o, g["dO"], lse, Dvec, acc, dq, dk, dv,
                                                    sc, True, stream), stream)
         lib = fa2.load_library()
@@ -416,14 +417,14 @@ def measure_square_rows(fa2, dev, stream, peaks, names=("stress", "b4h32n4096"))
                      "bwd_pct_of_peak_burst": 100 * tf(bf, b_ms) / peaks["bf16_tflops"],
                      "bwd_main_ms": m_ms, "bwd_main_tflops": tf(bf, m_ms),
                      "target": "forward >= 60 %, backward >= 45 % of the burst peak"}
-        del g, o, lse, dq, dk, dv, Dvec, acc
+        del g, o, lse, dq, dk, dv, Dvec, acc, fws
     return out
 
 
 def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
     """Microseconds per forward + backward step on the small workloads, where
     launch work rather than the GPU sets the time: 200 steps enqueued back to
-    back (fa2_fwd + fa2_bwd_ws, 4 kernels each; device time per step from CUDA
+    back (fa2_fwd_ws + fa2_bwd_ws, 5 kernels each; device time per step from CUDA
     events, host time per step from the clock around the enqueue), and the
     same step replayed from a CUDA graph."""
     out = {}
@@ -436,10 +437,11 @@ def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
         ws = torch.empty(fa2.fa2_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+        fws = torch.empty(fa2.fa2_fwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
         side = torch.cuda.Stream(device=dev)
 
         def step():
-            fa2.fa2_fwd(g["q"], g["k"], g["v"], o, lse, w.scale, True, side)
+            fa2.fa2_fwd_ws(g["q"], g["k"], g["v"], fws, o, lse, w.scale, True, side)
             fa2.fa2_bwd_ws(g["q"], g["k"], g["v"], o, g["dO"], lse, ws, dq, dk, dv, w.scale, True, side)
 
         n = 200
@@ -458,7 +460,7 @@ def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
             with torch.cuda.graph(graph, stream=side):
-                fa2.fa2_fwd(g["q"], g["k"], g["v"], o, lse, w.scale, True, None)
+                fa2.fa2_fwd_ws(g["q"], g["k"], g["v"], fws, o, lse, w.scale, True, None)
                 fa2.fa2_bwd_ws(g["q"], g["k"], g["v"], o, g["dO"], lse, ws, dq, dk, dv, w.scale, True, None)
         for _ in range(20):
             graph.replay()
@@ -472,8 +474,8 @@ def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
         graph_us = a.elapsed_time(b) / n * 1e3
         out[name] = {"workload": f"B={B} H={H} N={N} d={d} causal", "us_per_step": dev_us,
                      "host_enqueue_us_per_step": host_us, "graph_replay_us_per_step": graph_us,
-                     "launches_per_step": 4}
-        del graph, g, o, lse, dq, dk, dv, ws
+                     "launches_per_step": 5}
+        del graph, g, o, lse, dq, dk, dv, ws, fws
     return out
 
 
@@ -500,6 +502,7 @@ def run_gpu(args, w, causal):
     dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
     Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq_acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    fws = torch.empty(fa2.fa2_fwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     scale = w.scale
     fwd_flops, bwd_flops = w.fwd_flops(causal), w.bwd_flops(causal)
@@ -510,7 +513,7 @@ def run_gpu(args, w, causal):
     def step(i):
         e = ev[i]
         e[0].record(stream)
-        fa2.fa2_fwd(g["q"], g["k"], g["v"], o, lse, scale, causal, stream)
+        fa2.fa2_fwd_ws(g["q"], g["k"], g["v"], fws, o, lse, scale, causal, stream)
         fa2.fa2_bwd_stages(g["q"], g["k"], g["v"], o, g["dO"], lse, Dvec, dq_acc, dq, dk, dv, scale, causal,
                            stream, hook=lambda j: e[j + 1].record(stream))
 
@@ -583,6 +586,8 @@ def run_gpu(args, w, causal):
                "frac_of_burst": tf / peaks["bf16_tflops"],
                "frac_of_sustained": tf / peaks["bf16_tflops_sustained"]}
         for name, tf, ms in (("fa2_bwd_kernel", main_tf, main_ms), ("fa2_fwd_kernel", fwd_tf, fwd_ms))}
+    rooflines["fa2_fwd_kernel"]["note"] = ("time of the whole forward pass (fa2_v_to_f16_kernel, the fp16 copy of V, "
+                                           "then fa2_fwd_kernel); the launch list under profiles/ gives the split")
     dominant = "fa2_bwd_kernel" if main_ms >= fwd_ms else "fa2_fwd_kernel"
     if rank != 0:
         return 0
@@ -603,7 +608,7 @@ def run_gpu(args, w, causal):
         "roofline_other": rooflines["fa2_fwd_kernel" if dominant == "fa2_bwd_kernel" else "fa2_bwd_kernel"],
         "timing": {"fwd_ms": _stats(fwd_list), "bwd_main_ms": _stats(main_list),
                    "method": "CUDA events on the launching stream around each kernel of every timed step"},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "device_status": status,
         "clocks": clocks,
         "e2e": e2e,

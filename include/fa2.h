@@ -62,10 +62,27 @@ typedef enum {
  * Forward pass.  Writes o [B,H,N,d] bf16 and lse [B,H,N] fp32.
  * Source: the article's forward-pass bullet (blocked K/V walk, online
  * softmax state, no stored score matrix) and backward-pass bullet (the
- * saved log-sum-exp).  One kernel launch.
+ * saved log-sum-exp).  Two kernel launches: one writes an fp16 copy of V,
+ * the attention kernel then multiplies the weights P with it in fp16 (the
+ * weights carry 11 significant bits instead of bf16's 8, which keeps O's
+ * error under the parity bound on sharply peaked rows).  A K/V head holding
+ * a value of V outside the fp16 range (|v| > 65504) keeps bf16 V and
+ * weights.  The scratch (fa2_fwd_workspace_bytes bytes) is obtained with
+ * cudaMallocAsync and released with cudaFreeAsync on `stream`.
  */
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
             float scale, int causal, void* stream);
+
+/*
+ * fa2_fwd with caller-owned scratch: `workspace` (device, 256-byte aligned,
+ * not overlapping any argument) of at least fa2_fwd_workspace_bytes(B, H, N,
+ * d) bytes (H_kv in place of H for fa2_fwd_gqa_ws); FA2_ERR_WORKSPACE if it
+ * is NULL, misaligned or too small, FA2_ERR_ALIAS if it overlaps an input or
+ * output.  fa2_fwd_workspace_bytes returns 0 for invalid sizes.
+ */
+size_t fa2_fwd_workspace_bytes(int B, int H_kv, int N, int d);
+int fa2_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+               float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass for L with dL/dO = dO.  Reads q, k, v, the forward's o and
@@ -90,6 +107,8 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const vo
  */
 int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
                 int d, float scale, int causal, void* stream);
+int fa2_fwd_gqa_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                   int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 int fa2_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                 void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale, int causal,
                 void* stream);
@@ -113,7 +132,8 @@ int fa2_bwd_gqa_ws(const void* q, const void* k, const void* v, const void* o, c
  * workspace: device pointer, 256-byte aligned, of at least
  * fa2_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits) bytes (may be
  * NULL when that is 0, i.e. a single split).  Two launches (one if a single
- * split).  Other rules as fa2_fwd.
+ * split).  Other rules as fa2_fwd, except that P V runs in bf16 here (no
+ * fp16 copy of V: this path's time is the single read of the cache).
  */
 size_t fa2_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
 /*
@@ -153,7 +173,9 @@ int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float*
  * status word (fa2_device_status) is set to 3.
  * Sizes: B >= 1, total_q, total_k >= 0 (<= 2^30), 0 <= max_seqlen <= total,
  * max_seqlen >= 1 when its total is > 0.  Pointers of tensors with zero rows
- * may be NULL.  fa2_fwd_varlen: one kernel launch.  fa2_bwd_varlen: the same
+ * may be NULL.  fa2_fwd_varlen: two kernel launches (the fp16 copy of V,
+ * as in fa2_fwd, in a cudaMallocAsync workspace on `stream`, then the
+ * attention kernel; one if total_k is 0).  fa2_bwd_varlen: the same
  * three stages as fa2_bwd_ws with caller scratch of
  * fa2_bwd_varlen_workspace_bytes(H, total_q, d) bytes (256-byte aligned; may
  * be NULL when total_q or total_k is 0, which only zeroes dk, dv or dq).

@@ -20,7 +20,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "FA2Error", "load_library", "fa2_fwd", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
+    "FA2Error", "load_library", "fa2_fwd", "fa2_fwd_ws", "fa2_fwd_workspace_bytes", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
     "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
     "fa2_bwd_stages", "fa2_bwd_noalloc", "fa2_fwd_gqa", "fa2_bwd_gqa", "fa2_fwd_splitkv",
     "fa2_fwd_varlen", "fa2_bwd_varlen", "FA2_OK",
@@ -36,6 +36,9 @@ _sz = ctypes.c_size_t
 
 _SIGNATURES = {
     "fa2_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_fwd_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "fa2_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa2_fwd_gqa_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa2_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa2_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
@@ -154,6 +157,31 @@ def fa2_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: Optional[torch
                      _scale(scale, d), 1 if causal else 0, _stream(stream, q.device))
     if rc != FA2_OK:
         raise FA2Error("fa2_fwd", rc)
+    return o, lse
+
+
+def fa2_fwd_workspace_bytes(B: int, H_kv: int, N: int, d: int) -> int:
+    return load_library().fa2_fwd_workspace_bytes(B, H_kv, N, d)
+
+
+def fa2_fwd_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, workspace: torch.Tensor,
+               o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+               causal: bool = True, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """fa2_fwd with caller-owned scratch (a CUDA byte tensor of fa2_fwd_workspace_bytes bytes)."""
+    lib = load_library()
+    B, H, N, d = _shape(q, "q")
+    if _shape(k, "k") != (B, H, N, d) or _shape(v, "v") != (B, H, N, d):
+        raise ValueError("q, k and v must have the same shape")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    _shape(o, "o")
+    rc = lib.fa2_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                        _scale(scale, d), 1 if causal else 0, workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_fwd_ws", rc)
     return o, lse
 
 

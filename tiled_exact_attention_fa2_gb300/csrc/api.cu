@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -44,10 +45,13 @@ constexpr int kRowsPerTile = 128;
 // head_stride = N d.  Packed [total, H, d]: row_stride = H d, head_stride = d.
 // Box = [1, 128 rows, box_cols columns] with the swizzle as wide as the box
 // row; rows past `rows` read as zero and are dropped by reduce-adds.
-bool encode_rows(CUtensorMap* out, const void* base, bool f32, int heads, long long rows, int d,
+enum class Elem { kBf16, kF16, kF32 };
+
+bool encode_rows(CUtensorMap* out, const void* base, Elem type, int heads, long long rows, int d,
                  long long row_stride, long long head_stride) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
+  const bool f32 = type == Elem::kF32;
   const int esz = f32 ? 4 : 2;
   const int box_cols = f32 ? (d >= 32 ? 32 : d) : (d >= 64 ? 64 : d);
   const int row_bytes = box_cols * esz;
@@ -59,19 +63,21 @@ bool encode_rows(CUtensorMap* out, const void* base, bool f32, int heads, long l
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride) * esz, static_cast<cuuint64_t>(head_stride) * esz};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), kRowsPerTile, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+  const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : (type == Elem::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  return enc(out, dt, 3,
              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // [B*H, N, d] bf16 view, box = [1, 128 rows, min(d, 64) columns].
-bool make_tmap(CUtensorMap* out, const void* base, int BH, int N, int d) {
-  return encode_rows(out, base, false, BH, N, d, d, static_cast<long long>(N) * d);
+bool make_tmap(CUtensorMap* out, const void* base, int BH, int N, int d, Elem type = Elem::kBf16) {
+  return encode_rows(out, base, type, BH, N, d, d, static_cast<long long>(N) * d);
 }
 
 // Packed [total, heads, d] bf16 view (variable-length batches).
-bool make_tmap_packed(CUtensorMap* out, const void* base, int heads, int total, int d) {
-  return encode_rows(out, base, false, heads, total, d, static_cast<long long>(heads) * d, d);
+bool make_tmap_packed(CUtensorMap* out, const void* base, int heads, int total, int d, Elem type = Elem::kBf16) {
+  return encode_rows(out, base, type, heads, total, d, static_cast<long long>(heads) * d, d);
 }
 
 // Text of the last CUDA failure seen by an entry point on this host thread.
@@ -87,7 +93,7 @@ int cuda_fail(int cuda_code, const char* where) {
 // [B*H, N, d] fp32 view of the dQ accumulator for TMA reduce-add, box =
 // [1, 128 rows, min(d, 32) columns], swizzle = box row width.
 bool make_tmap_f32(CUtensorMap* out, const void* base, int BH, int N, int d) {
-  return encode_rows(out, base, true, BH, N, d, d, static_cast<long long>(N) * d);
+  return encode_rows(out, base, Elem::kF32, BH, N, d, d, static_cast<long long>(N) * d);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -119,6 +125,41 @@ size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 size_t workspace_bytes(int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
+}
+
+// Forward workspace: the fp16 copy of V (kv_elems values), then per K/V head
+// a 64-bit range flag and the fp32 scale of the head's copy.
+size_t fwd_workspace(size_t kv_elems, size_t kv_heads) {
+  return round_up(kv_elems * 2) + round_up(kv_heads * sizeof(unsigned long long)) + round_up(kv_heads * sizeof(float));
+}
+
+// A number no earlier forward call of this process used: a head's range
+// flag counts as set only if it holds the current call's number, so the
+// flags need no clearing between calls.
+unsigned long long next_fwd_call() {
+  static std::atomic<unsigned long long> calls{0};
+  return ++calls;
+}
+
+// Write the fp16 copy of V (and the per-head scales) into the workspace and
+// point p / tm.v16 at it.  V is [heads, rows, d] or packed [rows, heads, d].
+int prepare_v16(TmapSet* tm, FwdProblem* p, const void* v, int heads, int rows, int d, bool packed, void* ws,
+                cudaStream_t st) {
+  const size_t kv_elems = static_cast<size_t>(heads) * rows * d;
+  char* w = static_cast<char*>(ws);
+  void* v16 = w;
+  auto* flags = reinterpret_cast<unsigned long long*>(w + round_up(kv_elems * 2));
+  auto* scales = reinterpret_cast<float*>(w + round_up(kv_elems * 2) + round_up(heads * sizeof(unsigned long long)));
+  const bool ok = packed ? make_tmap_packed(&tm->v16, v16, heads, rows, d, Elem::kF16)
+                         : make_tmap(&tm->v16, v16, heads, rows, d, Elem::kF16);
+  if (!ok) return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
+  p->v_scale = scales;
+  const long long row_stride = packed ? static_cast<long long>(heads) * d : d;
+  const long long head_stride = packed ? d : static_cast<long long>(rows) * d;
+  if (int e = launch_v_to_f16(v, v16, flags, scales, next_fwd_call(), heads, rows, d, row_stride, head_stride, packed,
+                              st))
+    return cuda_fail(e, "v to f16 launch");
+  return FA2_OK;
 }
 
 // Query heads H, key/value heads Hkv (H a multiple of Hkv).
@@ -208,8 +249,12 @@ using namespace fa2;
 
 extern "C" {
 
-int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
-                int d, float scale, int causal, void* stream) {
+}  // extern "C" (reopened below)
+
+namespace {
+
+int validate_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                 int d, float scale) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
   if (int rc = check_sizes(B, H, N, d)) return rc;
   if (int rc = check_heads(H, H_kv)) return rc;
@@ -224,7 +269,24 @@ int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse
   for (const Range& r : ins)
     if (overlap(ro, r) || overlap(rl, r)) return FA2_ERR_ALIAS;
   if (overlap(ro, rl)) return FA2_ERR_ALIAS;
+  return FA2_OK;
+}
 
+// The workspace must not overlap any input or output.
+bool fwd_ws_overlaps(const void* ws, size_t ws_bytes, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, int B, int H, int H_kv, int N, int d) {
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t kb = static_cast<size_t>(B) * H_kv * N * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  const Range rw = range_of(ws, ws_bytes);
+  const Range all[] = {range_of(q, tb), range_of(k, kb), range_of(v, kb), range_of(o, tb), range_of(lse, lb)};
+  for (const Range& r : all)
+    if (overlap(rw, r)) return true;
+  return false;
+}
+
+int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N, int d,
+            float scale, int causal, void* ws, cudaStream_t st) {
   const int BH = B * H;
   TmapSet tm;
   if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, B * H_kv, N, d) || !make_tmap(&tm.v, v, B * H_kv, N, d))
@@ -239,9 +301,48 @@ int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse
   p.tiles_per_split = (N + kRowsPerTile - 1) / kRowsPerTile;
   p.o = o;
   p.lse = lse;
-  if (int e = launch_fwd(tm, p, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
-    return cuda_fail(e, "fwd launch");
+  if (int rc = prepare_v16(&tm, &p, v, B * H_kv, N, d, false, ws, st)) return rc;
+  if (int e = launch_fwd(tm, p, d, scale, causal != 0, st)) return cuda_fail(e, "fwd launch");
   return FA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa2_fwd_workspace_bytes(int B, int H_kv, int N, int d) {
+  if (check_sizes(B, H_kv, N, d) != FA2_OK) return 0;
+  return fwd_workspace(static_cast<size_t>(B) * H_kv * N * d, static_cast<size_t>(B) * H_kv);
+}
+
+int fa2_fwd_gqa_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                   int d, float scale, int causal, void* workspace, size_t workspace_bytes_given, void* stream) {
+  if (int rc = validate_fwd(q, k, v, o, lse, B, H, H_kv, N, d, scale)) return rc;
+  const size_t need = fa2_fwd_workspace_bytes(B, H_kv, N, d);
+  if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < need) return FA2_ERR_WORKSPACE;
+  if (fwd_ws_overlaps(workspace, need, q, k, v, o, lse, B, H, H_kv, N, d)) return FA2_ERR_ALIAS;
+  return run_fwd(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int fa2_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+               float scale, int causal, void* workspace, size_t workspace_bytes_given, void* stream) {
+  return fa2_fwd_gqa_ws(q, k, v, o, lse, B, H, H, N, d, scale, causal, workspace, workspace_bytes_given, stream);
+}
+
+int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                int d, float scale, int causal, void* stream) {
+  if (int rc = validate_fwd(q, k, v, o, lse, B, H, H_kv, N, d, scale)) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = fa2_fwd_workspace_bytes(B, H_kv, N, d);
+  void* ws = nullptr;
+  if (cudaError_t e = cudaMallocAsync(&ws, bytes, st)) {
+    cudaGetLastError();
+    cuda_fail(static_cast<int>(e), "cudaMallocAsync");
+    return FA2_ERR_ALLOC;
+  }
+  const int rc = run_fwd(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, ws, st);
+  if (cudaError_t e = cudaFreeAsync(ws, st)) return cuda_fail(static_cast<int>(e), "cudaFreeAsync");
+  return rc;
 }
 
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -527,9 +628,25 @@ int fa2_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* 
   if (!make_tmap_packed(&tm.q, q, H, total_q, d) || !make_tmap_packed(&tm.k, kb_ptr, H_kv, tk, d) ||
       !make_tmap_packed(&tm.v, vb_ptr, H_kv, tk, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
-  if (int e = launch_fwd(tm, p, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
-    return cuda_fail(e, "varlen fwd launch");
-  return FA2_OK;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (total_k == 0) {  // no keys: V is never read (its maps describe q)
+    tm.v16 = tm.v;
+    if (int e = launch_fwd(tm, p, d, scale, causal != 0, st)) return cuda_fail(e, "varlen fwd launch");
+    return FA2_OK;
+  }
+  // fp16 copy of the packed V ([total_k, H_kv, d]) in a stream-ordered workspace.
+  const size_t kv_elems = static_cast<size_t>(total_k) * H_kv * d;
+  void* ws = nullptr;
+  if (cudaError_t e = cudaMallocAsync(&ws, fwd_workspace(kv_elems, H_kv), st)) {
+    cudaGetLastError();
+    cuda_fail(static_cast<int>(e), "cudaMallocAsync");
+    return FA2_ERR_ALLOC;
+  }
+  int rc = prepare_v16(&tm, &p, v, H_kv, total_k, d, true, ws, st);
+  if (rc == FA2_OK)
+    if (int e = launch_fwd(tm, p, d, scale, causal != 0, st)) rc = cuda_fail(e, "varlen fwd launch");
+  if (cudaError_t e = cudaFreeAsync(ws, st)) return cuda_fail(static_cast<int>(e), "cudaFreeAsync");
+  return rc;
 }
 
 size_t fa2_bwd_varlen_workspace_bytes(int H, int total_q, int d) {
@@ -584,7 +701,7 @@ int fa2_bwd_varlen(const void* q, const void* k, const void* v, const void* o, c
   TmapSet tm;
   if (!make_tmap_packed(&tm.q, q, H, total_q, d) || !make_tmap_packed(&tm.k, k, H_kv, total_k, d) ||
       !make_tmap_packed(&tm.v, v, H_kv, total_k, d) || !make_tmap_packed(&tm.dO, dO, H, total_q, d) ||
-      !encode_rows(&tm.dqacc, dq_acc, true, H, total_q, d, static_cast<long long>(H) * d, d))
+      !encode_rows(&tm.dqacc, dq_acc, Elem::kF32, H, total_q, d, static_cast<long long>(H) * d, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
   // D and the zeroed accumulator in the packed row order ([total_q, H]).
   if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, H, total_q, d, st)) return cuda_fail(e, "bwd preprocess launch");

@@ -23,9 +23,16 @@
 // One issuer per tile, so that waiting on one tile's MMA never delays the
 // other tile's; K/V stages are released once both issuers are done with them.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A and O_B after them.  The
-// softmax overwrites the first 64 columns of S_X with P_X (bf16 pairs) and
+// softmax overwrites the first 64 columns of S_X with P_X (fp16 pairs) and
 // O_X += P_X V_j reads P_X straight from TMEM (A operand in TMEM), so P never
-// touches shared memory.  S_X(j+1) is issued only after P_X(j) V_j has
+// touches shared memory.  P V runs on fp16 operands, with V read from an
+// fp16 copy that fa2_v_to_f16_kernel writes before the forward kernel runs:
+// fp16 keeps three more significant bits than bf16, and with bf16 weights
+// their rounding alone moves O by up to about 0.2 % on rows dominated by a
+// few keys.  A K/V head holding a finite value beyond the fp16 range is
+// copied scaled by a power of two, which the epilogue multiplies back.  The
+// split-KV form (decoding), whose time is the single read of the cache,
+// runs P V in bf16 on V itself.  S_X(j+1) is issued only after P_X(j) V_j has
 // completed, because it overwrites the columns that MMA reads (decoding,
 // where tile B is empty, double-buffers S over both ranges instead).
 // The reference value m that the exponentials subtract is raised only when a
@@ -37,6 +44,7 @@
 // instruction count.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -55,7 +63,8 @@ constexpr int kSchedReaders = 11;
 constexpr uint32_t kTmemCols = 512;
 // A row's reference max is raised only when a tile's max exceeds it by more
 // than this (log2 units): weights 2^(s - m) then stay below 2^8, well inside
-// bf16 and fp32 range, and the result is the same softmax up to rounding.
+// fp16 (65504), bf16 and fp32 range, and the result is the same softmax up to
+// rounding.
 constexpr float kRescaleSlack = 8.f;
 
 enum FwdBar {
@@ -209,6 +218,9 @@ template <int D, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdProblem p, float scale_log2) {
+  // P V on fp16 operands (tm_v is then the fp16 copy of V), except in the
+  // split-KV form.
+  constexpr bool kF16 = MODE != kGeneral;
   using T = HeadDim<D>;
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -338,7 +350,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       const int x = warp - 9;
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q (K-major) x K (K-major)
-      constexpr uint32_t kIdescO = make_idesc_bf16(128, D, false, true);     // P (TMEM) x V (MN-major)
+      // P (TMEM) x V (MN-major)
+      constexpr uint32_t kIdescO = kF16 ? make_idesc_f16(128, D, false, true) : make_idesc_bf16(128, D, false, true);
       const uint32_t sQ0 = smem_u32(smem + C::kQ), sK0 = smem_u32(smem + C::kK), sV0 = smem_u32(smem + C::kV);
       const uint32_t tOx = tmem + (x ? C::kColO1 : C::kColO0);
       // S buffer of the tile's k-th S: S_x, or S_A / S_B alternately when dual.
@@ -491,6 +504,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
       const int imin_x = x ? w.imin[1] : w.imin[0];
       const int off = w.off, Nk = w.Nk;
+      // V scale of the unit's K/V head (read now, used by the epilogue)
+      const float v_scale = (kF16 && p.v_scale != nullptr) ? __ldg(p.v_scale + w.rh_kv) : 1.f;
       float m = -INFINITY;  // reference max, log2 units (scores * scale * log2 e); row max - m <= slack
       float l = 0.f;        // running sum of 2^(x - m) (fp32 weights: the LSE)
       float lo = 0.f;       // the same with each tile's largest weight as bf16 (normalises O)
@@ -540,7 +555,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // rounded to bf16; normalising O by a sum that carries the same
         // rounding keeps O the weighted mean of V that the MMA computed.
         const float pmax = ex2_approx(fmaf(mx, scale_log2, -m_use));
-        const float dpmax = unpack_bf16x2(pack_bf16x2(pmax, 0.f)).x - pmax;
+        const float dpmax = (kF16 ? f16lo_to_f32(pack_f16x2(pmax, 0.f)) : unpack_bf16x2(pack_bf16x2(pmax, 0.f)).x) - pmax;
         if (j < turns && !(ok = take_turn())) break;
 
         // P = 2^(s * scale_log2 - m) on packed pairs; 4 independent pair sums.
@@ -557,7 +572,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const float2 xx = f2_unpack(ffma2(f2_pack(s[e], s[e + 1]), scale2, negm2));
             const float p0 = ex2_approx(xx.x), p1 = ex2_approx(xx.y);
             acc[i & 3] = fadd2(acc[i & 3], f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
+            pk[i] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
           tmem_st16u(tS + 16 * c, pk);
         }
@@ -647,7 +662,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // race it.
       if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
       tc_fence_after();
-      const float inv_l = lo > 0.f ? 1.f / lo : 0.f;
+      const float inv_l = lo > 0.f ? v_scale / lo : 0.f;
       constexpr int kC = D >= 32 ? 32 : 16;
 #pragma unroll
       for (int c = 0; c < D / kC; ++c) {
@@ -702,7 +717,11 @@ template <int D, bool CAUSAL>
 int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stream) {
   using C = FwdCfg<D>;
   const bool varlen = p.cu_q != nullptr;
-  const bool general = p.splits > 1 || p.M != p.Nq || p.Nq != p.Nk;
+  // The square form runs P V in fp16 and needs the fp16 copy of V: a square
+  // problem without one (split-KV with one split and Nq = Nk) takes the
+  // general form.  Packed batches come with the copy, or (no keys) never
+  // read V.
+  const bool general = p.v_scale == nullptr || p.splits > 1 || p.M != p.Nq || p.Nq != p.Nk;
   // Every row-head re-reads the K and V rows of its split.
   const int kv_rows = min(p.Nk, p.tiles_per_split * kTileRows);
   p.heads_per_group = heads_per_l2_group(static_cast<size_t>(kv_rows) * D * 4 / p.kvdiv, p.RH);
@@ -717,7 +736,79 @@ int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stre
   const long long units = static_cast<long long>(num_pairs) * p.RH * (varlen ? p.batches : p.splits);
   const dim3 grid(static_cast<unsigned>(units > 0 ? units : 1));
   const float scale_log2 = scale * 1.44269504088896341f;
-  return launch_pdl(kern, grid, dim3(kFwdThreads), C::kBytes, stream, tm.q, tm.k, tm.v, p, scale_log2);
+  // Square and packed problems read the fp16 copy of V.
+  return launch_pdl(kern, grid, dim3(kFwdThreads), C::kBytes, stream, tm.q, tm.k, (general && !varlen) ? tm.v : tm.v16, p,
+                    scale_log2);
+}
+
+// V in fp16 for the P V MMA: one pass over V (16-byte loads and stores,
+// grid-stride), exact for every bf16 value of magnitude below 2^16 (below
+// 2^-14 fp16 keeps fewer significant bits: an absolute error under 2^-25;
+// infinities and NaN carry over).  A finite value beyond the fp16 range
+// (|v| > 65504) flags its K/V head for fa2_v_scale_kernel.
+__global__ void __launch_bounds__(256) fa2_v_to_f16_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16,
+                                                           unsigned long long* __restrict__ flags,
+                                                           unsigned long long call, long long n8, long long inner,
+                                                           int heads) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 a = __ldg(v + i);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t h[4];
+    bool big = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+      big |= (fabsf(lo) > 65504.f && fabsf(lo) < INFINITY) || (fabsf(hi) > 65504.f && fabsf(hi) < INFINITY);
+      h[e] = pack_f16x2(lo, hi);
+    }
+    v16[i] = make_uint4(h[0], h[1], h[2], h[3]);
+    if (big) flags[(i * 8 / inner) % heads] = call;
+  }
+}
+
+// One CTA per K/V head: v_scale[h] = 1, or for a head flagged by
+// fa2_v_to_f16_kernel the smallest power of two 2^k with
+// max |v| / 2^k <= 2^15 (finite values), after rewriting that head's copy as
+// fp16(v / 2^k) (exact scaling by a power of two).
+__global__ void __launch_bounds__(256) fa2_v_scale_kernel(const __nv_bfloat16* __restrict__ v,
+                                                          __half* __restrict__ v16,
+                                                          const unsigned long long* __restrict__ flags,
+                                                          float* __restrict__ scales, unsigned long long call,
+                                                          long long rows, int d, long long row_stride,
+                                                          long long head_stride) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int h = blockIdx.x;
+  if (flags[h] != call) {
+    if (threadIdx.x == 0) scales[h] = 1.f;
+    return;
+  }
+  const long long n = rows * d;
+  const long long base = static_cast<long long>(h) * head_stride;
+  auto at = [&](long long e) { return base + (e / d) * row_stride + e % d; };
+  float mx = 0.f;
+  for (long long e = threadIdx.x; e < n; e += blockDim.x) {
+    const float a = fabsf(__bfloat162float(v[at(e)]));
+    if (a < INFINITY) mx = fmaxf(mx, a);
+  }
+  __shared__ float red[32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = 0.f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) mx = fmaxf(mx, red[i]);
+  int k = 0;
+  while (ldexpf(mx, -k) > 32768.f) ++k;
+  const float inv = ldexpf(1.f, -k);
+  for (long long e = threadIdx.x; e < n; e += blockDim.x) {
+    const long long i = at(e);
+    v16[i] = __float2half_rn(__bfloat162float(v[i]) * inv);
+  }
+  if (threadIdx.x == 0) scales[h] = ldexpf(1.f, k);
 }
 
 // Merge per-split results: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
@@ -785,6 +876,22 @@ int launch_fwd(const TmapSet& tm, const FwdProblem& p, int d, float scale, bool 
       return causal ? launch_fwd_t<128, true>(tm, p, scale, stream) : launch_fwd_t<128, false>(tm, p, scale, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
+}
+
+int launch_v_to_f16(const void* v, void* v16, unsigned long long* v_flags, float* v_scale, unsigned long long call,
+                    int heads, long long rows, int d, long long row_stride, long long head_stride, bool packed,
+                    cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(heads) * rows * d / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  const long long inner = packed ? d : rows * d;
+  if (int e = launch_pdl(fa2_v_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                         static_cast<const uint4*>(v), static_cast<uint4*>(v16), v_flags, call, n8, inner, heads))
+    return e;
+  return launch_pdl(fa2_v_scale_kernel, dim3(static_cast<unsigned>(heads)), dim3(256), 0, stream,
+                    static_cast<const __nv_bfloat16*>(v), static_cast<__half*>(v16),
+                    static_cast<const unsigned long long*>(v_flags), v_scale, call, rows, d, row_stride, head_stride);
 }
 
 int launch_splitkv_combine(const FwdProblem& p, int d, cudaStream_t stream) {

@@ -6,10 +6,10 @@
 
 namespace fa2 {
 
-// TMA descriptors of the [B*H, N, d] views of the operands (bf16) and of
-// the fp32 dQ accumulator.
+// TMA descriptors of the [B*H, N, d] views of the operands (bf16), of the
+// fp16 copy of V the forward pass reads, and of the fp32 dQ accumulator.
 struct TmapSet {
-  CUtensorMap q, k, v, dO, dqacc;
+  CUtensorMap q, k, v, v16, dO, dqacc;
 };
 
 // Launch `kern` on `stream` with programmatic stream serialisation (the
@@ -64,6 +64,13 @@ inline int heads_per_l2_group(size_t bytes_per_head, int heads) {
 // cu_k[b] .. cu_k[b+1] - 1 (device arrays of batches + 1 ints), M = max
 // query length, Nk = max key length, one split.  Query i of a sequence with
 // Lq queries and Lk keys sees key j iff j <= i + Lk - Lq when causal.
+//
+// Square and variable-length problems run P V on fp16 operands: tm.v16
+// describes an fp16 copy of V (same layout) written by launch_v_to_f16, in
+// which K/V head h (index along the K/V map's head coordinate) is scaled by
+// 1 / v_scale[h] (a power of two, 1 unless the head holds a finite value
+// beyond the fp16 range); O of that head is multiplied by v_scale[h].  The
+// general (split-KV) form runs P V in bf16 on V itself.
 struct FwdProblem {
   int RH, M, Nq, Nk, kvdiv, splits, tiles_per_split;
   int heads_per_group;  // row-heads per CTA group (set by launch_fwd)
@@ -74,9 +81,22 @@ struct FwdProblem {
   const int* cu_q;
   const int* cu_k;
   int batches, total_q, total_k;
+  const float* v_scale;
 };
 
 int launch_fwd(const TmapSet& tm, const FwdProblem& p, int d, float scale, bool causal, cudaStream_t stream);
+// The fp16 copy of V for the forward pass, in two kernels: (1) v16[e] =
+// fp16(v[e]) for the `elems` bf16 values of V, and for every finite value
+// beyond the fp16 range v_flags[(e / inner) % heads] = call (the K/V head of
+// element e: [heads, N, d] -> inner = N d; packed [total, heads, d] -> inner
+// = d); (2) one CTA per K/V head writes v_scale[h] = 1, or, for a flagged
+// head, the power of two 2^k that brings its largest finite magnitude into
+// the fp16 range and rewrites the head's copy as fp16(v / 2^k).  Element
+// (row r, column c) of head h is v[r * row_stride + h * head_stride + c],
+// r < rows.  Flags holding another call's number count as clear.
+int launch_v_to_f16(const void* v, void* v16, unsigned long long* v_flags, float* v_scale, unsigned long long call,
+                    int heads, long long rows, int d, long long row_stride, long long head_stride, bool packed,
+                    cudaStream_t stream);
 int launch_splitkv_combine(const FwdProblem& p, int d, cudaStream_t stream);
 int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int BH, int N, int d,
                           cudaStream_t stream);

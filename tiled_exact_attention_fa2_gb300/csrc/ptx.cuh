@@ -369,6 +369,10 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_m
          (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+// The same for f16 x f16 -> fp32 (A and B format codes 0).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return make_idesc_bf16(M, N, a_mn_major, b_mn_major) & ~((7u << 7) | (7u << 10));
+}
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128-byte-swizzled tile whose rows are 128 bytes long (the layout TMA's
@@ -424,6 +428,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;  // round-to-nearest-even; `lo` lands in the low half
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;  // round-to-nearest-even; `lo` lands in the low half
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The low half of an f16x2 word as fp32.
+__device__ __forceinline__ float f16lo_to_f32(uint32_t v) {
+  float f;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, l;\n}" : "=f"(f) : "r"(v));
+  return f;
 }
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
