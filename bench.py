@@ -421,6 +421,48 @@ def measure_square_rows(fa2, dev, stream, peaks, names=("stress", "b4h32n4096"))
     return out
 
 
+def measure_dq_modes(fa2, dev, stream, peaks, names=("stress", "long")):
+    """The three ways dQ can leave the backward main kernel (TMA bulk
+    reduce-add, fp32 vector atomics, per-tile partial slots plus a
+    fixed-order reduction), timed on the same inputs: the main kernel alone
+    and the whole backward pass (the three stages), 3 warm-up and 5 timed
+    runs each, CUDA events on the launching stream."""
+    out = {}
+    lib = fa2.load_library()
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        x = workloads.workload_inputs(w)
+        g = {k: t.to(dev) for k, t in x.items()}
+        B, H, N, d = w.B, w.H, w.N, w.d
+        o, lse = fa2.fa2_fwd(g["q"], g["k"], g["v"], causal=True, stream=stream)
+        Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+        row = {"workload": f"{name}: B={B} H={H} N={N} d={d} causal"}
+        bf = w.bwd_flops(True)
+        for mode, label in ((0, "tma_reduce_add"), (1, "atomics_red_v4"), (2, "split_accumulate")):
+            if mode == 2:
+                buf = torch.empty(lib.fa2_bwd_dq_partials_bytes(B, H, N, d, 1) // 4, dtype=torch.float32, device=dev)
+            else:
+                buf = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            mains, totals = [], []
+            for it in range(8):
+                fa2.fa2_bwd_stages(g["q"], g["k"], g["v"], o, g["dO"], lse, Dvec, buf, dq, dk, dv, w.scale, True,
+                                   stream, hook=lambda j: ev[j].record(stream), dq_mode=mode)
+                torch.cuda.synchronize()
+                if it >= 3:
+                    mains.append(ev[1].elapsed_time(ev[2]))
+                    totals.append(ev[0].elapsed_time(ev[3]))
+            m, t = statistics.median(mains), statistics.median(totals)
+            row[label] = {"main_ms": m, "bwd_ms": t, "main_tflops": bf / (m * 1e-3) / 1e12,
+                          "bwd_tflops": bf / (t * 1e-3) / 1e12,
+                          "dq_buffer_bytes": buf.numel() * buf.element_size()}
+            del buf
+        out[name] = row
+        del g, o, lse, Dvec, dq, dk, dv
+    return out
+
+
 def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
     """Microseconds per forward + backward step on the small workloads, where
     launch work rather than the GPU sets the time: 200 steps enqueued back to
@@ -635,7 +677,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the GQA / decoding / varlen measurements")
-    ap.add_argument("--row", choices=["gqa", "decode", "varlen", "stress", "n4096", "latency"],
+    ap.add_argument("--row", choices=["gqa", "decode", "varlen", "stress", "n4096", "latency", "dqmodes"],
                     help="measure only this widened row and print it (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -650,7 +692,13 @@ def main():
         _build.build()
         dev = torch.device("cuda:0")
         stream = torch.cuda.Stream(device=dev)
-        print(json.dumps({"row": args.row, **measure_rows(fa2, dev, stream, _peaks(), only=args.row)}), flush=True)
+        if args.row == "dqmodes":
+            res = measure_dq_modes(fa2, dev, stream, _peaks())
+            torch.cuda.synchronize()
+            res["device_status"] = fa2.fa2_device_status(reset=True)
+        else:
+            res = measure_rows(fa2, dev, stream, _peaks(), only=args.row)
+        print(json.dumps({"row": args.row, **res}), flush=True)
         return 0
     return run_gpu(args, w, causal)
 

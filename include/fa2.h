@@ -207,8 +207,9 @@ int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const
  * on one stream is exactly fa2_bwd_ws.
  *
  * fa2_bwd_preprocess: Dvec[r] = sum_c dO[r,c] * o[r,c] (fp32 [B,H,N]) and
- *   dq_acc (fp32 [B,H,N,d], 16-byte aligned) set to zero.  The D identity is
- *   the standard FA2 backward identity (the pages do not state it).
+ *   dq_acc (fp32 [B,H,N,d], 16-byte aligned) set to zero; dq_acc may be NULL
+ *   (D only, for FA2_DQ_SPLIT below).  The D identity is the standard FA2
+ *   backward identity (the pages do not state it).
  * fa2_bwd_main: recomputes P from q, k and lse tile by tile (the article's
  *   backward-pass bullet), writes dk and dv (bf16) and ADDS the unscaled
  *   dS K into dq_acc with fp32 reduce-adds performed in L2 (TMA bulk
@@ -225,6 +226,46 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
                  float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                  void* stream);
 int fa2_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale, void* stream);
+
+/*
+ * How dQ leaves the main backward kernel (the pages name atomic reductions
+ * as a rounding source, section "Numerical Stability and Loss Drift"; the
+ * choice among these was made by measurement):
+ *   FA2_DQ_REDUCE (0): each (query tile, key tile) partial is reduce-added in
+ *     fp32 into the zeroed accumulator by TMA (cp.reduce.async.bulk): the
+ *     default of fa2_bwd / fa2_bwd_ws / fa2_bwd_main;
+ *   FA2_DQ_ATOMIC (1): the same sums by fp32 vector atomics
+ *     (red.global.add.v4.f32) from registers;
+ *   FA2_DQ_SPLIT (2): each partial is stored to its own slot and
+ *     fa2_bwd_dq_reduce sums the slots in a fixed order (deterministic).
+ * fa2_bwd_main_dq is fa2_bwd_main with the mode chosen (modes 1 and 2: d =
+ * 128 only, else FA2_ERR_HEADDIM; an unknown mode gives FA2_ERR_SHAPE).
+ * dq_buf: the zeroed fp32 accumulator [B,H,N,d] (modes 0 and 1), or
+ * fa2_bwd_dq_partials_bytes(B, H, N, d, causal) bytes of partial slots
+ * (mode 2; 0 for invalid sizes or d != 128), 16-byte aligned.
+ * fa2_bwd_dq_reduce: dq (bf16 [B,H,N,d]) = scale * sum of the slots.
+ */
+enum { FA2_DQ_REDUCE = 0, FA2_DQ_ATOMIC = 1, FA2_DQ_SPLIT = 2 };
+int fa2_bwd_main_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
+                    float* dq_buf, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int dq_mode,
+                    void* stream);
+size_t fa2_bwd_dq_partials_bytes(int B, int H, int N, int d, int causal);
+int fa2_bwd_dq_reduce(const float* dq_part, void* dq, int B, int H, int N, int d, float scale, int causal,
+                      void* stream);
+
+/*
+ * Deterministic backward pass (d = 128): the same results as fa2_bwd except
+ * that dQ is summed over key tiles in a fixed order (FA2_DQ_SPLIT), so every
+ * output is bitwise reproducible run to run.  Caller-owned workspace of
+ * fa2_bwd_deterministic_workspace_bytes(B, H, N, d, causal) bytes (256-byte
+ * aligned): D plus one 128 x d fp32 slot per (query tile, key tile) pair,
+ * i.e. B H (N/128)(N/128 + 1)/2 x 64 KB causal -- gigabytes at N = 16384.
+ * Three launches (D, main, ordered reduction).  Other rules as fa2_bwd_ws.
+ */
+size_t fa2_bwd_deterministic_workspace_bytes(int B, int H, int N, int d, int causal);
+int fa2_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                          void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa2_bwd without any device allocation.  The pages describe no such call; it

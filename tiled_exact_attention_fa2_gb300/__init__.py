@@ -48,6 +48,12 @@ _SIGNATURES = {
     "fa2_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "fa2_bwd_main": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "fa2_bwd_main_dq": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "fa2_bwd_dq_partials_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "fa2_bwd_dq_reduce": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa2_bwd_deterministic_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "fa2_bwd_deterministic": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz,
+                                   _vp]),
     "fa2_last_error_detail": (ctypes.c_char_p, []),
     "fa2_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_noalloc_scratch_capacity": (_sz, []),
@@ -403,8 +409,29 @@ def fa2_bwd_noalloc(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, scale: Optio
     return dq, dk, dv
 
 
+FA2_DQ_REDUCE, FA2_DQ_ATOMIC, FA2_DQ_SPLIT = 0, 1, 2
+
+
+def fa2_bwd_deterministic(q, k, v, o, dO, lse, dq=None, dk=None, dv=None, workspace=None,
+                          scale: Optional[float] = None, causal: bool = True, stream=None):
+    """Bitwise-reproducible backward (d = 128): dQ summed over key tiles in a
+    fixed order.  ``workspace`` (CUDA byte tensor) is allocated here when not given."""
+    lib = load_library()
+    (B, H, N, d), dq, dk, dv = _bwd_common(q, k, v, o, dO, lse, dq, dk, dv)
+    need = lib.fa2_bwd_deterministic_workspace_bytes(B, H, N, d, 1 if causal else 0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.fa2_bwd_deterministic(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                   _scale(scale, d), 1 if causal else 0, workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error("fa2_bwd_deterministic", rc)
+    return dq, dk, dv
+
+
 def fa2_bwd_stages(q, k, v, o, dO, lse, Dvec, dq_acc, dq, dk, dv, scale: Optional[float] = None,
-                   causal: bool = True, stream=None, hook=None):
+                   causal: bool = True, stream=None, hook=None, dq_mode: int = FA2_DQ_REDUCE):
     """fa2_bwd_ws as its three C-ABI stages; ``hook(i)`` is called before stage i
     (0: preprocess, 1: main, 2: dQ convert) and with i = 3 after the last, so a
     caller can record CUDA events between them."""
@@ -413,17 +440,22 @@ def fa2_bwd_stages(q, k, v, o, dO, lse, Dvec, dq_acc, dq, dk, dv, scale: Optiona
     sc, st = _scale(scale, d), _stream(stream, q.device)
     hook = hook or (lambda i: None)
     hook(0)
-    rc = lib.fa2_bwd_preprocess(o.data_ptr(), dO.data_ptr(), Dvec.data_ptr(), dq_acc.data_ptr(), B, H, N, d, st)
+    # (split mode: D only, the partial slots are written whole)
+    acc0 = None if dq_mode == FA2_DQ_SPLIT else dq_acc.data_ptr()
+    rc = lib.fa2_bwd_preprocess(o.data_ptr(), dO.data_ptr(), Dvec.data_ptr(), acc0, B, H, N, d, st)
     if rc != FA2_OK:
         raise FA2Error("fa2_bwd_preprocess", rc)
     hook(1)
-    rc = lib.fa2_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
-                          Dvec.data_ptr(), dq_acc.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, sc,
-                          1 if causal else 0, st)
+    rc = lib.fa2_bwd_main_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                             Dvec.data_ptr(), dq_acc.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, sc,
+                             1 if causal else 0, dq_mode, st)
     if rc != FA2_OK:
-        raise FA2Error("fa2_bwd_main", rc)
+        raise FA2Error("fa2_bwd_main_dq", rc)
     hook(2)
-    rc = lib.fa2_bwd_dq_convert(dq_acc.data_ptr(), dq.data_ptr(), B, H, N, d, sc, st)
+    if dq_mode == FA2_DQ_SPLIT:
+        rc = lib.fa2_bwd_dq_reduce(dq_acc.data_ptr(), dq.data_ptr(), B, H, N, d, sc, 1 if causal else 0, st)
+    else:
+        rc = lib.fa2_bwd_dq_convert(dq_acc.data_ptr(), dq.data_ptr(), B, H, N, d, sc, st)
     if rc != FA2_OK:
         raise FA2Error("fa2_bwd_dq_convert", rc)
     hook(3)

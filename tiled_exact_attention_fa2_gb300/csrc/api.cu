@@ -493,12 +493,12 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const vo
 
 int fa2_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc, int B, int H, int N, int d,
                        void* stream) {
-  if (!o || !dO || !Dvec || !dq_acc) return FA2_ERR_NULL;
+  if (!o || !dO || !Dvec) return FA2_ERR_NULL;  // dq_acc == NULL: D only
   if (int rc = check_sizes(B, H, N, d)) return rc;
   if (!aligned(o, 16) || !aligned(dO, 16) || !aligned(Dvec, 4) || !aligned(dq_acc, 16)) return FA2_ERR_ALIGN;
   const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
   const Range rd = range_of(Dvec, static_cast<size_t>(B) * H * N * 4);
-  const Range ra = range_of(dq_acc, static_cast<size_t>(B) * H * N * d * 4);
+  const Range ra = range_of(dq_acc, dq_acc ? static_cast<size_t>(B) * H * N * d * 4 : 0);
   const Range ins[] = {range_of(o, tb), range_of(dO, tb)};
   for (const Range& r : ins)
     if (overlap(rd, r) || overlap(ra, r)) return FA2_ERR_ALIAS;
@@ -508,19 +508,30 @@ int fa2_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_acc
   return FA2_OK;
 }
 
-int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
-                 float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
-                 void* stream) {
-  if (!q || !k || !v || !dO || !lse || !Dvec || !dq_acc || !dk || !dv) return FA2_ERR_NULL;
+}  // extern "C" (reopened below)
+
+namespace {
+
+// The main backward kernel as a stage: dq_buf is the zeroed fp32 accumulator
+// [B, H, N, d] (kDqReduce, kDqAtomic) or the partial slots of
+// fa2_bwd_dq_partials_bytes bytes (kDqSplit).
+int bwd_main_stage(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
+                   float* dq_buf, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int dq_mode,
+                   cudaStream_t st) {
+  if (!q || !k || !v || !dO || !lse || !Dvec || !dq_buf || !dk || !dv) return FA2_ERR_NULL;
   if (int rc = check_sizes(B, H, N, d)) return rc;
   if (int rc = check_scale(scale)) return rc;
+  if (dq_mode != kDqReduce && dq_mode != kDqAtomic && dq_mode != kDqSplit) return FA2_ERR_SHAPE;
+  if (dq_mode != kDqReduce && d != 128) return FA2_ERR_HEADDIM;
   const void* bf[] = {q, k, v, dO, dk, dv};
   for (const void* p : bf)
     if (!aligned(p, 16)) return FA2_ERR_ALIGN;
-  if (!aligned(lse, 4) || !aligned(Dvec, 4) || !aligned(dq_acc, 16)) return FA2_ERR_ALIGN;
+  if (!aligned(lse, 4) || !aligned(Dvec, 4) || !aligned(dq_buf, 16)) return FA2_ERR_ALIGN;
   const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
   const size_t lb = static_cast<size_t>(B) * H * N * 4;
-  const Range outs[] = {range_of(dk, tb), range_of(dv, tb), range_of(dq_acc, tb * 2)};
+  const long long pairs = bwd_dq_pairs(B * H, N, causal != 0);
+  const size_t qb = dq_mode == kDqSplit ? static_cast<size_t>(pairs) * kRowsPerTile * d * 4 : tb * 2;
+  const Range outs[] = {range_of(dk, tb), range_of(dv, tb), range_of(dq_buf, qb)};
   const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(dO, tb), range_of(lse, lb),
                        range_of(Dvec, lb)};
   for (int a = 0; a < 3; ++a) {
@@ -530,7 +541,11 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
       if (overlap(outs[a], outs[b])) return FA2_ERR_ALIAS;
   }
   TmapSet tm;
-  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, B * H, B * H, N, d)) return rc;
+  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_buf, B * H, B * H, N, d)) return rc;
+  if (dq_mode == kDqSplit &&
+      !encode_rows(&tm.dqacc, dq_buf, Elem::kF32, static_cast<int>(pairs), kRowsPerTile, d, d,
+                   static_cast<long long>(kRowsPerTile) * d))
+    return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
   BwdProblem p{};
   p.lse = lse;
   p.Dvec = Dvec;
@@ -539,8 +554,71 @@ int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, co
   p.BH = B * H;
   p.N = N;
   p.group = 1;
-  if (int e = launch_bwd_main(tm, p, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
-    return cuda_fail(e, "bwd main launch");
+  p.dq_mode = dq_mode;
+  p.dq_buf = dq_buf;
+  if (int e = launch_bwd_main(tm, p, d, scale, causal != 0, st)) return cuda_fail(e, "bwd main launch");
+  return FA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa2_bwd_main(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
+                 float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                 void* stream) {
+  return bwd_main_stage(q, k, v, dO, lse, Dvec, dq_acc, dk, dv, B, H, N, d, scale, causal, kDqReduce,
+                        static_cast<cudaStream_t>(stream));
+}
+
+size_t fa2_bwd_dq_partials_bytes(int B, int H, int N, int d, int causal) {
+  if (check_sizes(B, H, N, d) != FA2_OK || d != 128) return 0;
+  return static_cast<size_t>(bwd_dq_pairs(B * H, N, causal != 0)) * kRowsPerTile * d * sizeof(float);
+}
+
+int fa2_bwd_main_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* Dvec,
+                    float* dq_buf, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int dq_mode,
+                    void* stream) {
+  return bwd_main_stage(q, k, v, dO, lse, Dvec, dq_buf, dk, dv, B, H, N, d, scale, causal, dq_mode,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int fa2_bwd_dq_reduce(const float* dq_part, void* dq, int B, int H, int N, int d, float scale, int causal,
+                      void* stream) {
+  if (!dq_part || !dq) return FA2_ERR_NULL;
+  if (int rc = check_sizes(B, H, N, d)) return rc;
+  if (d != 128) return FA2_ERR_HEADDIM;
+  if (int rc = check_scale(scale)) return rc;
+  if (!aligned(dq_part, 16) || !aligned(dq, 16)) return FA2_ERR_ALIGN;
+  const size_t pb = fa2_bwd_dq_partials_bytes(B, H, N, d, causal);
+  if (overlap(range_of(dq_part, pb), range_of(dq, static_cast<size_t>(B) * H * N * d * 2))) return FA2_ERR_ALIAS;
+  if (int e = launch_bwd_dq_reduce(dq_part, dq, B * H, N, d, scale, causal != 0, static_cast<cudaStream_t>(stream)))
+    return cuda_fail(e, "dq reduce launch");
+  return FA2_OK;
+}
+
+size_t fa2_bwd_deterministic_workspace_bytes(int B, int H, int N, int d, int causal) {
+  const size_t pb = fa2_bwd_dq_partials_bytes(B, H, N, d, causal);
+  if (pb == 0) return 0;
+  return round_up(static_cast<size_t>(B) * H * N * sizeof(float)) + round_up(pb);
+}
+
+int fa2_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                          void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                          void* workspace, size_t workspace_bytes_given, void* stream) {
+  if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d, scale)) return rc;
+  if (d != 128) return FA2_ERR_HEADDIM;
+  const size_t need = fa2_bwd_deterministic_workspace_bytes(B, H, N, d, causal);
+  if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < need) return FA2_ERR_WORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* Dvec = static_cast<float*>(workspace);
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         round_up(static_cast<size_t>(B) * H * N * sizeof(float)));
+  // D only: the partial slots are written whole, nothing to zero.
+  if (int e = launch_bwd_preprocess(o, dO, Dvec, nullptr, B * H, N, d, st)) return cuda_fail(e, "bwd preprocess launch");
+  if (int rc = bwd_main_stage(q, k, v, dO, lse, Dvec, part, dk, dv, B, H, N, d, scale, causal, kDqSplit, st))
+    return rc;
+  if (int e = launch_bwd_dq_reduce(part, dq, B * H, N, d, scale, causal != 0, st)) return cuda_fail(e, "dq reduce launch");
   return FA2_OK;
 }
 

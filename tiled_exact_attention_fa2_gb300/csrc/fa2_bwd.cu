@@ -77,11 +77,13 @@ enum BwdBar {
   kNumBwdBars = 23,
 };
 
-template <int D>
+template <int D, int DQM = kDqReduce>
 struct BwdCfg {
   using T = HeadDim<D>;
   static constexpr int kQStages = 2;
-  static constexpr int kDoStages = D == 128 ? 1 : 2;  // shared memory is full at D = 128
+  // Shared memory is full at D = 128 with the dQ staging buffers; without
+  // them (atomics) dO gets its second stage back.
+  static constexpr int kDoStages = (D == 128 && DQM != kDqAtomic) ? 1 : 2;
   // TMEM: S^T [0,128) (P^T, as bf16 pairs, overwrites columns [0,32) and
   // [64,96): each P/dS warpgroup writes inside its own half),
   // dP^T [128,256) (dQ_i reuses these columns once dS^T is formed), dV and dK
@@ -98,7 +100,7 @@ struct BwdCfg {
   // accumulator by TMA.
   static constexpr int kChunk = D < 32 ? D : 32;
   static constexpr int kChunks = D / kChunk;
-  static constexpr int kStageBytes = 128 * kChunk * 4;
+  static constexpr int kStageBytes = DQM == kDqAtomic ? 0 : 128 * kChunk * 4;
   static constexpr int kDSt = kDo + kDoStages * T::kTileBytes;
   static constexpr int kStage = kDSt + Square::kTileBytes;
   // Per Q stage: -LSE_i * log2 e [128] then -D_i [128] (fp32), written by
@@ -145,7 +147,9 @@ __global__ void __launch_bounds__(256) fa2_bwd_preprocess_kernel(const __nv_bflo
   for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && sub == 0) Dvec[row] = acc;
 
-  // Zero dQacc (rows * D fp32) with 16-byte stores, grid-stride.
+  // Zero dQacc (rows * D fp32) with 16-byte stores, grid-stride (none when
+  // dQ leaves as per-tile partials).
+  if (dq_acc == nullptr) return;
   const long long n4 = rows * D / 4;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   float4* acc4 = reinterpret_cast<float4*>(dq_acc);
@@ -172,13 +176,13 @@ __global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __rest
 // ---------------------------------------------------------------- main
 // VARLEN = true: packed variable-length batch (per-sequence lengths from
 // p.cu_q / p.cu_k); otherwise the square [B * H, N, d] problem.
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, int DQM>
 __global__ void __launch_bounds__(512, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_dqacc, const BwdProblem p, float scale, float scale_log2) {
   using T = HeadDim<D>;
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, DQM>;
   const float* __restrict__ lse = p.lse;
   const float* __restrict__ Dvec = p.Dvec;
   __nv_bfloat16* __restrict__ dk = static_cast<__nv_bfloat16*>(p.dk);
@@ -535,10 +539,38 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
 #pragma unroll 1
     for (int it = 0; it < n_iter; ++it) {
-      const int q0 = (i_begin + it % n_q) * kTileRows;
+      const int i = i_begin + it % n_q;
+      const int q0 = i * kTileRows;
       const int bh = bh_kv * group + it / n_q;
       if (!(ok = mbar_wait_sleep(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
+      if constexpr (DQM == kDqAtomic) {
+        // fp32 atomics straight from registers: two 32-column pieces at a
+        // time, the TMEM columns released right after the last read.
+        const int q_row = q0 + t;
+        float* dst = p.dq_buf + (static_cast<size_t>(bh) * Nq + (q_row < Nq ? q_row : 0)) * D;
+        float g2[2][32];
+#pragma unroll
+        for (int h2 = 0; h2 < D / 64; ++h2) {
+          tmem_ld32(tmem + lane_base + C::kColDQ + 64 * h2, g2[0]);
+          tmem_ld32(tmem + lane_base + C::kColDQ + 64 * h2 + 32, g2[1]);
+          tmem_wait_ld();
+          if (h2 == D / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+          }
+          if (q_row < Nq) {
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                red_add_v4(dst + 64 * h2 + 32 * pc + 4 * j, g2[pc][4 * j], g2[pc][4 * j + 1], g2[pc][4 * j + 2],
+                           g2[pc][4 * j + 3]);
+          }
+        }
+        continue;
+      }
       // The first three pieces are read from TMEM at once (96 registers),
       // the fourth as soon as the first is staged, and the columns are
       // released right after that read: dP^T(i+1) reuses them, so only one
@@ -584,7 +616,16 @@ __global__ void __launch_bounds__(512, 1)
         if (lane == 0) mbar_arrive(&bars[kBarStageFull + bsel]);
         if (issuer) {
           if ((ok = mbar_wait(&bars[kBarStageFull + bsel], u & 1, status))) {
-            tma_reduce_add_3d(&tm_dqacc, sb, c * C::kChunk, q_base + q0, bh);
+            if constexpr (DQM == kDqSplit) {
+              // this (query tile, key tile) pair's own partial slot
+              const int nq_t = num_q_tiles;
+              const long long pair = CAUSAL ? static_cast<long long>(bh) * nq_t * (nq_t + 1) / 2 +
+                                                  static_cast<long long>(i) * (i + 1) / 2 + jt
+                                            : (static_cast<long long>(bh) * nq_t + i) * kv_tiles_grid + jt;
+              tma_store_3d(&tm_dqacc, sb, c * C::kChunk, 0, static_cast<int>(pair));
+            } else {
+              tma_reduce_add_3d(&tm_dqacc, sb, c * C::kChunk, q_base + q0, bh);
+            }
             bulk_commit_group();
             // The previous chunk's reduce (other buffer) has read its source
             // once at most this one is still pending: release that buffer.
@@ -599,7 +640,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       if (!ok) break;
     }
-    if (issuer) bulk_wait_group0();  // every reduce has landed before the CTA exits
+    if (issuer) bulk_wait_group0();  // every reduce / store has landed before the CTA exits
     // ------------------------------------------------------------ epilogue: dV, dK * scale -> bf16
     if (ok && mbar_wait_sleep(&bars[kBarAccFull], 0, status)) {
       tc_fence_after();
@@ -663,11 +704,11 @@ int launch_preprocess_t(const void* o, const void* dO, float* Dvec, float* dq_ac
                     static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc, rows);
 }
 
-template <int D, bool CAUSAL>
-int launch_bwd_main_t(const TmapSet& tm, BwdProblem p, float scale, cudaStream_t stream) {
-  using C = BwdCfg<D>;
-  const bool varlen = p.cu_q != nullptr;
-  auto kern = varlen ? fa2_bwd_kernel<D, CAUSAL, true> : fa2_bwd_kernel<D, CAUSAL, false>;
+template <int D, bool CAUSAL, bool VARLEN, int DQM>
+int launch_bwd_main_k(const TmapSet& tm, BwdProblem p, float scale, cudaStream_t stream) {
+  using C = BwdCfg<D, DQM>;
+  const bool varlen = VARLEN;
+  auto kern = fa2_bwd_kernel<D, CAUSAL, VARLEN, DQM>;
   if (int rc = ensure_max_smem(reinterpret_cast<const void*>(kern), C::kBytes)) return rc;
   const int rows_q = varlen ? p.max_q : p.N;
   const int num_kv_tiles = ((varlen ? p.max_k : p.N) + kTileRows - 1) / kTileRows;
@@ -680,6 +721,53 @@ int launch_bwd_main_t(const TmapSet& tm, BwdProblem p, float scale, cudaStream_t
   p.heads_per_group = heads_per_l2_group(per_head, kv_heads);
   return launch_pdl(kern, grid, dim3(kBwdThreads), C::kBytes, stream, tm.q, tm.k, tm.v, tm.dO, tm.dqacc, p, scale,
                     scale * kLog2e);
+}
+
+// The atomic and split dQ modes are compiled for d = 128 square problems only.
+template <int D, bool CAUSAL>
+int launch_bwd_main_t(const TmapSet& tm, const BwdProblem& p, float scale, cudaStream_t stream) {
+  if (p.cu_q != nullptr) {
+    if (p.dq_mode != kDqReduce) return static_cast<int>(cudaErrorInvalidValue);
+    return launch_bwd_main_k<D, CAUSAL, true, kDqReduce>(tm, p, scale, stream);
+  }
+  if constexpr (D == 128) {
+    if (p.dq_mode == kDqAtomic) return launch_bwd_main_k<D, CAUSAL, false, kDqAtomic>(tm, p, scale, stream);
+    if (p.dq_mode == kDqSplit) return launch_bwd_main_k<D, CAUSAL, false, kDqSplit>(tm, p, scale, stream);
+  }
+  if (p.dq_mode != kDqReduce) return static_cast<int>(cudaErrorInvalidValue);
+  return launch_bwd_main_k<D, CAUSAL, false, kDqReduce>(tm, p, scale, stream);
+}
+
+// dQ = bf16(scale * sum over key tiles jt, in increasing jt, of the partial
+// of (query tile, jt)); thread = 8 columns of one row.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256) fa2_dq_reduce_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ dq,
+                                                            int BH, int N, float scale) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int kTpr = D / 8;
+  const int nq = (N + kTileRows - 1) / kTileRows;
+  const long long total = static_cast<long long>(BH) * N * kTpr;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+    const int c8 = static_cast<int>(e % kTpr);
+    const long long row = e / kTpr;  // bh * N + n
+    const int bh = static_cast<int>(row / N), n = static_cast<int>(row % N);
+    const int i = n / kTileRows, r = n % kTileRows;
+    const long long first = CAUSAL ? static_cast<long long>(bh) * nq * (nq + 1) / 2 + static_cast<long long>(i) * (i + 1) / 2
+                                   : (static_cast<long long>(bh) * nq + i) * nq;
+    const int count = CAUSAL ? i + 1 : nq;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int jt = 0; jt < count; ++jt) {
+      const float4* src = reinterpret_cast<const float4*>(part + ((first + jt) * kTileRows + r) * D + c8 * 8);
+      const float4 a = __ldg(src), b = __ldg(src + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    reinterpret_cast<uint4*>(dq + row * D + c8 * 8)[0] =
+        make_uint4(pack_bf16x2(acc[0] * scale, acc[1] * scale), pack_bf16x2(acc[2] * scale, acc[3] * scale),
+                   pack_bf16x2(acc[4] * scale, acc[5] * scale), pack_bf16x2(acc[6] * scale, acc[7] * scale));
+  }
 }
 
 int launch_dq_convert(const float* dq_acc, void* dq, long long elems, float scale, cudaStream_t stream) {
@@ -714,6 +802,22 @@ int launch_bwd_main(const TmapSet& tm, const BwdProblem& p, int d, float scale, 
       return causal ? launch_bwd_main_t<128, true>(tm, p, scale, stream) : launch_bwd_main_t<128, false>(tm, p, scale, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
+}
+
+long long bwd_dq_pairs(int BH, int N, bool causal) {
+  const long long nq = (static_cast<long long>(N) + kTileRows - 1) / kTileRows;
+  return causal ? BH * (nq * (nq + 1) / 2) : BH * nq * nq;
+}
+
+int launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, float scale, bool causal,
+                         cudaStream_t stream) {
+  if (d != 128) return static_cast<int>(cudaErrorInvalidValue);
+  const long long threads = static_cast<long long>(BH) * N * (128 / 8);
+  long long blocks = (threads + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  auto kern = causal ? fa2_dq_reduce_kernel<128, true> : fa2_dq_reduce_kernel<128, false>;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, dq_part,
+                    static_cast<__nv_bfloat16*>(dq), BH, N, scale);
 }
 
 int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, float scale, cudaStream_t stream) {

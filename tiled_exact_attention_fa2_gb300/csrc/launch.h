@@ -110,6 +110,17 @@ int launch_bwd_preprocess(const void* o, const void* dO, float* Dvec, float* dq_
 // preprocess kernel's row order); sequence b owns query rows cu_q[b] ..
 // cu_q[b+1] - 1 and key rows cu_k[b] .. cu_k[b+1] - 1, at most max_q / max_k
 // of each; causal: query i sees key j iff j <= i + Lk - Lq.
+//
+// dQ leaves the main kernel in one of three ways (dq_mode): kDqReduce, TMA
+// bulk reduce-add of each query tile's fp32 partial into the zeroed
+// accumulator (tm.dqacc); kDqAtomic, fp32 vector atomics (red.global.add)
+// from registers into dq_buf, the zeroed accumulator [B*H, N, d]; kDqSplit,
+// TMA store of each (query tile, key tile) partial into its own 128 x d
+// slot of dq_buf (tm.dqacc describes [pairs, 128, d]), summed afterwards in
+// a fixed order by launch_bwd_dq_reduce (deterministic).  The last two exist
+// for d = 128 square problems only.
+enum DqMode : int { kDqReduce = 0, kDqAtomic = 1, kDqSplit = 2 };
+
 struct BwdProblem {
   const float* lse;
   const float* Dvec;
@@ -120,9 +131,16 @@ struct BwdProblem {
   const int* cu_q;
   const int* cu_k;
   int batches, H, Hkv, total_q, total_k, max_q, max_k;
+  int dq_mode;
+  float* dq_buf;
 };
 int launch_bwd_main(const TmapSet& tm, const BwdProblem& p, int d, float scale, bool causal, cudaStream_t stream);
 int launch_bwd_dq_convert(const float* dq_acc, void* dq, int BH, int N, int d, float scale, cudaStream_t stream);
+// kDqSplit: number of (query tile, key tile) partial slots and the bf16 dQ
+// = scale * (sum over key tiles, in increasing order) of the partials.
+long long bwd_dq_pairs(int BH, int N, bool causal);
+int launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, float scale, bool causal,
+                         cudaStream_t stream);
 
 int read_fwd_status(int* value, bool reset);
 

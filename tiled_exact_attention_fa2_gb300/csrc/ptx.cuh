@@ -143,6 +143,22 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t sme
       "r"(smem_src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 3-D tiled TMA store (smem tile -> global), tracked by the issuing thread's
+// bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t smem_src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Four fp32 adds into global memory, performed at L2 (no return value).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The bulk ops of this thread have finished reading their shared-memory source.
 __device__ __forceinline__ void bulk_wait_group_read0() {
