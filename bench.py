@@ -44,7 +44,11 @@ METRIC = "causal bf16 FA2 fwd / bwd TFLOPS and % of GB300 dense bf16 peak (1 GPU
 # kernel build whose device sources hash to the recorded digest; a figure
 # whose digest no longer matches the sources is reported as null.
 KERNEL_TRAFFIC = {
-    # (kernel, workload, causal): (read + write bytes, digest of the sources)
+    # (kernel, workload, causal): (read + write bytes, digest of the sources).
+    # Capture summarised in the DRAM-traffic profile of the long causal
+    # workload (dram__bytes_read.sum + dram__bytes_write.sum, one launch each).
+    ("fa2_fwd_kernel", "long", True): (405447936 + 115087360, "497c146894f62f6e"),
+    ("fa2_bwd_kernel", "long", True): (809664512 + 485897472, "8fd85d1274a4b3ea"),
 }
 
 KERNEL_SOURCES = {
@@ -543,7 +547,11 @@ def run_gpu(args, w, causal):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
     Dvec = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq_acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    if args.dq_mode == 2:  # per-tile partial slots
+        dq_acc = torch.empty(fa2.load_library().fa2_bwd_dq_partials_bytes(B, H, N, d, int(causal)) // 4,
+                             dtype=torch.float32, device=dev)
+    else:
+        dq_acc = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
     fws = torch.empty(fa2.fa2_fwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     scale = w.scale
@@ -557,7 +565,7 @@ def run_gpu(args, w, causal):
         e[0].record(stream)
         fa2.fa2_fwd_ws(g["q"], g["k"], g["v"], fws, o, lse, scale, causal, stream)
         fa2.fa2_bwd_stages(g["q"], g["k"], g["v"], o, g["dO"], lse, Dvec, dq_acc, dq, dk, dv, scale, causal,
-                           stream, hook=lambda j: e[j + 1].record(stream))
+                           stream, hook=lambda j: e[j + 1].record(stream), dq_mode=args.dq_mode)
 
     for i in range(args.warmup):
         step(i)
@@ -639,7 +647,9 @@ def run_gpu(args, w, causal):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{w.name}: B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'}",
                    "B": B, "H": H, "N": N, "d": d, "causal": causal, "parallelism": f"weak x{world} (heads)",
-                   "l2": "inputs larger than L2 (Q, K, V, dO 134 MB each), no flush"},
+                   "dq_reduction": ["tma_reduce_add", "atomics_red_v4", "split_accumulate"][args.dq_mode],
+                   "l2": (f"inputs larger than L2 (Q, K, V, dO {B * H * N * d * 2 / 1e6:.0f} MB each), no flush"
+                          if 4 * B * H * N * d * 2 > 129e6 else "inputs fit in L2 together; back-to-back steps")},
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "pct_of_peak_burst": 100 * fwd_tf / peaks["bf16_tflops"],
                 "pct_of_peak_sustained": 100 * fwd_tf / peaks["bf16_tflops_sustained"]},
         "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "pct_of_peak_burst": 100 * bwd_tf / peaks["bf16_tflops"],
@@ -677,6 +687,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the GQA / decoding / varlen measurements")
+    ap.add_argument("--dq-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="how dQ leaves the backward main kernel: 0 TMA reduce-add (default), 1 fp32 atomics, "
+                         "2 per-tile partials + ordered reduction (d = 128 only)")
     ap.add_argument("--row", choices=["gqa", "decode", "varlen", "stress", "n4096", "latency", "dqmodes"],
                     help="measure only this widened row and print it (for profiling)")
     args = ap.parse_args()

@@ -47,8 +47,51 @@ constexpr int kRowsPerTile = 128;
 // row; rows past `rows` read as zero and are dropped by reduce-adds.
 enum class Elem { kBf16, kF16, kF32 };
 
+// Recently encoded tensor maps.  A map is a pure function of the address and
+// the layout, so a cached one is exact for the same (address, layout); the
+// cache only saves the host time of encoding (a few per call, on the launch
+// path of small problems).
+struct TmapKey {
+  const void* base;
+  Elem type;
+  int heads, d;
+  long long rows, row_stride, head_stride;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && type == o.type && heads == o.heads && d == o.d && rows == o.rows &&
+           row_stride == o.row_stride && head_stride == o.head_stride;
+  }
+};
+constexpr int kTmapCacheSize = 64;
+std::mutex g_tmap_mu;
+TmapKey g_tmap_keys[kTmapCacheSize];
+CUtensorMap g_tmap_vals[kTmapCacheSize];
+int g_tmap_count = 0, g_tmap_next = 0;
+
+bool encode_rows_uncached(CUtensorMap* out, const void* base, Elem type, int heads, long long rows, int d,
+                          long long row_stride, long long head_stride);
+
 bool encode_rows(CUtensorMap* out, const void* base, Elem type, int heads, long long rows, int d,
                  long long row_stride, long long head_stride) {
+  const TmapKey key{base, type, heads, d, rows, row_stride, head_stride};
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    for (int i = 0; i < g_tmap_count; ++i)
+      if (g_tmap_keys[i] == key) {
+        *out = g_tmap_vals[i];
+        return true;
+      }
+  }
+  if (!encode_rows_uncached(out, base, type, heads, rows, d, row_stride, head_stride)) return false;
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  g_tmap_keys[g_tmap_next] = key;
+  g_tmap_vals[g_tmap_next] = *out;
+  g_tmap_next = (g_tmap_next + 1) % kTmapCacheSize;
+  if (g_tmap_count < kTmapCacheSize) ++g_tmap_count;
+  return true;
+}
+
+bool encode_rows_uncached(CUtensorMap* out, const void* base, Elem type, int heads, long long rows, int d,
+                          long long row_stride, long long head_stride) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const bool f32 = type == Elem::kF32;

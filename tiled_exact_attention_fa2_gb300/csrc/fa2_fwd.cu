@@ -36,8 +36,8 @@
 // completed, because it overwrites the columns that MMA reads (decoding,
 // where tile B is empty, double-buffers S over both ranges instead).
 // The reference value m that the exponentials subtract is raised only when a
-// tile's row max exceeds it by more than kRescaleSlack (log2 units), so the
-// weights stay below 2^kRescaleSlack and O is rescaled in TMEM (for the whole
+// tile's row max exceeds it by more than a slack (15 or 8 log2 units), so the
+// weights stay below 2^slack and O is rescaled in TMEM (for the whole
 // warp) only on those rare tiles; softmax warps w and w + 4, which share an
 // SMSP, take turns at the exponentials.  The softmax arithmetic runs on
 // packed fp32 pairs (f32x2 FMA/ADD/MUL) and 3-input max to halve its
@@ -62,10 +62,14 @@ constexpr int kFwdThreads = 352;
 constexpr int kSchedReaders = 11;
 constexpr uint32_t kTmemCols = 512;
 // A row's reference max is raised only when a tile's max exceeds it by more
-// than this (log2 units): weights 2^(s - m) then stay below 2^8, well inside
-// fp16 (65504), bf16 and fp32 range, and the result is the same softmax up to
-// rounding.
-constexpr float kRescaleSlack = 8.f;
+// than the slack (log2 units): weights 2^(s - m) then stay below 2^slack,
+// inside fp16 (65504 > 2^15) and fp32 range, and the result is the same
+// softmax up to rounding.  fp16 weights keep their 11 significant bits at
+// any magnitude, so their slack is the widest fp16 allows (fewer O rescales
+// on sharply peaked rows: +1.5 % on the large-logit stress workload, same
+// error); bf16 weights (split-KV form) keep 8, beyond which a row's weight
+// drifts into weights whose bf16 rounding the normaliser does not see.
+constexpr float kRescaleSlackF16 = 15.f, kRescaleSlackBf16 = 8.f;
 
 enum FwdBar {
   kBarQFull = 0,    // +tile (A, B)
@@ -545,7 +549,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // Raise m to this tile's max only when that exceeds it by more than
         // the slack (always on the first tile that sees a key).
         const float mt = mx * scale_log2;
-        const bool grow = mt > m + kRescaleSlack;
+        const bool grow = mt > m + (kF16 ? kRescaleSlackF16 : kRescaleSlackBf16);
         const float m_new = grow ? mt : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // (no key seen yet)
         const float alpha = ex2_approx(m - m_use);
