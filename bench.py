@@ -37,6 +37,9 @@ import torch  # noqa: E402
 
 import workloads  # noqa: E402
 
+# One step: fa2_v_to_f16_kernel, fa2_v_scale_kernel, fa2_fwd_kernel, then the
+# backward's preprocess, main kernel and dQ conversion (or ordered reduction).
+LAUNCHES_PER_STEP = 6
 METRIC = "causal bf16 FA2 fwd / bwd TFLOPS and % of GB300 dense bf16 peak (1 GPU)"
 
 # DRAM bytes (read + write) per launch of a kernel on a workload, from one
@@ -173,15 +176,54 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _dist():
+def _dist(backend: str = "nccl"):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        else:
+            dist.init_process_group(backend)
     return world, rank, local
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def spawn_local_replicas(n: int, argv, script: str = None) -> int:
+    """Run ``python <script> <argv>`` as n local ranks, each with the
+    environment torchrun gives one rank of one node (RANK = LOCAL_RANK = i,
+    WORLD_SIZE = n, rendezvous on 127.0.0.1 at a free port), so rank i uses
+    cuda:i.  Waits for all of them; returns 0, else the first non-zero exit
+    code (the other ranks are then stopped, as torchrun does)."""
+    script = script or os.path.abspath(__file__)
+    port = str(_free_port())
+    procs = []
+    for i in range(n):
+        env = dict(os.environ, RANK=str(i), LOCAL_RANK=str(i), WORLD_SIZE=str(n), LOCAL_WORLD_SIZE=str(n),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=port)
+        procs.append(subprocess.Popen([sys.executable, script, *argv], env=env))
+    rc = 0
+    pending = list(procs)
+    while pending:
+        for p in list(pending):
+            r = p.poll()
+            if r is None:
+                continue
+            pending.remove(p)
+            if r != 0 and rc == 0:
+                rc = r
+                for q in pending:
+                    q.terminate()
+        time.sleep(0.05)
+    return rc
 
 
 def _barrier(world):
@@ -248,7 +290,7 @@ def cpu_baseline(w, causal):
 
 
 def run_reference(args, w, causal):
-    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     budget = 150.0 / max(1, args.steps + args.warmup)
@@ -262,7 +304,7 @@ def run_reference(args, w, causal):
         tot_t += t
     value = tot_flops / tot_t / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} "
@@ -470,7 +512,7 @@ def measure_dq_modes(fa2, dev, stream, peaks, names=("stress", "long")):
 def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
     """Microseconds per forward + backward step on the small workloads, where
     launch work rather than the GPU sets the time: 200 steps enqueued back to
-    back (fa2_fwd_ws + fa2_bwd_ws, 5 kernels each; device time per step from CUDA
+    back (fa2_fwd_ws + fa2_bwd_ws: 3 kernels each; device time per step from CUDA
     events, host time per step from the clock around the enqueue), and the
     same step replayed from a CUDA graph."""
     out = {}
@@ -520,7 +562,7 @@ def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
         graph_us = a.elapsed_time(b) / n * 1e3
         out[name] = {"workload": f"B={B} H={H} N={N} d={d} causal", "us_per_step": dev_us,
                      "host_enqueue_us_per_step": host_us, "graph_replay_us_per_step": graph_us,
-                     "launches_per_step": 5}
+                     "launches_per_step": 6}
         del graph, g, o, lse, dq, dk, dv, ws, fws
     return out
 
@@ -660,7 +702,7 @@ def run_gpu(args, w, causal):
         "roofline_other": rooflines["fa2_fwd_kernel" if dominant == "fa2_bwd_kernel" else "fa2_bwd_kernel"],
         "timing": {"fwd_ms": _stats(fwd_list), "bwd_main_ms": _stats(main_list),
                    "method": "CUDA events on the launching stream around each kernel of every timed step"},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "device_status": status,
         "clocks": clocks,
         "e2e": e2e,
@@ -697,6 +739,14 @@ def main():
         args.warmup = 3
     w = workloads.WORKLOADS[args.workload]
     causal = not args.noncausal
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # Not started by torchrun: start the args.gpus replicas here.
+        if args.impl == "ours":
+            if torch.cuda.device_count() < args.gpus:
+                sys.exit(f"--gpus {args.gpus}: only {torch.cuda.device_count()} GPU(s) visible")
+            from tiled_exact_attention_fa2_gb300 import _build
+            _build.build()
+        return spawn_local_replicas(args.gpus, sys.argv[1:])
     if args.impl == "reference":
         return run_reference(args, w, causal)
     if args.row:

@@ -9,6 +9,7 @@ it only needs a driver to run).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -53,8 +54,21 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if not force and up_to_date():
         return LIB_PATH
-    nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
+    # Several local ranks may start at once: one compiles, the others wait on
+    # the lock and then find the library current.
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return LIB_PATH
+            return _compile(verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _compile(verbose, extra_flags) -> str:
+    nvcc = _nvcc()
     srcs = _sources()
 
     def compile_one(src):
