@@ -513,8 +513,9 @@ def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
     """Microseconds per forward + backward step on the small workloads, where
     launch work rather than the GPU sets the time: 200 steps enqueued back to
     back (fa2_fwd_ws + fa2_bwd_ws: 3 kernels each; device time per step from CUDA
-    events, host time per step from the clock around the enqueue), and the
-    same step replayed from a CUDA graph."""
+    events, host time per step from the clock around the enqueue), the same
+    through prepared_step (arguments marshalled once), and the step replayed
+    from a CUDA graph."""
     out = {}
     for name in names:
         w = workloads.WORKLOADS[name]
@@ -532,19 +533,25 @@ def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
             fa2.fa2_fwd_ws(g["q"], g["k"], g["v"], fws, o, lse, w.scale, True, side)
             fa2.fa2_bwd_ws(g["q"], g["k"], g["v"], o, g["dO"], lse, ws, dq, dk, dv, w.scale, True, side)
 
+        prepared = fa2.prepared_step(g["q"], g["k"], g["v"], o, lse, g["dO"], dq, dk, dv, fws, ws, w.scale, True, side)
         n = 200
-        for _ in range(20):
-            step()
-        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(side)
-        t0 = time.perf_counter()
-        for _ in range(n):
-            step()
-        host_us = (time.perf_counter() - t0) / n * 1e6
-        b.record(side)
-        torch.cuda.synchronize()
-        dev_us = a.elapsed_time(b) / n * 1e3
+
+        def timed(fn):
+            for _ in range(20):
+                fn()
+            torch.cuda.synchronize()
+            a.record(side)
+            t0 = time.perf_counter()
+            for _ in range(n):
+                fn()
+            host = (time.perf_counter() - t0) / n * 1e6
+            b.record(side)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / n * 1e3, host
+
+        dev_us, host_us = timed(step)
+        prep_us, prep_host_us = timed(prepared)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
             with torch.cuda.graph(graph, stream=side):
@@ -561,9 +568,10 @@ def measure_latency_rows(fa2, dev, peaks, names=("tiny", "small")):
         torch.cuda.synchronize()
         graph_us = a.elapsed_time(b) / n * 1e3
         out[name] = {"workload": f"B={B} H={H} N={N} d={d} causal", "us_per_step": dev_us,
-                     "host_enqueue_us_per_step": host_us, "graph_replay_us_per_step": graph_us,
+                     "host_enqueue_us_per_step": host_us, "prepared_step_us": prep_us,
+                     "prepared_host_enqueue_us_per_step": prep_host_us, "graph_replay_us_per_step": graph_us,
                      "launches_per_step": 6}
-        del graph, g, o, lse, dq, dk, dv, ws, fws
+        del graph, prepared, g, o, lse, dq, dk, dv, ws, fws
     return out
 
 

@@ -23,7 +23,7 @@ __all__ = [
     "FA2Error", "load_library", "fa2_fwd", "fa2_fwd_ws", "fa2_fwd_workspace_bytes", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
     "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
     "fa2_bwd_stages", "fa2_bwd_noalloc", "fa2_fwd_gqa", "fa2_bwd_gqa", "fa2_fwd_splitkv",
-    "fa2_fwd_varlen", "fa2_bwd_varlen", "FA2_OK",
+    "fa2_fwd_varlen", "fa2_bwd_varlen", "prepared_step", "FA2_OK",
 ]
 
 FA2_OK = 0
@@ -231,6 +231,44 @@ def fa2_bwd_ws(q, k, v, o, dO, lse, workspace: torch.Tensor, dq=None, dk=None, d
     if rc != FA2_OK:
         raise FA2Error("fa2_bwd_ws", rc)
     return dq, dk, dv
+
+
+def prepared_step(q, k, v, o, lse, dO, dq, dk, dv, fwd_workspace: torch.Tensor, bwd_workspace: torch.Tensor,
+                  scale: Optional[float] = None, causal: bool = True, stream=None):
+    """A callable that enqueues fa2_fwd_ws then fa2_bwd_ws on fixed buffers.
+
+    Every argument is checked and converted to its C type once, here; each
+    call of the returned function makes the two C calls with those values
+    (which still validate their arguments).  For loops that run the same
+    small problem many times, where marshalling arguments in Python would
+    take as long as the kernels.  The tensors must stay alive (and in place)
+    for as long as the callable is used.
+    """
+    lib = load_library()
+    B, H, N, d = _shape(q, "q")
+    if _shape(k, "k") != (B, H, N, d) or _shape(v, "v") != (B, H, N, d):
+        raise ValueError("q, k and v must have the same shape")
+    _shape(o, "o")
+    _bwd_common(q, k, v, o, dO, lse, dq, dk, dv)
+    vp, ci, cf, cs = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sc, cz, st = cf(_scale(scale, d)), ci(1 if causal else 0), vp(_stream(stream, q.device))
+    dims = (ci(B), ci(H), ci(N), ci(d))
+    fargs = (vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(o.data_ptr()), vp(lse.data_ptr()), *dims,
+             sc, cz, vp(fwd_workspace.data_ptr()), cs(fwd_workspace.numel() * fwd_workspace.element_size()), st)
+    bargs = (vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(o.data_ptr()), vp(dO.data_ptr()),
+             vp(lse.data_ptr()), vp(dq.data_ptr()), vp(dk.data_ptr()), vp(dv.data_ptr()), *dims, sc, cz,
+             vp(bwd_workspace.data_ptr()), cs(bwd_workspace.numel() * bwd_workspace.element_size()), st)
+    fwd, bwd = lib.fa2_fwd_ws, lib.fa2_bwd_ws
+
+    def step():
+        rc = fwd(*fargs)
+        if rc != FA2_OK:
+            raise FA2Error("fa2_fwd_ws", rc)
+        rc = bwd(*bargs)
+        if rc != FA2_OK:
+            raise FA2Error("fa2_bwd_ws", rc)
+
+    return step
 
 
 def _gqa_shapes(q, k, v):

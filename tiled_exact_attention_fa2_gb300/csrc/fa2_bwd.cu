@@ -423,9 +423,21 @@ __global__ void __launch_bounds__(512, 1)
         // dQ_i = dS K (dS read as the MN-major view of dS^T); dK += dS^T Q_i
         if (!(ok = mbar_wait(&bars[kBarDsFull], it & 1, status))) break;
         tc_fence_after();
+        if constexpr (DQM == kDqAtomic) {
+          // dQ_i^T = K^T dS^T: the same two MN-major tiles with their roles
+          // swapped (D = 128, so both are 128 x 128 and the instruction
+          // descriptor is unchanged).  TMEM lane = head dimension, column =
+          // query row, so a warp's 32 lanes hold 32 consecutive elements of a
+          // dQ row.
+          static_assert(DQM != kDqAtomic || D == 128, "transposed dQ needs D = 128");
 #pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ss(tDQ, Square::mnmajor_desc(sDSt, kk), T::mnmajor_desc(sK, kk), kIdDQ, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kTileRows / 16; ++kk)
+            mma_bf16_ss(tDQ, T::mnmajor_desc(sK, kk), Square::mnmajor_desc(sDSt, kk), kIdDQ, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kTileRows / 16; ++kk)
+            mma_bf16_ss(tDQ, Square::mnmajor_desc(sDSt, kk), T::mnmajor_desc(sK, kk), kIdDQ, kk > 0 ? 1u : 0u);
+        }
         mma_commit(&bars[kBarDqFull]);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
@@ -477,15 +489,19 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld32(tmem + lane_base + C::kColS + col0, sv);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = col0 + e;
-          const uint64_t nl = *reinterpret_cast<const uint64_t*>(nlse2 + col);
-          const float2 xx = f2_unpack(ffma2(f2_pack(sv[e], sv[e + 1]), scale2, nl));
-          float p0 = ex2_approx(xx.x);
-          float p1 = ex2_approx(xx.y);
-          if (row_dead || col < first) p0 = 0.f;
-          if (row_dead || col + 1 < first) p1 = 0.f;
-          pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
+        for (int e = 0; e < 32; e += 4) {
+          // one 16-byte broadcast load of -LSE log2 e for four columns
+          const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(nlse2 + col0 + e);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = col0 + e + 2 * h;
+            const float2 xx = f2_unpack(ffma2(f2_pack(sv[e + 2 * h], sv[e + 2 * h + 1]), scale2, h ? nl.y : nl.x));
+            float p0 = ex2_approx(xx.x);
+            float p1 = ex2_approx(xx.y);
+            if (row_dead || col < first) p0 = 0.f;
+            if (row_dead || col + 1 < first) p1 = 0.f;
+            pk[16 * c + (e + 2 * h) / 2] = pack_bf16x2(p0, p1);
+          }
         }
         tmem_st16u(tmem + lane_base + C::kColS + 64 * hh + 16 * c, pk + 16 * c);
       }
@@ -507,11 +523,13 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint32_t w[4];
+          // -D for these eight columns: two 16-byte broadcast loads
+          const ulonglong2 nd01 = *reinterpret_cast<const ulonglong2*>(nd + col0 + e);
+          const ulonglong2 nd23 = *reinterpret_cast<const ulonglong2*>(nd + col0 + e + 4);
+          const uint64_t ndx[4] = {nd01.x, nd01.y, nd23.x, nd23.y};
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            const int col = col0 + e + 2 * x;
-            const uint64_t diff = fadd2(f2_pack(dp[e + 2 * x], dp[e + 2 * x + 1]),
-                                        *reinterpret_cast<const uint64_t*>(nd + col));
+            const uint64_t diff = fadd2(f2_pack(dp[e + 2 * x], dp[e + 2 * x + 1]), ndx[x]);
             const float2 pp = unpack_bf16x2(pk[16 * c + (e + 2 * x) / 2]);
             const float2 ds = f2_unpack(fmul2(f2_pack(pp.x, pp.y), diff));
             w[x] = pack_bf16x2(ds.x, ds.y);
@@ -545,28 +563,35 @@ __global__ void __launch_bounds__(512, 1)
       if (!(ok = mbar_wait_sleep(&bars[kBarDqFull], it & 1, status))) break;
       tc_fence_after();
       if constexpr (DQM == kDqAtomic) {
-        // fp32 atomics straight from registers: two 32-column pieces at a
-        // time, the TMEM columns released right after the last read.
-        const int q_row = q0 + t;
-        float* dst = p.dq_buf + (static_cast<size_t>(bh) * Nq + (q_row < Nq ? q_row : 0)) * D;
+        // dQ_i^T in TMEM: thread t holds head dimension t of every query row
+        // (one row per column).  fp32 reductions straight from registers:
+        // for each row the warp's 32 lanes add 32 consecutive floats, one
+        // 128-byte line per instruction.  Two 32-row pieces at a time; the
+        // TMEM columns are released right after the last read.
+        const int rows = Nq - q0;  // rows of this tile that exist (>= 1)
+        float* dst = p.dq_buf + (static_cast<size_t>(bh) * Nq + q0) * D + t;
         float g2[2][32];
 #pragma unroll
-        for (int h2 = 0; h2 < D / 64; ++h2) {
+        for (int h2 = 0; h2 < 2; ++h2) {
           tmem_ld32(tmem + lane_base + C::kColDQ + 64 * h2, g2[0]);
           tmem_ld32(tmem + lane_base + C::kColDQ + 64 * h2 + 32, g2[1]);
           tmem_wait_ld();
-          if (h2 == D / 64 - 1) {
+          if (h2 == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
           }
-          if (q_row < Nq) {
+          if (rows >= kTileRows) {
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc)
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                red_add_v4(dst + 64 * h2 + 32 * pc + 4 * j, g2[pc][4 * j], g2[pc][4 * j + 1], g2[pc][4 * j + 2],
-                           g2[pc][4 * j + 3]);
+              for (int j = 0; j < 32; ++j) red_add_f32(dst + static_cast<size_t>(64 * h2 + 32 * pc + j) * D, g2[pc][j]);
+          } else {
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (64 * h2 + 32 * pc + j < rows) red_add_f32(dst + static_cast<size_t>(64 * h2 + 32 * pc + j) * D, g2[pc][j]);
           }
         }
         continue;
