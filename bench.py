@@ -50,8 +50,8 @@ KERNEL_TRAFFIC = {
     # (kernel, workload, causal): (read + write bytes, digest of the sources).
     # Capture summarised in the DRAM-traffic profile of the long causal
     # workload (dram__bytes_read.sum + dram__bytes_write.sum, one launch each).
-    ("fa2_fwd_kernel", "long", True): (405447936 + 115087360, "497c146894f62f6e"),
-    ("fa2_bwd_kernel", "long", True): (809664512 + 485897472, "8fd85d1274a4b3ea"),
+    ("fa2_fwd_kernel", "long", True): (406046208 + 115090176, "56e91a63ba57c352"),
+    ("fa2_bwd_kernel", "long", True): (810566144 + 485902592, "89b307daeb0fe5f6"),
 }
 
 KERNEL_SOURCES = {
@@ -485,7 +485,7 @@ def measure_dq_modes(fa2, dev, stream, peaks, names=("stress", "long")):
         dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
         row = {"workload": f"{name}: B={B} H={H} N={N} d={d} causal"}
         bf = w.bwd_flops(True)
-        for mode, label in ((0, "tma_reduce_add"), (1, "atomics_red_v4"), (2, "split_accumulate")):
+        for mode, label in ((0, "tma_reduce_add"), (1, "atomics_red_transposed"), (2, "split_accumulate")):
             if mode == 2:
                 buf = torch.empty(lib.fa2_bwd_dq_partials_bytes(B, H, N, d, 1) // 4, dtype=torch.float32, device=dev)
             else:
@@ -697,7 +697,7 @@ def run_gpu(args, w, causal):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{w.name}: B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'}",
                    "B": B, "H": H, "N": N, "d": d, "causal": causal, "parallelism": f"weak x{world} (heads)",
-                   "dq_reduction": ["tma_reduce_add", "atomics_red_v4", "split_accumulate"][args.dq_mode],
+                   "dq_reduction": ["tma_reduce_add", "atomics_red_transposed", "split_accumulate"][args.dq_mode],
                    "l2": (f"inputs larger than L2 (Q, K, V, dO {B * H * N * d * 2 / 1e6:.0f} MB each), no flush"
                           if 4 * B * H * N * d * 2 > 129e6 else "inputs fit in L2 together; back-to-back steps")},
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "pct_of_peak_burst": 100 * fwd_tf / peaks["bf16_tflops"],
