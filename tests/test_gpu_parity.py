@@ -130,7 +130,8 @@ def test_nonzero_stream_and_invalid_args_raise():
 
 def test_host_step_pipeline_matches_device_calls():
     # attention_step_from_host pipelines host<->device copies with the
-    # kernels over groups of heads; its results must be those of plain
+    # kernels over groups of heads (equal groups, the default ramp, explicit
+    # groups; one to three compute streams); its results must be those of plain
     # fa2_fwd / fa2_bwd on the same inputs (bit-identical except dQ, whose
     # fp32 reduction order varies between runs).
     import tiled_exact_attention_fa2_gb300 as fa2
@@ -146,10 +147,16 @@ def test_host_step_pipeline_matches_device_calls():
     devb = {k: torch.empty_like(t) for k, t in g.items()}
     devb.update({k: torch.empty_like(g["q"]) for k in ("o", "dq", "dk", "dv")})
     devb["lse"] = torch.empty_like(lse)
-    for chunks in (1, 3):
-        fa2.attention_step_from_host(host, devb, True, None, None, chunks=chunks)
+    plans = [dict(chunks=1, compute_streams=1), dict(chunks=3), dict(),  # default: ramp of groups, 2 streams
+             dict(groups=[1, 5, 10, 10, 6], compute_streams=3)]
+    for plan in plans:
+        for name in ("o", "lse", "dq", "dk", "dv"):
+            host[name].zero_()
+        fa2.attention_step_from_host(host, devb, True, None, None, **plan)
         torch.cuda.synchronize()
         assert fa2.fa2_device_status(reset=True) == 0
         assert torch.equal(host["o"], o.cpu()) and torch.equal(host["lse"], lse.cpu())
         assert torch.equal(host["dk"], dk.cpu()) and torch.equal(host["dv"], dv.cpu())
         check_grad(to_np(host["dq"]), to_np(dq), "dQ")
+    with pytest.raises(ValueError):
+        fa2.attention_step_from_host(host, devb, True, None, None, groups=[16, 15])

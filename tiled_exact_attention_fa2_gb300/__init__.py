@@ -511,26 +511,60 @@ def _copy_streams(device):
     return _COPY_STREAMS[key]
 
 
+_COMPUTE_STREAMS = {}
+
+
+def _compute_streams(device, n):
+    """n extra compute streams per device, created once."""
+    if n <= 0:
+        return ()
+    key = (str(device), n)
+    if key not in _COMPUTE_STREAMS:
+        _COMPUTE_STREAMS[key] = tuple(torch.cuda.Stream(device=device) for _ in range(n))
+    return _COMPUTE_STREAMS[key]
+
+
 def attention_step_from_host(host: dict, dev: dict, causal: bool = True, scale: Optional[float] = None,
-                             stream=None, chunks: Optional[int] = None) -> dict:
+                             stream=None, chunks: Optional[int] = None, groups=None,
+                             compute_streams: int = 2) -> dict:
     """One forward + backward pass starting from pinned host tensors.
 
     ``host`` holds pinned CPU bf16 tensors q, k, v, dO and pinned outputs
     o, lse, dq, dk, dv; ``dev`` holds device buffers of the same names
     ([B, H, N, d]; lse [B, H, N]).  Every (batch, head) is an independent
-    problem, so the B * H heads are processed in ``chunks`` groups (default:
-    up to 4) as a pipeline over three streams: the host->device copy of group
-    c + 1 and the device->host copy of group c - 1 run while fa2_fwd and
-    fa2_bwd of group c run on ``stream``.  Everything is enqueued
-    asynchronously and ``stream`` waits for the last copy: synchronise it
-    before reading ``host``.
+    problem, so the B * H heads are processed in groups as a pipeline: the
+    host->device copy of a later group and the device->host copy of an
+    earlier one run while fa2_fwd and fa2_bwd of the current group run.
+    Groups: ``groups`` (head counts summing to B * H), else ``chunks`` equal
+    groups, else by default a ramp of B*H/8, three of B*H/4 and the rest
+    (small first and last groups shorten the first upload and the last
+    download; the large middle ones keep the kernels efficient).  The groups
+    take turns on ``compute_streams`` streams (``stream`` and extra ones), so
+    one group's causal tail overlaps the next group's start.  Everything is
+    enqueued asynchronously and ``stream`` waits for the last copy:
+    synchronise it before reading ``host``.
     """
     s = torch.cuda.current_stream() if stream is None else stream
     device = dev["q"].device
     B, H, N, d = dev["q"].shape
     BH = B * H
-    n = max(1, min(BH, chunks if chunks is not None else 4))
-    bounds = [BH * i // n for i in range(n + 1)]
+    if groups is not None:
+        if sum(groups) != BH or min(groups) < 1:
+            raise ValueError(f"groups must be positive head counts summing to B * H = {BH}")
+        bounds = [0]
+        for size in groups:
+            bounds.append(bounds[-1] + int(size))
+        n = len(groups)
+    elif chunks is not None or BH < 8:
+        n = max(1, min(BH, chunks if chunks is not None else 4))
+        bounds = [BH * i // n for i in range(n + 1)]
+    else:
+        sizes = [BH // 8, BH // 4, BH // 4, BH // 4]
+        sizes.append(BH - sum(sizes))
+        bounds = [0]
+        for size in sizes:
+            bounds.append(bounds[-1] + size)
+        n = len(sizes)
     cin, cout = _copy_streams(device)
     flat = {k: (t.view(BH, N, d) if k != "lse" else t.view(BH, N)) for k, t in dev.items()}
     hflat = {k: (t.view(BH, N, d) if k != "lse" else t.view(BH, N)) for k, t in host.items()}
@@ -546,15 +580,19 @@ def attention_step_from_host(host: dict, dev: dict, causal: bool = True, scale: 
             e = torch.cuda.Event()
             e.record(cin)
             loaded.append(e)
+    comp = [s] + list(_compute_streams(device, compute_streams - 1))
+    for extra in comp[1:]:
+        extra.wait_event(start)
     for c in range(n):
         a, b = bounds[c], bounds[c + 1]
-        s.wait_event(loaded[c])
+        cs = comp[c % len(comp)]
+        cs.wait_event(loaded[c])
         view = {k: flat[k][a:b].unsqueeze(0) for k in flat}
-        fa2_fwd(view["q"], view["k"], view["v"], view["o"], view["lse"], scale, causal, s)
+        fa2_fwd(view["q"], view["k"], view["v"], view["o"], view["lse"], scale, causal, cs)
         fa2_bwd(view["q"], view["k"], view["v"], view["o"], view["dO"], view["lse"], view["dq"], view["dk"],
-                view["dv"], scale, causal, s)
+                view["dv"], scale, causal, cs)
         e = torch.cuda.Event()
-        e.record(s)
+        e.record(cs)
         computed.append(e)
     for c in range(n):
         a, b = bounds[c], bounds[c + 1]
