@@ -54,11 +54,11 @@ enum class Elem { kBf16, kF16, kF32 };
 struct TmapKey {
   const void* base;
   Elem type;
-  int heads, d;
+  int heads, d, box_rows;
   long long rows, row_stride, head_stride;
   bool operator==(const TmapKey& o) const {
-    return base == o.base && type == o.type && heads == o.heads && d == o.d && rows == o.rows &&
-           row_stride == o.row_stride && head_stride == o.head_stride;
+    return base == o.base && type == o.type && heads == o.heads && d == o.d && box_rows == o.box_rows &&
+           rows == o.rows && row_stride == o.row_stride && head_stride == o.head_stride;
   }
 };
 constexpr int kTmapCacheSize = 64;
@@ -68,11 +68,11 @@ CUtensorMap g_tmap_vals[kTmapCacheSize];
 int g_tmap_count = 0, g_tmap_next = 0;
 
 bool encode_rows_uncached(CUtensorMap* out, const void* base, Elem type, int heads, long long rows, int d,
-                          long long row_stride, long long head_stride);
+                          long long row_stride, long long head_stride, int box_rows);
 
 bool encode_rows(CUtensorMap* out, const void* base, Elem type, int heads, long long rows, int d,
-                 long long row_stride, long long head_stride) {
-  const TmapKey key{base, type, heads, d, rows, row_stride, head_stride};
+                 long long row_stride, long long head_stride, int box_rows = kRowsPerTile) {
+  const TmapKey key{base, type, heads, d, box_rows, rows, row_stride, head_stride};
   {
     std::lock_guard<std::mutex> lock(g_tmap_mu);
     for (int i = 0; i < g_tmap_count; ++i)
@@ -81,7 +81,7 @@ bool encode_rows(CUtensorMap* out, const void* base, Elem type, int heads, long 
         return true;
       }
   }
-  if (!encode_rows_uncached(out, base, type, heads, rows, d, row_stride, head_stride)) return false;
+  if (!encode_rows_uncached(out, base, type, heads, rows, d, row_stride, head_stride, box_rows)) return false;
   std::lock_guard<std::mutex> lock(g_tmap_mu);
   g_tmap_keys[g_tmap_next] = key;
   g_tmap_vals[g_tmap_next] = *out;
@@ -91,7 +91,7 @@ bool encode_rows(CUtensorMap* out, const void* base, Elem type, int heads, long 
 }
 
 bool encode_rows_uncached(CUtensorMap* out, const void* base, Elem type, int heads, long long rows, int d,
-                          long long row_stride, long long head_stride) {
+                          long long row_stride, long long head_stride, int box_rows) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const bool f32 = type == Elem::kF32;
@@ -104,7 +104,7 @@ bool encode_rows_uncached(CUtensorMap* out, const void* base, Elem type, int hea
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(heads)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride) * esz, static_cast<cuuint64_t>(head_stride) * esz};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), kRowsPerTile, 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : (type == Elem::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
@@ -116,6 +116,12 @@ bool encode_rows_uncached(CUtensorMap* out, const void* base, Elem type, int hea
 // [B*H, N, d] bf16 view, box = [1, 128 rows, min(d, 64) columns].
 bool make_tmap(CUtensorMap* out, const void* base, int BH, int N, int d, Elem type = Elem::kBf16) {
   return encode_rows(out, base, type, BH, N, d, d, static_cast<long long>(N) * d);
+}
+
+// [heads, rows, d] bf16 view of the forward output for its TMA stores: box =
+// [1, 32 rows, min(d, 64) columns] (one softmax warp's rows).
+bool make_tmap_out(CUtensorMap* out, const void* base, int heads, int rows, int d) {
+  return encode_rows(out, base, Elem::kBf16, heads, rows, d, d, static_cast<long long>(rows) * d, 32);
 }
 
 // Packed [total, heads, d] bf16 view (variable-length batches).
@@ -332,7 +338,8 @@ int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
             float scale, int causal, void* ws, cudaStream_t st) {
   const int BH = B * H;
   TmapSet tm;
-  if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, B * H_kv, N, d) || !make_tmap(&tm.v, v, B * H_kv, N, d))
+  if (!make_tmap(&tm.q, q, BH, N, d) || !make_tmap(&tm.k, k, B * H_kv, N, d) || !make_tmap(&tm.v, v, B * H_kv, N, d) ||
+      !make_tmap_out(&tm.o, o, BH, N, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
   FwdProblem p{};
   p.RH = BH;
@@ -481,7 +488,7 @@ int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float*
   }
   TmapSet tm;
   if (!make_tmap(&tm.q, q, p.RH, p.M, d) || !make_tmap(&tm.k, k, B * H_kv, Nk, d) ||
-      !make_tmap(&tm.v, v, B * H_kv, Nk, d))
+      !make_tmap(&tm.v, v, B * H_kv, Nk, d) || !make_tmap_out(&tm.o, o, p.RH, p.M, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (int e = launch_fwd(tm, p, d, scale, causal != 0, st)) return cuda_fail(e, "split-kv fwd launch");
@@ -749,6 +756,7 @@ int fa2_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* 
   if (!make_tmap_packed(&tm.q, q, H, total_q, d) || !make_tmap_packed(&tm.k, kb_ptr, H_kv, tk, d) ||
       !make_tmap_packed(&tm.v, vb_ptr, H_kv, tk, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
+  tm.o = tm.q;  // packed batches store O without TMA (a tile may end inside the next sequence)
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (total_k == 0) {  // no keys: V is never read (its maps describe q)
     tm.v16 = tm.v;

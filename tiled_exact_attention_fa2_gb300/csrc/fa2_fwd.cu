@@ -98,7 +98,11 @@ struct FwdCfg {
   static constexpr int kQ = 0;  // Q_A, Q_B
   static constexpr int kK = kQ + 2 * T::kTileBytes;
   static constexpr int kV = kK + 2 * T::kTileBytes;
-  static constexpr int kBars = kV + 2 * T::kTileBytes;
+  // O leaves through one 4 KB slice per softmax warp (its 32 rows x 64
+  // columns, 128B-swizzled) and a TMA store, for D >= 64.
+  static constexpr bool kTmaOut = D >= 64;
+  static constexpr int kOStage = kV + 2 * T::kTileBytes;
+  static constexpr int kBars = kOStage + (kTmaOut ? 8 * 4096 : 0);
   static constexpr int kSched = (kBars + kNumFwdBars * 8 + 15) / 16 * 16;  // 2 x 16-byte responses
   static constexpr int kTmemSlot = kSched + 32;
   static constexpr int kUsed = kTmemSlot + 16;
@@ -221,7 +225,8 @@ __device__ __forceinline__ int next_unit(uint64_t* bars, const uint8_t* sched, i
 template <int D, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdProblem p, float scale_log2) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const FwdProblem p, float scale_log2) {
   // P V on fp16 operands (tm_v is then the fp16 copy of V), except in the
   // split-KV form.
   constexpr bool kF16 = MODE != kGeneral;
@@ -667,9 +672,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
       tc_fence_after();
       const float inv_l = lo > 0.f ? v_scale / lo : 0.f;
+      // Square and split-KV forms with bf16 output: through shared memory and
+      // TMA stores, so the warp does not wait for its rows to reach L2 (TMA
+      // drops the rows past M).  Packed batches store directly: a tile's last
+      // rows may belong to the next sequence.
+      const bool tma_out = C::kTmaOut && MODE != kVarlen && !partial;
+      if (tma_out) {
+        const int row_w0 = w.q0 + x * kTileRows + (warp & 3) * 32;  // this warp's first row
+        const uint32_t slice = smem_u32(smem + C::kOStage + warp * 4096);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          float o[64];
+          tmem_ld32(tO + 64 * h, *reinterpret_cast<float(*)[32]>(o));
+          tmem_ld32(tO + 64 * h + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+          tmem_wait_ld();
+          // the slice is free once this warp's previous store has read it
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(slice + sw128_offset(lane, c), pack_bf16x2(o[8 * c + 0] * inv_l, o[8 * c + 1] * inv_l),
+                         pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l),
+                         pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l),
+                         pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row_w0 < w.M) {
+            tma_store_3d(&tm_o, slice, 64 * h, row_w0, w.rh);
+            bulk_commit_group();
+          }
+        }
+      }
       constexpr int kC = D >= 32 ? 32 : 16;
 #pragma unroll
-      for (int c = 0; c < D / kC; ++c) {
+      for (int c = 0; c < D / kC && !tma_out; ++c) {
         float o[kC];
         if constexpr (kC == 32)
           tmem_ld32(tO + c * 32, o);
@@ -707,6 +743,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&bars[kBarSchedEmpty + (n & 1)]);
     }
+    // Every O store has read its slice and landed before the CTA exits.
+    if (lane == 0) bulk_wait_group0();
     tc_fence_before();
   }
 
@@ -741,8 +779,8 @@ int launch_fwd_t(const TmapSet& tm, FwdProblem p, float scale, cudaStream_t stre
   const dim3 grid(static_cast<unsigned>(units > 0 ? units : 1));
   const float scale_log2 = scale * 1.44269504088896341f;
   // Square and packed problems read the fp16 copy of V.
-  return launch_pdl(kern, grid, dim3(kFwdThreads), C::kBytes, stream, tm.q, tm.k, (general && !varlen) ? tm.v : tm.v16, p,
-                    scale_log2);
+  return launch_pdl(kern, grid, dim3(kFwdThreads), C::kBytes, stream, tm.q, tm.k, (general && !varlen) ? tm.v : tm.v16,
+                    tm.o, p, scale_log2);
 }
 
 // V in fp16 for the P V MMA: one pass over V (16-byte loads and stores,
