@@ -50,8 +50,8 @@ KERNEL_TRAFFIC = {
     # (kernel, workload, causal): (read + write bytes, digest of the sources).
     # Capture summarised in the DRAM-traffic profile of the long causal
     # workload (dram__bytes_read.sum + dram__bytes_write.sum, one launch each).
-    ("fa2_fwd_kernel", "long", True): (406364416 + 117090560, "4a46c8f284d30609"),
-    ("fa2_bwd_kernel", "long", True): (809677312 + 485670144, "808a93ad5ab32f3c"),
+    ("fa2_fwd_kernel", "long", True): (406577152 + 117581312, "9f75b96de2b6b196"),
+    ("fa2_bwd_kernel", "long", True): (809710080 + 488250624, "9893f9accc3e32fa"),
 }
 
 KERNEL_SOURCES = {

@@ -239,10 +239,11 @@ int validate_bwd(const void* q, const void* k, const void* v, const void* o, con
   return FA2_OK;
 }
 
-int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const void* dO, const float* dq_acc, int BH,
-               int BHkv, int N, int d) {
+int make_tmaps(TmapSet* tm, const void* q, const void* k, const void* v, const void* dO, const float* dq_acc,
+               const void* dk, const void* dv, int BH, int BHkv, int N, int d) {
   return (make_tmap(&tm->q, q, BH, N, d) && make_tmap(&tm->k, k, BHkv, N, d) && make_tmap(&tm->v, v, BHkv, N, d) &&
-          make_tmap(&tm->dO, dO, BH, N, d) && make_tmap_f32(&tm->dqacc, dq_acc, BH, N, d))
+          make_tmap(&tm->dO, dO, BH, N, d) && make_tmap_f32(&tm->dqacc, dq_acc, BH, N, d) &&
+          make_tmap(&tm->dk, dk, BHkv, N, d) && make_tmap(&tm->dv, dv, BHkv, N, d))
              ? FA2_OK
              : cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
 }
@@ -255,7 +256,7 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
   float* Dvec = static_cast<float*>(ws);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(rows * sizeof(float)));
   TmapSet tm;
-  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, BH, B * Hkv, N, d)) return rc;
+  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_acc, dk, dv, BH, B * Hkv, N, d)) return rc;
   if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, BH, N, d, st)) return cuda_fail(e, "bwd preprocess launch");
   BwdProblem p{};
   p.lse = lse;
@@ -591,7 +592,7 @@ int bwd_main_stage(const void* q, const void* k, const void* v, const void* dO, 
       if (overlap(outs[a], outs[b])) return FA2_ERR_ALIAS;
   }
   TmapSet tm;
-  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_buf, B * H, B * H, N, d)) return rc;
+  if (int rc = make_tmaps(&tm, q, k, v, dO, dq_buf, dk, dv, B * H, B * H, N, d)) return rc;
   if (dq_mode == kDqSplit &&
       !encode_rows(&tm.dqacc, dq_buf, Elem::kF32, static_cast<int>(pairs), kRowsPerTile, d, d,
                    static_cast<long long>(kRowsPerTile) * d))
@@ -832,6 +833,7 @@ int fa2_bwd_varlen(const void* q, const void* k, const void* v, const void* o, c
       !make_tmap_packed(&tm.v, v, H_kv, total_k, d) || !make_tmap_packed(&tm.dO, dO, H, total_q, d) ||
       !encode_rows(&tm.dqacc, dq_acc, Elem::kF32, H, total_q, d, static_cast<long long>(H) * d, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
+  tm.dk = tm.dv = tm.q;  // packed batches store dK, dV without TMA (a tile may end inside the next sequence)
   // D and the zeroed accumulator in the packed row order ([total_q, H]).
   if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, H, total_q, d, st)) return cuda_fail(e, "bwd preprocess launch");
   BwdProblem p{};

@@ -74,7 +74,8 @@ enum BwdBar {
   kBarDrain = 18,
   kBarStageFull = 19,  // +buffer (2): dQ chunk staged in shared memory (4 warp arrivals)
   kBarStageFree = 21,  // +buffer (2): the TMA reduce of that chunk has read it
-  kNumBwdBars = 23,
+  kBarEpi = 23,        // the 4 drain warps have staged dK, dV for their TMA stores
+  kNumBwdBars = 24,
 };
 
 template <int D, int DQM = kDqReduce>
@@ -180,7 +181,8 @@ template <int D, bool CAUSAL, bool VARLEN, int DQM>
 __global__ void __launch_bounds__(512, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const __grid_constant__ CUtensorMap tm_dqacc, const BwdProblem p, float scale, float scale_log2) {
+                   const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dk,
+                   const __grid_constant__ CUtensorMap tm_dv, const BwdProblem p, float scale, float scale_log2) {
   using T = HeadDim<D>;
   using C = BwdCfg<D, DQM>;
   const float* __restrict__ lse = p.lse;
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bars[kBarDqDrained], 4);
     mbar_init(&bars[kBarAccFull], 1);
     mbar_init(&bars[kBarDrain], 1);
+    mbar_init(&bars[kBarEpi], 4);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -667,8 +670,52 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (issuer) bulk_wait_group0();  // every reduce / store has landed before the CTA exits
     // ------------------------------------------------------------ epilogue: dV, dK * scale -> bf16
+    // dK, dV of square problems with D >= 64 leave by TMA stores; packed
+    // batches store directly (a tile may end inside the next sequence).
+    constexpr bool kTmaKV = D >= 64 && !VARLEN;
     if (ok && mbar_wait_sleep(&bars[kBarAccFull], 0, status)) {
       tc_fence_after();
+      if constexpr (kTmaKV) {
+      // Every MMA has completed, so the Q stages are free: dV goes to stage 0
+      // and dK to stage 1 in the layout a TMA load of a K tile produces, and
+      // leaves by TMA stores (rows past N are dropped).  The CTA exits once
+      // the stores have read shared memory; the writes drain while the next
+      // CTA on this SM starts.
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+        const float mul = which == 0 ? 1.f : scale;
+        const uint32_t tile = smem_u32(smem + C::kQ + which * T::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float g[32];
+          tmem_ld32(tmem + lane_base + col + c * 32, g);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = c * 4 + q;  // 8 columns
+            st_shared_v4(tile + (chunk >> 3) * T::kBoxBytes + sw128_offset(t, chunk & 7),
+                         pack_bf16x2(g[8 * q + 0] * mul, g[8 * q + 1] * mul),
+                         pack_bf16x2(g[8 * q + 2] * mul, g[8 * q + 3] * mul),
+                         pack_bf16x2(g[8 * q + 4] * mul, g[8 * q + 5] * mul),
+                         pack_bf16x2(g[8 * q + 6] * mul, g[8 * q + 7] * mul));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarEpi]);
+      if (issuer && mbar_wait(&bars[kBarEpi], 0, status)) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which)
+#pragma unroll
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_store_3d(which == 0 ? &tm_dv : &tm_dk, smem_u32(smem + C::kQ + which * T::kTileBytes) + b * T::kBoxBytes,
+                         b * T::kBoxCols, kv0, bh_kv);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      } else {
       const int kv_row = kv0 + t;
       const bool valid = kv_row < Nk;
       const int vrow = valid ? kv_row : 0;
@@ -708,6 +755,7 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
+      }
     }
     tc_fence_before();
   }
@@ -744,8 +792,8 @@ int launch_bwd_main_k(const TmapSet& tm, BwdProblem p, float scale, cudaStream_t
   // accumulator and LSE, D of its `group` query heads.
   const size_t per_head = static_cast<size_t>(p.group) * rows_q * (static_cast<size_t>(D) * 8 + 8);
   p.heads_per_group = heads_per_l2_group(per_head, kv_heads);
-  return launch_pdl(kern, grid, dim3(kBwdThreads), C::kBytes, stream, tm.q, tm.k, tm.v, tm.dO, tm.dqacc, p, scale,
-                    scale * kLog2e);
+  return launch_pdl(kern, grid, dim3(kBwdThreads), C::kBytes, stream, tm.q, tm.k, tm.v, tm.dO, tm.dqacc, tm.dk, tm.dv, p,
+                    scale, scale * kLog2e);
 }
 
 // The atomic and split dQ modes are compiled for d = 128 square problems only.

@@ -10,7 +10,8 @@ namespace fa2 {
 // fp16 copy of V the forward pass reads, and of the fp32 dQ accumulator.
 struct TmapSet {
   CUtensorMap q, k, v, v16, dO, dqacc;
-  CUtensorMap o;  // forward output, 32-row boxes (square and split-KV forms, bf16 output)
+  CUtensorMap o;       // forward output, 32-row boxes (square and split-KV forms, bf16 output)
+  CUtensorMap dk, dv;  // backward outputs (square form), 128-row boxes
 };
 
 // Launch `kern` on `stream` with programmatic stream serialisation (the
