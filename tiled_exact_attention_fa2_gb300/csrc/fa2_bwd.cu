@@ -222,10 +222,13 @@ __global__ void __launch_bounds__(512, 1)
   const int BHkv = VARLEN ? p.Hkv : p.BH / group;
   const int per_batch = BHkv * kv_tiles_grid;
   const int local = VARLEN ? static_cast<int>(blockIdx.x % per_batch) : static_cast<int>(blockIdx.x);
-  const int per_group = p.heads_per_group * kv_tiles_grid;
-  const int hg0 = local / per_group * p.heads_per_group;
-  const int within = local % per_group;
-  const int hg = min(p.heads_per_group, BHkv - hg0);
+  // Groups of heads_per_group heads; the last one also takes the heads left
+  // over, so that its heavy tiles are not few against a short group.
+  const int n_groups = max(1, BHkv / p.heads_per_group);
+  const int gi = min(local / (p.heads_per_group * kv_tiles_grid), n_groups - 1);
+  const int hg0 = gi * p.heads_per_group;
+  const int hg = gi == n_groups - 1 ? BHkv - hg0 : p.heads_per_group;
+  const int within = local - hg0 * kv_tiles_grid;
   const int jt = within / hg;  // key/value tile
   const int bh_kv = hg0 + within % hg;
   const int kv0 = jt * kTileRows;
@@ -791,7 +794,7 @@ int launch_bwd_main_k(const TmapSet& tm, BwdProblem p, float scale, cudaStream_t
   // Bytes one K/V head's CTAs keep re-reading: Q, dO (bf16), the fp32 dQ
   // accumulator and LSE, D of its `group` query heads.
   const size_t per_head = static_cast<size_t>(p.group) * rows_q * (static_cast<size_t>(D) * 8 + 8);
-  p.heads_per_group = heads_per_l2_group(per_head, kv_heads);
+  p.heads_per_group = heads_per_l2_group(per_head, kv_heads, kL2GroupBytesBwd);
   return launch_pdl(kern, grid, dim3(kBwdThreads), C::kBytes, stream, tm.q, tm.k, tm.v, tm.dO, tm.dqacc, tm.dk, tm.dv, p,
                     scale, scale * kLog2e);
 }

@@ -40,10 +40,13 @@ int ensure_max_smem(const void* kernel, int bytes);
 // group of heads run before the next group's, so the rows every CTA of a head
 // re-reads (K/V in the forward pass, Q/dO/dQ in the backward pass) are read
 // from HBM about once per group instead of once per wave of CTAs.  A group's
-// re-read set is kept to about a quarter of the L2.
+// re-read set is kept to about a quarter of the L2 in the forward pass and
+// about half of it in the backward pass (measured: at N = 4096 the larger
+// backward groups are 3 % faster, the forward is 1 % slower with them).
 constexpr size_t kL2GroupBytes = size_t(32) << 20;
-inline int heads_per_l2_group(size_t bytes_per_head, int heads) {
-  size_t g = bytes_per_head ? kL2GroupBytes / bytes_per_head : static_cast<size_t>(heads);
+constexpr size_t kL2GroupBytesBwd = size_t(64) << 20;
+inline int heads_per_l2_group(size_t bytes_per_head, int heads, size_t group_bytes = kL2GroupBytes) {
+  size_t g = bytes_per_head ? group_bytes / bytes_per_head : static_cast<size_t>(heads);
   if (g < 1) g = 1;
   if (g > static_cast<size_t>(heads)) g = static_cast<size_t>(heads);
   return static_cast<int>(g);
