@@ -17,7 +17,8 @@ import pytest
 from protocol_model import Engine
 
 
-def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0, one_p_full=False):
+def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0, one_p_full=False,
+                  phantom_turns_a=False):
     """Roles of one CTA.  ``dual``: decoding (tile B never has rows), where
     tile A alternates its S / P / PV barriers between the two S buffers and
     issues S(j+1) before PV(j)."""
@@ -134,7 +135,10 @@ def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0
         tok_wait, tok_pass = (("TokB", w), ("TokA", w)) if x else (("TokA", w), ("TokB", w))
         for n, cnt in enumerate(units):
             nx = cnt[x]
-            n_turns = max(cnt) if (turns and not dual and min(cnt) > 0) else 0
+            # turns only for the K/V tiles both query tiles visit
+            n_turns = min(cnt) if (turns and not dual and min(cnt) > 0) else 0
+            if phantom_turns_a and x == 0 and n_turns:  # planted: tile A also takes turns for B's extra tiles
+                n_turns = max(cnt)
             for j in range(max(nx, n_turns)):
                 if j < nx:
                     b, i = buf(x, k)
@@ -230,3 +234,16 @@ def test_model_catches_a_single_p_full_barrier_in_decode():
         if found:
             break
     assert found and "two phases" in found
+
+
+def test_model_catches_turns_taken_by_one_tile_only():
+    # Tile A taking turns for the K/V tiles only tile B visits (while B
+    # takes turns only for the shared ones) puts the two token barriers out
+    # of step: a waiter ends up two phases behind or waits forever.
+    found = None
+    for seed in range(2000):
+        units = _units(random.Random(seed), "causal")
+        found = _run(units, seed, phantom_turns_a=True)
+        if found:
+            break
+    assert found

@@ -483,9 +483,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int k = 0;  // S_x tiles consumed so far
     // Softmax warps w (tile A) and w + 4 (tile B) share an SMSP and take
     // turns at the exponentials, so that the two never contend for its MUFU
-    // and issue slots: per unit, turn j of tile A, then turn j of tile B,
-    // for every K/V tile j of the unit (a tile the warp does not visit is a
-    // turn it passes on at once).  Tile A's turn t waits for B's turn t - 1;
+    // and issue slots: per unit, turn j of tile A, then turn j of tile B, for
+    // every K/V tile j that both tiles visit.  A tile's K/V tiles beyond the
+    // other's (tile B's diagonal tile in a causal unit) take no turn: the
+    // other tile is then in its epilogue or starting its next unit, and
+    // need not wait for them.  Tile A's turn t waits for B's turn t - 1;
     // B's turn t waits for A's turn t.  Each waiter is exactly one phase
     // behind the token barrier it waits on.
     int tn = 0;  // turns this warp has taken
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!w.valid) break;
       const int nx = x ? w.cnt[1] : w.cnt[0];  // (selects keep the struct in registers)
       // Turns are taken only in units where both tiles have K/V tiles.
-      const int turns = (!dual && w.cnt[0] > 0 && w.cnt[1] > 0) ? max(w.cnt[0], w.cnt[1]) : 0;
+      const int turns = (!dual && w.cnt[0] > 0 && w.cnt[1] > 0) ? min(w.cnt[0], w.cnt[1]) : 0;
       const int q_row = w.q0 + x * kTileRows + r;              // row in the row-head
       const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
       const int imin_x = x ? w.imin[1] : w.imin[0];
@@ -625,13 +627,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l = l * alpha + rs;
         lo = lo * alpha + (rs + dpmax);
         m = m_new;
-      }
-      if (!ok) break;
-      // Turns of the K/V tiles this warp does not visit.
-#pragma unroll 1
-      for (int j = nx; j < turns; ++j) {
-        if (!(ok = take_turn())) break;
-        pass_turn();
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
