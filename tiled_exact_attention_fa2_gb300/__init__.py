@@ -534,7 +534,9 @@ def attention_step_from_host(host: dict, dev: dict, causal: bool = True, scale: 
     ([B, H, N, d]; lse [B, H, N]).  Every (batch, head) is an independent
     problem, so the B * H heads are processed in groups as a pipeline: the
     host->device copy of a later group and the device->host copy of an
-    earlier one run while fa2_fwd and fa2_bwd of the current group run.
+    earlier one run while fa2_fwd and fa2_bwd of the current group run (a
+    group's forward starts once its q, k, v have arrived, and its O and LSE
+    go back while its backward runs).
     Groups: ``groups`` (head counts summing to B * H), else ``chunks`` equal
     groups, else by default a ramp of B*H/8, three of B*H/4 and the rest
     (small first and last groups shorten the first upload and the last
@@ -571,35 +573,49 @@ def attention_step_from_host(host: dict, dev: dict, causal: bool = True, scale: 
     start = torch.cuda.Event()
     start.record(s)
     cin.wait_event(start)  # the device buffers are free once earlier work on `stream` is done
-    loaded, computed = [], []
-    for c in range(n):
-        a, b = bounds[c], bounds[c + 1]
-        with torch.cuda.stream(cin):
-            for name in ("q", "k", "v", "dO"):
-                flat[name][a:b].copy_(hflat[name][a:b], non_blocking=True)
+    def copies(stream, names, a, b, to_host):
+        with torch.cuda.stream(stream):
+            for name in names:
+                if to_host:
+                    hflat[name][a:b].copy_(flat[name][a:b], non_blocking=True)
+                else:
+                    flat[name][a:b].copy_(hflat[name][a:b], non_blocking=True)
             e = torch.cuda.Event()
-            e.record(cin)
-            loaded.append(e)
+            e.record(stream)
+        return e
+
+    # Uploads: a group's q, k, v (all its forward needs), then its dO.
+    qkv_in, do_in = [], []
+    for c in range(n):
+        qkv_in.append(copies(cin, ("q", "k", "v"), bounds[c], bounds[c + 1], False))
+        do_in.append(copies(cin, ("dO",), bounds[c], bounds[c + 1], False))
     comp = [s] + list(_compute_streams(device, compute_streams - 1))
     for extra in comp[1:]:
         extra.wait_event(start)
+    fwd_done, bwd_done = [], []
     for c in range(n):
         a, b = bounds[c], bounds[c + 1]
         cs = comp[c % len(comp)]
-        cs.wait_event(loaded[c])
         view = {k: flat[k][a:b].unsqueeze(0) for k in flat}
+        cs.wait_event(qkv_in[c])
         fa2_fwd(view["q"], view["k"], view["v"], view["o"], view["lse"], scale, causal, cs)
+        e = torch.cuda.Event()
+        e.record(cs)
+        fwd_done.append(e)
+        cs.wait_event(do_in[c])
         fa2_bwd(view["q"], view["k"], view["v"], view["o"], view["dO"], view["lse"], view["dq"], view["dk"],
                 view["dv"], scale, causal, cs)
         e = torch.cuda.Event()
         e.record(cs)
-        computed.append(e)
+        bwd_done.append(e)
+    # Downloads: a group's O and LSE as soon as its forward is done, its
+    # gradients after its backward.
     for c in range(n):
         a, b = bounds[c], bounds[c + 1]
-        cout.wait_event(computed[c])
-        with torch.cuda.stream(cout):
-            for name in ("o", "lse", "dq", "dk", "dv"):
-                hflat[name][a:b].copy_(flat[name][a:b], non_blocking=True)
+        cout.wait_event(fwd_done[c])
+        copies(cout, ("o", "lse"), a, b, True)
+        cout.wait_event(bwd_done[c])
+        copies(cout, ("dq", "dk", "dv"), a, b, True)
     done = torch.cuda.Event()
     done.record(cout)
     s.wait_event(done)
