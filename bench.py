@@ -50,8 +50,8 @@ KERNEL_TRAFFIC = {
     # (kernel, workload, causal): (read + write bytes, digest of the sources).
     # Capture summarised in the DRAM-traffic profile of the long causal
     # workload (dram__bytes_read.sum + dram__bytes_write.sum, one launch each).
-    ("fa2_fwd_kernel", "long", True): (406150400 + 117425920, "aa6d6fede7b57374"),
-    ("fa2_bwd_kernel", "long", True): (835401216 + 505532672, "d1202ce3abd037fb"),
+    ("fa2_fwd_kernel", "long", True): (405978112 + 117757696, "b8fcaa5fdcbc2afc"),
+    ("fa2_bwd_kernel", "long", True): (835823872 + 505265664, "ee334c7fc2955bad"),
 }
 
 KERNEL_SOURCES = {
