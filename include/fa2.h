@@ -196,7 +196,9 @@ size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);
 /* fa2_bwd with caller-provided scratch: `workspace` is a device pointer,
  * 256-byte aligned, of at least fa2_bwd_workspace_bytes(B,H,N,d) bytes,
  * owned by the caller and not used by anything else until the stream has
- * passed this call.  Allocates nothing. */
+ * passed this call.  Allocates nothing.  FA2_ERR_WORKSPACE if it is NULL,
+ * misaligned or too small, FA2_ERR_ALIAS if its first
+ * fa2_bwd_workspace_bytes bytes overlap any tensor of the call. */
 int fa2_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                void* workspace, size_t workspace_bytes, void* stream);

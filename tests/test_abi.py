@@ -199,3 +199,74 @@ def test_bwd_varlen_rejects_bad_arguments(lib):
     assert call(wsp=None) == 8
     assert call(wsb=need - 1) == 8
     assert call(wsp=ws + 16) == 8
+
+
+def _round256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_fwd_workspace_bytes(lib):
+    # fp16 copy of V, then a 64-bit flag and an fp32 scale per K/V head,
+    # each part 256-byte rounded
+    B, Hkv, N, d = 2, 4, 300, 64
+    heads = B * Hkv
+    assert fa2.fa2_fwd_workspace_bytes(B, Hkv, N, d) == (_round256(heads * N * d * 2) + _round256(heads * 8) +
+                                                         _round256(heads * 4))
+    assert fa2.fa2_fwd_workspace_bytes(1, 1, 1, 48) == 0
+    assert fa2.fa2_fwd_workspace_bytes(0, 1, 1, 16) == 0
+
+
+def test_fwd_ws_rejects_bad_workspace(lib):
+    need = fa2.fa2_fwd_workspace_bytes(1, 1, 128, 64)
+    args = (A, 2 * A, 3 * A, 4 * A, 5 * A, 1, 1, 128, 64, 0.125, 1)
+    ws = 64 * A
+    assert lib.fa2_fwd_ws(*args, None, need, None) == 8
+    assert lib.fa2_fwd_ws(*args, ws, need - 1, None) == 8
+    assert lib.fa2_fwd_ws(*args, ws + 16, need, None) == 8
+    for p in (A, 2 * A, 3 * A, 4 * A, 5 * A):  # over q, k, v, o, lse
+        assert lib.fa2_fwd_ws(*args, p, need, None) == 9
+
+
+def test_bwd_ws_rejects_overlapping_workspace(lib):
+    p = [A * (i + 1) for i in range(9)]
+    need = fa2.fa2_bwd_workspace_bytes(1, 1, 128, 64)
+    for i in range(9):  # over each of q, k, v, o, dO, lse, dq, dk, dv
+        assert lib.fa2_bwd_ws(*p, 1, 1, 128, 64, 0.125, 1, p[i], need, None) == 9
+
+
+def test_dq_partials_and_deterministic_workspace_bytes(lib):
+    f = lib.fa2_bwd_dq_partials_bytes
+    # one 128 x d fp32 slot per (query tile, key tile) pair; causal: the
+    # pairs on or below the diagonal.  N = 300: 3 tiles.
+    assert f(2, 3, 300, 128, 1) == 2 * 3 * 6 * 128 * 128 * 4
+    assert f(2, 3, 300, 128, 0) == 2 * 3 * 9 * 128 * 128 * 4
+    assert f(1, 1, 300, 64, 1) == 0
+    g = lib.fa2_bwd_deterministic_workspace_bytes
+    assert g(2, 3, 300, 128, 1) == _round256(2 * 3 * 300 * 4) + _round256(f(2, 3, 300, 128, 1))
+    assert g(1, 1, 128, 64, 1) == 0
+
+
+def test_bwd_main_dq_rejects_bad_modes(lib):
+    p = [A * (i + 1) for i in range(9)]  # q, k, v, dO, lse, D, dq buffer, dk, dv
+    f = lib.fa2_bwd_main_dq
+    assert f(*p, 1, 1, 128, 128, 0.125, 1, 3, None) == 2  # unknown mode
+    assert f(*p, 1, 1, 128, 64, 0.125, 1, 1, None) == 3   # register reductions: d = 128 only
+    assert f(*p, 1, 1, 128, 64, 0.125, 1, 2, None) == 3   # split partials: d = 128 only
+    q = list(p)
+    q[8] = q[7]  # dv == dk
+    assert f(*q, 1, 1, 128, 128, 0.125, 1, 1, None) == 9
+
+
+def test_bwd_deterministic_and_dq_reduce_reject_bad_arguments(lib):
+    p = [A * (i + 1) for i in range(9)]
+    need = lib.fa2_bwd_deterministic_workspace_bytes(1, 1, 256, 128, 1)
+    f = lib.fa2_bwd_deterministic
+    assert f(*p, 1, 1, 256, 64, 0.125, 1, 64 * A, 1 << 30, None) == 3  # d = 128 only
+    assert f(*p, 1, 1, 256, 128, 0.125, 1, None, need, None) == 8
+    assert f(*p, 1, 1, 256, 128, 0.125, 1, 64 * A, need - 1, None) == 8
+    assert f(*p, 1, 1, 256, 128, 0.125, 1, p[6], need, None) == 9  # workspace over dq
+    r = lib.fa2_bwd_dq_reduce
+    assert r(None, A, 1, 1, 256, 128, 0.125, 1, None) == 1
+    assert r(A, 2 * A, 1, 1, 256, 64, 0.125, 1, None) == 3
+    assert r(A + 8, 2 * A, 1, 1, 256, 128, 0.125, 1, None) == 4
+    assert r(A, A, 1, 1, 256, 128, 0.125, 1, None) == 9

@@ -335,6 +335,21 @@ bool fwd_ws_overlaps(const void* ws, size_t ws_bytes, const void* q, const void*
   return false;
 }
 
+// Caller scratch of the backward pass against every tensor of the call.
+bool bwd_ws_overlaps(const void* ws, size_t ws_bytes, const void* q, const void* k, const void* v, const void* o,
+                     const void* dO, const float* lse, const void* dq, const void* dk, const void* dv, int B, int H,
+                     int H_kv, int N, int d) {
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t kb = static_cast<size_t>(B) * H_kv * N * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  const Range rw = range_of(ws, ws_bytes);
+  const Range all[] = {range_of(q, tb),  range_of(k, kb),  range_of(v, kb),  range_of(o, tb),  range_of(dO, tb),
+                       range_of(lse, lb), range_of(dq, tb), range_of(dk, kb), range_of(dv, kb)};
+  for (const Range& r : all)
+    if (overlap(rw, r)) return true;
+  return false;
+}
+
 int run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N, int d,
             float scale, int causal, void* ws, cudaStream_t st) {
   const int BH = B * H;
@@ -507,8 +522,9 @@ int fa2_bwd_gqa_ws(const void* q, const void* k, const void* v, const void* o, c
                    void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale, int causal,
                    void* workspace, size_t workspace_bytes_given, void* stream) {
   if (int rc = validate_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale)) return rc;
-  if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < workspace_bytes(B, H, N, d))
-    return FA2_ERR_WORKSPACE;
+  const size_t need = workspace_bytes(B, H, N, d);
+  if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < need) return FA2_ERR_WORKSPACE;
+  if (bwd_ws_overlaps(workspace, need, q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d)) return FA2_ERR_ALIAS;
   return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, workspace,
                  static_cast<cudaStream_t>(stream));
 }
@@ -661,6 +677,7 @@ int fa2_bwd_deterministic(const void* q, const void* k, const void* v, const voi
   if (d != 128) return FA2_ERR_HEADDIM;
   const size_t need = fa2_bwd_deterministic_workspace_bytes(B, H, N, d, causal);
   if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes_given < need) return FA2_ERR_WORKSPACE;
+  if (bwd_ws_overlaps(workspace, need, q, k, v, o, dO, lse, dq, dk, dv, B, H, H, N, d)) return FA2_ERR_ALIAS;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* Dvec = static_cast<float*>(workspace);
   float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
