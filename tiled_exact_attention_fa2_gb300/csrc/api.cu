@@ -124,6 +124,12 @@ bool make_tmap_out(CUtensorMap* out, const void* base, int heads, int rows, int 
   return encode_rows(out, base, Elem::kBf16, heads, rows, d, d, static_cast<long long>(rows) * d, 32);
 }
 
+// Packed [total, heads, d] bf16 view of the forward output for its TMA
+// stores, box = [1, 32 rows, min(d, 64) columns].
+bool make_tmap_out_packed(CUtensorMap* out, const void* base, int heads, int total, int d) {
+  return encode_rows(out, base, Elem::kBf16, heads, total, d, static_cast<long long>(heads) * d, d, 32);
+}
+
 // Packed [total, heads, d] bf16 view (variable-length batches).
 bool make_tmap_packed(CUtensorMap* out, const void* base, int heads, int total, int d, Elem type = Elem::kBf16) {
   return encode_rows(out, base, type, heads, total, d, static_cast<long long>(heads) * d, d);
@@ -774,7 +780,8 @@ int fa2_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* 
   if (!make_tmap_packed(&tm.q, q, H, total_q, d) || !make_tmap_packed(&tm.k, kb_ptr, H_kv, tk, d) ||
       !make_tmap_packed(&tm.v, vb_ptr, H_kv, tk, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
-  tm.o = tm.q;  // packed batches store O without TMA (a tile may end inside the next sequence)
+  if (!make_tmap_out_packed(&tm.o, o, H, total_q, d))
+    return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (total_k == 0) {  // no keys: V is never read (its maps describe q)
     tm.v16 = tm.v;

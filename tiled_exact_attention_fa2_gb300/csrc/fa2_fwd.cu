@@ -667,13 +667,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
       tc_fence_after();
       const float inv_l = lo > 0.f ? v_scale / lo : 0.f;
-      // Square and split-KV forms with bf16 output: through shared memory and
-      // TMA stores, so the warp does not wait for its rows to reach L2 (TMA
-      // drops the rows past M).  Packed batches store directly: a tile's last
-      // rows may belong to the next sequence.
-      const bool tma_out = C::kTmaOut && MODE != kVarlen && !partial;
+      // bf16 output leaves through shared memory and TMA stores, so the warp
+      // does not wait for its rows to reach L2 (TMA drops the rows past M).
+      // In a packed batch only a warp whose 32 rows all lie in the sequence
+      // does so; the others store directly (their rows past the sequence
+      // belong to the next one).
+      const int row_w0 = w.q0 + x * kTileRows + (warp & 3) * 32;  // this warp's first row
+      const bool tma_out = C::kTmaOut && !partial && (MODE != kVarlen || row_w0 + 32 <= w.M);
       if (tma_out) {
-        const int row_w0 = w.q0 + x * kTileRows + (warp & 3) * 32;  // this warp's first row
         const uint32_t slice = smem_u32(smem + C::kOStage + warp * 4096);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && row_w0 < w.M) {
-            tma_store_3d(&tm_o, slice, 64 * h, row_w0, w.rh);
+            tma_store_3d(&tm_o, slice, 64 * h, w.q_base + row_w0, w.rh);
             bulk_commit_group();
           }
         }

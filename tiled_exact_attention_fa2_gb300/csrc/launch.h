@@ -10,7 +10,7 @@ namespace fa2 {
 // fp16 copy of V the forward pass reads, and of the fp32 dQ accumulator.
 struct TmapSet {
   CUtensorMap q, k, v, v16, dO, dqacc;
-  CUtensorMap o;       // forward output, 32-row boxes (square and split-KV forms, bf16 output)
+  CUtensorMap o;       // forward output (bf16), 32-row boxes
   CUtensorMap dk, dv;  // backward outputs (square form), 128-row boxes
 };
 
