@@ -857,7 +857,8 @@ int fa2_bwd_varlen(const void* q, const void* k, const void* v, const void* o, c
       !make_tmap_packed(&tm.v, v, H_kv, total_k, d) || !make_tmap_packed(&tm.dO, dO, H, total_q, d) ||
       !encode_rows(&tm.dqacc, dq_acc, Elem::kF32, H, total_q, d, static_cast<long long>(H) * d, d))
     return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
-  tm.dk = tm.dv = tm.q;  // packed batches store dK, dV without TMA (a tile may end inside the next sequence)
+  if (!make_tmap_packed(&tm.dk, dk, H_kv, total_k, d) || !make_tmap_packed(&tm.dv, dv, H_kv, total_k, d))
+    return cuda_fail(static_cast<int>(cudaErrorInvalidValue), "tensor map encode");
   // D and the zeroed accumulator in the packed row order ([total_q, H]).
   if (int e = launch_bwd_preprocess(o, dO, Dvec, dq_acc, H, total_q, d, st)) return cuda_fail(e, "bwd preprocess launch");
   BwdProblem p{};

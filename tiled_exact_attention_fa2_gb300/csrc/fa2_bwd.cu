@@ -673,12 +673,13 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (issuer) bulk_wait_group0();  // every reduce / store has landed before the CTA exits
     // ------------------------------------------------------------ epilogue: dV, dK * scale -> bf16
-    // dK, dV of square problems with D >= 64 leave by TMA stores; packed
-    // batches store directly (a tile may end inside the next sequence).
-    constexpr bool kTmaKV = D >= 64 && !VARLEN;
+    // dK, dV (D >= 64) leave by TMA stores; in a packed batch only a key
+    // tile that lies inside its sequence does so (the rows past a sequence
+    // belong to the next one), the others store directly.
+    const bool tma_kv = D >= 64 && (!VARLEN || kv0 + kTileRows <= Nk);
     if (ok && mbar_wait_sleep(&bars[kBarAccFull], 0, status)) {
       tc_fence_after();
-      if constexpr (kTmaKV) {
+      if (tma_kv) {
       // Every MMA has completed, so the Q stages are free: dV goes to stage 0
       // and dK to stage 1 in the layout a TMA load of a K tile produces, and
       // leaves by TMA stores (rows past N are dropped).  The CTA exits once
@@ -714,7 +715,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int b = 0; b < T::kNumBoxes; ++b)
             tma_store_3d(which == 0 ? &tm_dv : &tm_dk, smem_u32(smem + C::kQ + which * T::kTileBytes) + b * T::kBoxBytes,
-                         b * T::kBoxCols, kv0, bh_kv);
+                         b * T::kBoxCols, k_base + kv0, bh_kv);
         bulk_commit_group();
         bulk_wait_group_read0();
       }

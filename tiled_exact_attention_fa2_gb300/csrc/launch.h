@@ -11,7 +11,7 @@ namespace fa2 {
 struct TmapSet {
   CUtensorMap q, k, v, v16, dO, dqacc;
   CUtensorMap o;       // forward output (bf16), 32-row boxes
-  CUtensorMap dk, dv;  // backward outputs (square form), 128-row boxes
+  CUtensorMap dk, dv;  // backward outputs, 128-row boxes
 };
 
 // Launch `kern` on `stream` with programmatic stream serialisation (the
