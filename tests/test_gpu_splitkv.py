@@ -29,6 +29,11 @@ CASES = [
     (4, 16, 4, 1, 16384, 128, True, 16),
     (1, 8, 2, 1, 65536, 128, True, 16),
     (2, 8, 8, 3, 20000, 64, True, 8),      # several queries per sequence, ragged cache
+    # one split: bf16 O straight from the kernel (TMA stores of 32-row boxes
+    # that the few packed rows clip)
+    (1, 8, 2, 1, 700, 128, True, 1),       # 4 packed rows per K/V head
+    (2, 8, 8, 3, 900, 64, False, 1),       # 3 rows per head
+    (1, 16, 4, 40, 1000, 128, True, 1),    # 160 rows: a full and a clipped warp block
 ]
 
 
