@@ -50,8 +50,8 @@ KERNEL_TRAFFIC = {
     # (kernel, workload, causal): (read + write bytes, digest of the sources).
     # Capture summarised in the DRAM-traffic profile of the long causal
     # workload (dram__bytes_read.sum + dram__bytes_write.sum, one launch each).
-    ("fa2_fwd_kernel", "long", True): (405978112 + 117757696, "b8fcaa5fdcbc2afc"),
-    ("fa2_bwd_kernel", "long", True): (835823872 + 505265664, "ee334c7fc2955bad"),
+    ("fa2_fwd_kernel", "long", True): (406438400 + 117232640, "6838d306c9ba247e"),
+    ("fa2_bwd_kernel", "long", True): (835994624 + 505667840, "7449512d1e58f071"),
 }
 
 KERNEL_SOURCES = {
