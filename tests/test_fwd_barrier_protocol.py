@@ -4,11 +4,19 @@
 groups of four softmax warps) through mbarriers waited on by phase parity.
 This model replays each role's sequence of waits, arrivals, TMA loads and
 MMA commits (`protocol_model.Engine`: loads land in any order, one issuer's
-commits in issue order) and checks that no wait is ever two phases away
-from its barrier and that every run ends.  Barrier names and counts follow
-the kernel's FwdBar enum; a unit is the pair (K/V tiles of query tile A,
-K/V tiles of query tile B) that `fwd_unit` computes.  The scheduler
-barriers (one response per unit, read by all eleven roles) are included.
+MMAs and commits complete in issue order) and checks that no wait is ever
+two phases away from its barrier and that every run ends.  Barrier names and
+counts follow the kernel's FwdBar enum; a unit is the pair (K/V tiles of
+query tile A, K/V tiles of query tile B) that `fwd_unit` computes.  K and V
+tiles share one ring of three slots, loaded in the order K_0, (K_j, V_{j-1})
+for j = 1 .. n-1, V_{n-1}.  The scheduler barriers (one response per unit,
+read by all eleven roles) are included.
+
+Besides the barrier phases, the model tracks the data the barriers protect
+and reports a hazard when a protocol step would let one side overwrite what
+the other still reads: a ring slot reloaded while an MMA reads it, S_x
+computed again before every softmax warp has read the previous S_x, P_x
+written while the P V MMA that reads the previous P_x may still run.
 """
 import random
 
@@ -16,31 +24,38 @@ import pytest
 
 from protocol_model import Engine
 
+RING = 3
 
-def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0, one_p_full=False,
-                  phantom_turns_a=False):
-    """Roles of one CTA.  ``dual``: decoding (tile B never has rows), where
-    tile A alternates its S / P / PV barriers between the two S buffers and
-    issues S(j+1) before PV(j)."""
-    rng = random.Random(seed + 7)
 
-    def buf(x, k):  # S buffer (and barrier index) of a tile's k-th S, and its use count
-        return (k & 1, k >> 1) if dual else (x, k)
+def ring_pos_k(j):
+    return 0 if j == 0 else 2 * j - 1
 
-    def p_full(x, k):  # P-full barrier and completion number of a tile's k-th P
-        if one_p_full:  # (one barrier per tile even when S is double-buffered)
-            return ("PFull", x), k
-        b, i = buf(x, k)
-        return ("PFull", b), i
 
+def ring_pos_v(j, n):
+    return 2 * j + 2 if j + 1 < n else 2 * n - 1
+
+
+def forward_roles(e, units, turns=True, planted=None):
+    """Roles of one CTA.  ``planted`` names one deliberate protocol mistake
+    (for the tests that check the model catches it)."""
     for s in range(2):
-        for name, count in (("QFull", 1), ("QEmpty", 1), ("KFull", 1), ("KEmpty", 2), ("VFull", 1),
-                            ("VEmpty", 2), ("SFull", 1), ("PFull", 4), ("PVDone", 1), ("SchedFull", 1),
-                            ("SchedEmpty", 11)):
+        for name, count in (("QFull", 1), ("QEmpty", 1), ("SFull", 1), ("SRead", 4), ("PFull", 4), ("PVDone", 1),
+                            ("SchedFull", 1), ("SchedEmpty", 11)):
             e.bar((name, s), count, f"{name}[{s}]")
+    for s in range(RING):
+        e.bar(("KVFull", s), 1, f"KVFull[{s}]")
+        e.bar(("KVEmpty", s), 2, f"KVEmpty[{s}]")
     for w in range(4):
         e.bar(("TokA", w), 1, f"TokA[{w}]")
         e.bar(("TokB", w), 1, f"TokB[{w}]")
+
+    reading = {sl: set() for sl in range(RING)}  # MMAs in flight that read a ring slot
+    s_read = [[0] * 4 for _ in range(2)]  # S tiles each softmax warp has read, per tile
+    pv_done = [0, 0]  # P V MMAs completed, per tile
+
+    def hazard(msg):
+        if e.error is None:
+            e.error = "hazard: " + msg
 
     def load(key):
         e.unordered(lambda: e.arrive(key))
@@ -49,28 +64,48 @@ def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0
         for key in keys:
             e.ordered(("mma", x), lambda key=key: e.arrive(key))
 
+    def mma_reads(x, slot, use, tag, pv=False):
+        item = (use, x, tag)
+        reading[slot].add(item)
+
+        def done():
+            reading[slot].discard(item)
+            if pv:
+                pv_done[x] += 1
+
+        e.ordered(("mma", x), done)
+
     def producer():
         g, qn = 0, [0, 0]
         for n, (na, nb) in enumerate(units):
+            n_kv = max(na, nb)
+
             def load_q(x):
                 if qn[x] >= 1:
                     yield ("QEmpty", x), qn[x] - 1
                 load(("QFull", x))
                 qn[x] += 1
 
-            if na > 0:
-                yield from load_q(0)
-            for j in range(max(na, nb)):
-                st = g & 1
-                if g >= 2:
-                    yield ("KEmpty", st), (g >> 1) - 1
-                load(("KFull", st))
-                if g >= 2:
-                    yield ("VEmpty", st), (g >> 1) - 1
-                load(("VFull", st))
-                if j == 0 and nb > 0:
-                    yield from load_q(1)
+            def load_kv():
+                nonlocal g
+                slot, use = g % RING, g // RING
+                if use >= 1:
+                    yield ("KVEmpty", slot), use - 1
+                if reading[slot]:
+                    hazard(f"slot {slot} reloaded (use {use}) while MMAs read it: {sorted(reading[slot])}")
+                load(("KVFull", slot))
                 g += 1
+
+            if n_kv > 0:
+                if na > 0:
+                    yield from load_q(0)
+                yield from load_kv()
+                if nb > 0:
+                    yield from load_q(1)
+                for _ in range(1, n_kv):
+                    yield from load_kv()  # K_j
+                    yield from load_kv()  # V_{j-1}
+                yield from load_kv()  # V_{n-1}
             if n >= 2:
                 yield ("SchedEmpty", n & 1), (n >> 1) - 1
             load(("SchedFull", n & 1))
@@ -79,54 +114,60 @@ def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0
 
     def issuer(x):
         g = k = qn = 0
+
+        def full(pos):
+            return ("KVFull", pos % RING), pos // RING
+
+        def issue_s(pos, kk, last_q):
+            if min(s_read[x]) < kk:
+                hazard(f"S_{'AB'[x]} #{kk} computed before every warp read S #{kk - 1}")
+            mma_reads(x, pos % RING, pos // RING, f"S{kk}")
+            commit(x, ("SFull", x), ("KVEmpty", pos % RING), *([("QEmpty", x)] if last_q else []))
+
         for n, cnt in enumerate(units):
             n_kv, nx = max(cnt), cnt[x]
             if n_kv > 0:
-                def s_ready(kk):  # S number kk may overwrite its buffer
-                    prev = kk - 2 if dual else kk - 1
-                    if prev >= 0:
-                        b, i = buf(x, prev)
-                        yield ("PVDone", b), i
-
-                def issue_s(kk, st, last):
-                    b, _ = buf(x, kk)
-                    commit(x, ("SFull", b), ("KEmpty", st), *([("QEmpty", x)] if last else []))
-
                 if nx > 0:
                     yield ("QFull", x), qn
                     qn += 1
-                    yield from s_ready(k)
-                    yield ("KFull", g & 1), g >> 1
-                    issue_s(k, g & 1, nx == 1)
+                    if k >= 1:
+                        yield ("SRead", x), k - 1
+                    yield full(g)
+                    issue_s(g, k, nx == 1)
                 for j in range(nx):
-                    gj = g + j
-                    st = gj & 1
-                    if dual and j + 1 < nx:
-                        yield from s_ready(k + 1)
-                        yield ("KFull", st ^ 1), (gj + 1) >> 1
-                        issue_s(k + 1, st ^ 1, j + 2 == nx)
-                    yield ("VFull", st), gj >> 1
-                    yield p_full(x, k)
-                    b, _ = buf(x, k)
-                    commit(x, ("PVDone", b), ("VEmpty", st))
+                    if j + 1 < nx:
+                        pk = g + ring_pos_k(j + 1)
+                        if planted != "s_before_read":
+                            yield ("SRead", x), k
+                        yield full(pk)
+                        issue_s(pk, k + 1, j + 2 == nx)
+                    pv = g + ring_pos_v(j, n_kv)
+                    yield full(pv)
+                    yield ("PFull", x), k
+                    mma_reads(x, pv % RING, pv // RING, f"PV{k}", pv=True)
+                    commit(x, ("PVDone", x), ("KVEmpty", pv % RING))
                     k += 1
-                    if not dual and j + 1 < nx:
-                        yield from s_ready(k)
-                        yield ("KFull", st ^ 1), (gj + 1) >> 1
-                        issue_s(k, st ^ 1, j + 2 == nx)
-                for j in range(nx, n_kv):  # K/V tiles this issuer does not visit
-                    gj = g + j
-                    st = gj & 1
-                    if skip_full_waits:
-                        yield ("KFull", st), gj >> 1
-                        yield ("VFull", st), gj >> 1
-                    if gj >= 2:
-                        yield ("KEmpty", st), (gj >> 1) - 1
-                    e.arrive(("KEmpty", st))
-                    if gj >= 2:
-                        yield ("VEmpty", st), (gj >> 1) - 1
-                    e.arrive(("VEmpty", st))
-                g += n_kv
+                # ring positions of the tiles this query tile does not visit
+                start = g + (0 if nx == 0 else ring_pos_k(nx))
+                for pos in range(start, g + 2 * n_kv):
+                    rel = pos - g
+                    if rel == 0:
+                        mine = nx > 0
+                    elif rel == 2 * n_kv - 1:
+                        mine = nx == n_kv
+                    elif rel & 1:
+                        mine = (rel + 1) // 2 < nx
+                    else:
+                        mine = (rel - 2) // 2 < nx
+                    if mine:
+                        continue
+                    slot, use = pos % RING, pos // RING
+                    if planted != "release_without_full":
+                        yield full(pos)
+                    if use >= 1:
+                        yield ("KVEmpty", slot), use - 1
+                    e.arrive(("KVEmpty", slot))
+                g += 2 * n_kv
             yield ("SchedFull", n & 1), n >> 1
             e.arrive(("SchedEmpty", n & 1))
 
@@ -136,28 +177,31 @@ def forward_roles(e, units, skip_full_waits=True, turns=True, dual=False, seed=0
         for n, cnt in enumerate(units):
             nx = cnt[x]
             # turns only for the K/V tiles both query tiles visit
-            n_turns = min(cnt) if (turns and not dual and min(cnt) > 0) else 0
-            if phantom_turns_a and x == 0 and n_turns:  # planted: tile A also takes turns for B's extra tiles
+            n_turns = min(cnt) if (turns and min(cnt) > 0) else 0
+            if planted == "phantom_turns_a" and x == 0 and n_turns:  # tile A also takes B's extra turns
                 n_turns = max(cnt)
             for j in range(max(nx, n_turns)):
                 if j < nx:
-                    b, i = buf(x, k)
-                    yield ("SFull", b), i
+                    yield ("SFull", x), k
+                    s_read[x][w] += 1
+                    e.arrive(("SRead", x))
                 if j < n_turns:
                     t = tn if x else tn - 1
                     if t >= 0:
                         yield tok_wait, t
+                if j < nx:
+                    if k >= 1 and planted != "p_before_pv_done":
+                        yield ("PVDone", x), k - 1
+                    if pv_done[x] < k:
+                        hazard(f"P_{'AB'[x]} #{k} written while P V #{k - 1} may still read P")
+                if j < n_turns:
                     e.arrive(tok_pass)
                     tn += 1
                 if j < nx:
-                    if dual and j >= 1 and rng.random() < 0.5:  # O rescale waits for PV(k - 1)
-                        pb, pi = buf(x, k - 1)
-                        yield ("PVDone", pb), pi
-                    e.arrive(p_full(x, k)[0])
+                    e.arrive(("PFull", x))
                     k += 1
             if nx > 0:
-                pb, pi = buf(x, k - 1)
-                yield ("PVDone", pb), pi
+                yield ("PVDone", x), k - 1
             yield ("SchedFull", n & 1), n >> 1
             e.arrive(("SchedEmpty", n & 1))
 
@@ -175,12 +219,14 @@ def _units(rng, kind):
         r = rng.random()
         if kind == "causal" or r < 0.4:
             out.append((2 * p + 1, 2 * p + 2))   # square causal pair: tile B sees one more K/V tile
-        elif r < 0.6:
+        elif r < 0.55:
             out.append((p + 1, 0))               # tile B past the last row
-        elif r < 0.7:
+        elif r < 0.65:
             out.append((0, p + 1))               # tile A sees no key (N_q > N_k alignment)
-        elif r < 0.85:
+        elif r < 0.8:
             out.append((p + 1, p + 3))           # general causal offsets
+        elif r < 0.9:
+            out.append((p + 3, p + 1))           # tile A sees more (key splits)
         else:
             out.append((p + 1, p + 1))           # non-causal
     return out
@@ -188,62 +234,53 @@ def _units(rng, kind):
 
 def _run(units, seed, **kw):
     e = Engine(seed)
-    return e.run(forward_roles(e, units, seed=seed, **kw))
+    return e.run(forward_roles(e, units, **kw))
 
 
 @pytest.mark.parametrize("kind", ["causal", "mixed"])
-def test_forward_protocol_has_no_deadlock_or_parity_aliasing(kind):
+def test_forward_protocol_has_no_deadlock_parity_aliasing_or_hazard(kind):
     for seed in range(400):
         units = _units(random.Random(seed), kind)
         result = _run(units, seed)
         assert result is None, f"seed {seed}, units {units}: {result}"
 
 
-def test_model_catches_a_release_without_the_full_waits():
-    # Releasing a skipped K/V tile without first taking its full phases lets
-    # the issuer's next wait on that stage pass on an older load's parity.
-    found = None
-    for seed in range(3000):
-        units = _units(random.Random(seed), "mixed")
-        found = _run(units, seed, skip_full_waits=False)
-        if found:
-            break
-    assert found and "parity wait passes early" in found
-
-
-def test_decode_protocol_has_no_deadlock_or_parity_aliasing():
+def test_decode_protocol_has_no_deadlock_parity_aliasing_or_hazard():
     # Decoding: every unit is (K/V tiles of its split, 0).
-    for seed in range(400):
+    for seed in range(300):
         rng = random.Random(seed)
         units = [(rng.randint(1, 9), 0) for _ in range(rng.randint(1, 5))]
-        result = _run(units, seed, dual=True)
+        result = _run(units, seed)
         assert result is None, f"seed {seed}, units {units}: {result}"
 
 
-def test_model_catches_a_single_p_full_barrier_in_decode():
-    # One P-full barrier per tile while S is double-buffered lets a fast
-    # softmax warp arrive for P(j+1) before a slow one has arrived for P(j):
-    # the phase completes with arrivals of two tiles, PV(j) and S(j+2) go
-    # out early, and the slow warp ends up two phases behind.
-    found = None
-    for seed in range(2000):
-        rng = random.Random(seed)
-        units = [(rng.randint(2, 9), 0) for _ in range(rng.randint(1, 3))]
-        e = Engine(seed)
-        found = e.run(forward_roles(e, units, dual=True, seed=seed, one_p_full=True))
+def _first_failure(planted, kind="mixed", seeds=3000):
+    for seed in range(seeds):
+        found = _run(_units(random.Random(seed), kind), seed, planted=planted)
         if found:
-            break
-    assert found and "two phases" in found
+            return found
+    return None
+
+
+def test_model_catches_a_release_without_the_full_wait():
+    # Releasing a skipped K/V tile without first taking its full phase lets
+    # the issuer's next wait on that slot pass on an older load's parity.
+    found = _first_failure("release_without_full")
+    assert found and "parity wait passes early" in found
+
+
+def test_model_catches_s_computed_before_the_softmax_read_it():
+    found = _first_failure("s_before_read")
+    assert found and "computed before every warp read" in found
+
+
+def test_model_catches_p_written_while_the_previous_p_v_may_run():
+    found = _first_failure("p_before_pv_done")
+    assert found and "may still read P" in found
 
 
 def test_model_catches_turns_taken_by_one_tile_only():
     # Tile A taking turns for the K/V tiles only tile B visits (while B
     # takes turns only for the shared ones) puts the two token barriers out
     # of step: a waiter ends up two phases behind or waits forever.
-    found = None
-    for seed in range(2000):
-        units = _units(random.Random(seed), "causal")
-        found = _run(units, seed, phantom_turns_a=True)
-        if found:
-            break
-    assert found
+    assert _first_failure("phantom_turns_a", kind="causal", seeds=2000)

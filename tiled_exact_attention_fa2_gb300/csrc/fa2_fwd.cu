@@ -17,24 +17,29 @@
 // other tile's softmax runs:
 //   warps 0-3  softmax of tile A   (thread t owns row t = TMEM lane t)
 //   warps 4-7  softmax of tile B
-//   warp  8    TMA producer: Q_A, Q_B per unit, then K_j / V_j into 2-stage rings
+//   warp  8    TMA producer: Q_A, Q_B per unit, K / V tiles through one 3-slot ring
 //   warp  9    MMA issuer for tile A (one thread) + TMEM owner
 //   warp 10    MMA issuer for tile B (one thread)
 // One issuer per tile, so that waiting on one tile's MMA never delays the
-// other tile's; K/V stages are released once both issuers are done with them.
-// TMEM columns: S_A [0,128), S_B [128,256), O_A and O_B after them.  The
-// softmax overwrites the first 64 columns of S_X with P_X (fp16 pairs) and
-// O_X += P_X V_j reads P_X straight from TMEM (A operand in TMEM), so P never
-// touches shared memory.  P V runs on fp16 operands, with V read from an
-// fp16 copy that fa2_v_to_f16_kernel writes before the forward kernel runs:
-// fp16 keeps three more significant bits than bf16, and with bf16 weights
-// their rounding alone moves O by up to about 0.2 % on rows dominated by a
-// few keys.  A K/V head holding a finite value beyond the fp16 range is
-// copied scaled by a power of two, which the epilogue multiplies back.  The
-// split-KV form (decoding), whose time is the single read of the cache,
-// runs P V in bf16 on V itself.  S_X(j+1) is issued only after P_X(j) V_j has
-// completed, because it overwrites the columns that MMA reads (decoding,
-// where tile B is empty, double-buffers S over both ranges instead).
+// other tile's; ring slots are released once both issuers are done with them.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A and O_B after them (all 512).
+// P_X goes from the softmax registers to shared memory (128 x 128 16-bit
+// weights per tile, the K-major A operand of O_X += P_X V_j), so S_X(j+1)
+// can be computed into S_X as soon as the softmax has read S_X(j) into
+// registers, while the exponentials of tile j still run: the chain
+// S -> softmax -> P V -> S of one tile no longer serialises the tensor core.
+// The shared memory that takes (2 x 32 KB) comes from the K/V staging: K and
+// V share three 32 KB slots, filled in the order the MMAs use them (K_0, K_1,
+// V_0, K_2, V_1, ...).  P V runs on fp16 operands, with V read from an fp16
+// copy that fa2_v_to_f16_kernel writes before the forward kernel runs: fp16
+// keeps three more significant bits than bf16, and with bf16 weights their
+// rounding alone moves O by up to about 0.2 % on rows dominated by a few
+// keys.  A K/V head holding a finite value beyond the fp16 range is copied
+// scaled by a power of two, which the epilogue multiplies back.  The split-KV
+// form (decoding), whose time is the single read of the cache, runs P V in
+// bf16 on V itself.  A barrier wait costs well over a hundred cycles even
+// when its phase has completed, so waits that are usually already satisfied
+// are tested early without blocking and only waited on when the test failed.
 // The reference value m that the exponentials subtract is raised only when a
 // tile's row max exceeds it by more than a slack (15 or 8 log2 units), so the
 // weights stay below 2^slack and O is rescaled in TMEM (for the whole
@@ -72,22 +77,28 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleSlackF16 = 15.f, kRescaleSlackBf16 = 8.f;
 
 enum FwdBar {
-  kBarQFull = 0,    // +tile (A, B)
-  kBarKFull = 2,    // +stage (2)
-  kBarKEmpty = 4,   // +stage
-  kBarVFull = 6,    // +stage
-  kBarVEmpty = 8,   // +stage
-  kBarSFull = 10,   // +tile
-  kBarPFull = 12,   // +tile, 4 warp arrivals
-  kBarPVDone = 14,  // +tile
-  kBarDrain = 16,   // +tile
-  kBarQEmpty = 18,      // +tile: the tile's issuer is done with its Q tile of a unit
+  kBarQFull = 0,        // +tile (A, B)
+  kBarQEmpty = 2,       // +tile: the tile's issuer is done with its Q tile of a unit
+  kBarKVFull = 4,       // +ring slot (3)
+  kBarKVEmpty = 7,      // +ring slot, one arrival per issuer
+  kBarSFull = 10,       // +tile
+  kBarSRead = 12,       // +tile, 4 warp arrivals: S_x is in registers, the next S may overwrite it
+  kBarPFull = 14,       // +tile, 4 warp arrivals: P_x is in shared memory
+  kBarPVDone = 16,      // +tile
+  kBarDrain = 18,       // +tile
   kBarSchedFull = 20,   // +slot (2): scheduler response landed (16 transaction bytes)
   kBarSchedEmpty = 22,  // +slot: every role has read the response (kSchedReaders arrivals)
   kBarTokA = 24,        // +SMSP slot (4): softmax warp of tile A may start its exponentials
   kBarTokB = 28,        // +SMSP slot (4): softmax warp of tile B may start its exponentials
   kNumFwdBars = 32,
 };
+
+// K and V tiles share one ring of three slots, loaded in the order the MMAs
+// use them: K_0, then (K_j, V_{j-1}) for j = 1 .. n-1, then V_{n-1}.  Ring
+// position of a unit's K_j / V_j (n K/V tiles in the unit).
+__device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int ring_pos_v(int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; }
+constexpr int kRingSlots = 3;
 
 template <int D>
 struct FwdCfg {
@@ -96,13 +107,14 @@ struct FwdCfg {
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + kCols;
   static constexpr int kQ = 0;  // Q_A, Q_B
-  static constexpr int kK = kQ + 2 * T::kTileBytes;
-  static constexpr int kV = kK + 2 * T::kTileBytes;
-  // O leaves through one 4 KB slice per softmax warp (its 32 rows x 64
-  // columns, 128B-swizzled) and a TMA store, for D >= 64.
+  static constexpr int kKV = kQ + 2 * T::kTileBytes;  // K/V ring
+  // P_A, P_B: 128 x 128 16-bit weights each, K-major (Square layout), the A
+  // operand of O += P V.  A softmax warp's 32 rows of P_x also stage its O
+  // rows for the TMA stores (32 rows x 64 columns = 4 KB per half, D >= 64).
+  static constexpr int kP = kKV + kRingSlots * T::kTileBytes;
+  static constexpr int kPBytes = kTileRows * kTileRows * 2;
   static constexpr bool kTmaOut = D >= 64;
-  static constexpr int kOStage = kV + 2 * T::kTileBytes;
-  static constexpr int kBars = kOStage + (kTmaOut ? 8 * 4096 : 0);
+  static constexpr int kBars = kP + 2 * kPBytes;
   static constexpr int kSched = (kBars + kNumFwdBars * 8 + 15) / 16 * 16;  // 2 x 16-byte responses
   static constexpr int kTmemSlot = kSched + 32;
   static constexpr int kUsed = kTmemSlot + 16;
@@ -243,11 +255,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int lane = lane_id();
   const int num_row_tiles = (p.M + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_row_tiles + 1) / 2;
-  // Decoding (split-KV with at most 128 packed rows per row-head): tile B
-  // never has rows, so tile A double-buffers S over both S column ranges
-  // (and uses tile B's S-full / P-full / PV-done barriers for the second
-  // buffer): S(j+1) is computed while the softmax of tile j runs.
-  const bool dual = MODE == kGeneral && num_row_tiles == 1;
 
   if (threadIdx.x == 8 * 32) {
     for (int s = 0; s < 2; ++s) {
@@ -255,14 +262,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars[kBarQEmpty + s], 1);
       mbar_init(&bars[kBarSchedFull + s], 1);
       mbar_init(&bars[kBarSchedEmpty + s], kSchedReaders);
-      mbar_init(&bars[kBarKFull + s], 1);
-      mbar_init(&bars[kBarKEmpty + s], 2);
-      mbar_init(&bars[kBarVFull + s], 1);
-      mbar_init(&bars[kBarVEmpty + s], 2);
       mbar_init(&bars[kBarSFull + s], 1);
+      mbar_init(&bars[kBarSRead + s], 4);
       mbar_init(&bars[kBarPFull + s], 4);
       mbar_init(&bars[kBarPVDone + s], 1);
       mbar_init(&bars[kBarDrain + s], 1);
+    }
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(&bars[kBarKVFull + s], 1);
+      mbar_init(&bars[kBarKVEmpty + s], 2);
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars[kBarTokA + s], 1);
@@ -287,9 +295,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int g = 0;   // K/V tiles loaded so far (stage g & 1, use g >> 1)
+      int g = 0;             // ring loads so far (slot g % 3, use g / 3)
       int qn0 = 0, qn1 = 0;  // Q_A / Q_B tiles loaded so far
-      int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;  // last tile armed per stage
+      int last_use[kRingSlots] = {-1, -1, -1};  // last use armed per slot
       bool ok = true;
       int pending = -1;  // scheduler request issued but not yet read here
 #pragma unroll 1
@@ -299,8 +307,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int n_kv = max(w.cnt[0], w.cnt[1]);
         if (!w.valid || n_kv == 0) break;
         // Q_x smem is free once issuer x's last S of its previous unit is
-        // done.  Order: Q_A, K/V tile 0, Q_B, then the other K/V tiles, so
-        // tile A can start the unit while tile B still finishes the last one.
+        // done.  Order: Q_A, K_0, Q_B, then the rest of the ring, so tile A
+        // can start the unit while tile B still finishes the last one.
         auto load_q = [&](int x) -> bool {
           int& qn = x ? qn1 : qn0;
           if (qn >= 1 && !mbar_wait(&bars[kBarQEmpty + x], (qn - 1) & 1, status)) return false;
@@ -311,27 +319,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ++qn;
           return true;
         };
+        // K_j (v = false) or V_j into the next ring slot, once both issuers
+        // have released the slot's previous tile.
+        auto load_kv = [&](bool v, int j) -> bool {
+          const int slot = g % kRingSlots, use = g / kRingSlots;
+          if (use >= 1 && !mbar_wait(&bars[kBarKVEmpty + slot], (use - 1) & 1, status)) return false;
+          mbar_arrive_expect_tx(&bars[kBarKVFull + slot], T::kTileBytes);
+          for (int b = 0; b < T::kNumBoxes; ++b)
+            tma_load_3d(smem + C::kKV + slot * T::kTileBytes + b * T::kBoxBytes, v ? &tm_v : &tm_k,
+                        &bars[kBarKVFull + slot], b * T::kBoxCols, w.k_base + (w.jb + j) * kTileRows, w.rh_kv);
+          last_use[slot] = use;
+          ++g;
+          return true;
+        };
         if (w.cnt[0] > 0 && !(ok = load_q(0))) break;
+        if (!(ok = load_kv(false, 0))) break;
+        if (w.cnt[1] > 0 && !(ok = load_q(1))) break;
 #pragma unroll 1
-        for (int j = 0; j < n_kv; ++j, ++g) {
-          const int st = g & 1;
-          if (g >= 2 && !(ok = mbar_wait(&bars[kBarKEmpty + st], ((g >> 1) - 1) & 1, status))) break;
-          mbar_arrive_expect_tx(&bars[kBarKFull + st], T::kTileBytes);
-          for (int b = 0; b < T::kNumBoxes; ++b)
-            tma_load_3d(smem + C::kK + st * T::kTileBytes + b * T::kBoxBytes, &tm_k, &bars[kBarKFull + st],
-                        b * T::kBoxCols, w.k_base + (w.jb + j) * kTileRows, w.rh_kv);
-          (st ? last_k1 : last_k0) = g;
-          if (g >= 2 && !(ok = mbar_wait(&bars[kBarVEmpty + st], ((g >> 1) - 1) & 1, status))) break;
-          mbar_arrive_expect_tx(&bars[kBarVFull + st], T::kTileBytes);
-          for (int b = 0; b < T::kNumBoxes; ++b)
-            tma_load_3d(smem + C::kV + st * T::kTileBytes + b * T::kBoxBytes, &tm_v, &bars[kBarVFull + st],
-                        b * T::kBoxCols, w.k_base + (w.jb + j) * kTileRows, w.rh_kv);
-          (st ? last_v1 : last_v0) = g;
-          if (j == 0 && w.cnt[1] > 0 && !(ok = load_q(1))) break;
-        }
+        for (int j = 1; j < n_kv; ++j)
+          if (!(ok = load_kv(false, j) && load_kv(true, j - 1))) break;
+        if (!ok) break;
+        if (!(ok = load_kv(true, n_kv - 1))) break;
         } while (false);
         if (!ok) break;
-        // Every load of this unit is issued (about two K/V tiles ahead of the
+        // Every load of this unit is issued (about a K/V tile ahead of the
         // MMAs): ask for the next unit now, late enough that CTAs which
         // finish first take the remaining units.  Slot n & 1 is free once
         // every reader has taken request n - 2's answer.
@@ -349,55 +360,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // wait for the last completion of every full barrier that was armed.
       if (qn0 >= 1) mbar_wait(&bars[kBarQFull + 0], (qn0 - 1) & 1, status);
       if (qn1 >= 1) mbar_wait(&bars[kBarQFull + 1], (qn1 - 1) & 1, status);
-      if (last_k0 >= 0) mbar_wait(&bars[kBarKFull + 0], (last_k0 >> 1) & 1, status);
-      if (last_k1 >= 0) mbar_wait(&bars[kBarKFull + 1], (last_k1 >> 1) & 1, status);
-      if (last_v0 >= 0) mbar_wait(&bars[kBarVFull + 0], (last_v0 >> 1) & 1, status);
-      if (last_v1 >= 0) mbar_wait(&bars[kBarVFull + 1], (last_v1 >> 1) & 1, status);
+      for (int s = 0; s < kRingSlots; ++s)
+        if (last_use[s] >= 0) mbar_wait(&bars[kBarKVFull + s], last_use[s] & 1, status);
     }
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------ MMA issuer of tile x
     if (lane == 0) {
       const int x = warp - 9;
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q (K-major) x K (K-major)
-      // P (TMEM) x V (MN-major)
+      // P (K-major) x V (MN-major)
       constexpr uint32_t kIdescO = kF16 ? make_idesc_f16(128, D, false, true) : make_idesc_bf16(128, D, false, true);
-      const uint32_t sQ0 = smem_u32(smem + C::kQ), sK0 = smem_u32(smem + C::kK), sV0 = smem_u32(smem + C::kV);
+      const uint32_t sQ0 = smem_u32(smem + C::kQ), sKV0 = smem_u32(smem + C::kKV);
+      const uint32_t sP = smem_u32(smem + C::kP) + x * C::kPBytes;
+      const uint32_t tSx = tmem + (x ? C::kColS1 : C::kColS0);
       const uint32_t tOx = tmem + (x ? C::kColO1 : C::kColO0);
-      // S buffer of the tile's k-th S: S_x, or S_A / S_B alternately when dual.
-      auto sbuf = [&](int kk) { return dual ? (kk & 1) : x; };
-      auto sphase = [&](int kk) { return dual ? (kk >> 1) & 1 : kk & 1; };
-      // S = Q_x K^T for the K/V tile in stage st, into S buffer b.
-      auto issue_s = [&](int st, int b) {
-        uint32_t sQ = sQ0, sK = sK0;
+      auto full = [&](int pos) {  // wait for the ring tile at global position pos
+        return mbar_wait(&bars[kBarKVFull + pos % kRingSlots], (pos / kRingSlots) & 1, status);
+      };
+      // S_x = Q_x K^T, K in ring position pos.
+      auto issue_s = [&](int pos) {
+        uint32_t sQ = sQ0, sKV = sKV0;
         opaque(sQ);
-        opaque(sK);
-        const uint32_t qb = sQ + x * T::kTileBytes, kb = sK + st * T::kTileBytes;
-        const uint32_t tS = tmem + (b ? C::kColS1 : C::kColS0);
+        opaque(sKV);
+        const uint32_t qb = sQ + x * T::kTileBytes, kb = sKV + (pos % kRingSlots) * T::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tS, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
-        mma_commit(&bars[kBarSFull + b]);
-        mma_commit(&bars[kBarKEmpty + st]);
+          mma_bf16_ss(tSx, T::kmajor_desc(qb, kk), T::kmajor_desc(kb, kk), kIdescS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kBarSFull + x]);
+        mma_commit(&bars[kBarKVEmpty + pos % kRingSlots]);
       };
-      // O_x (+)= P V with P read from the first 64 columns of S buffer b.
-      auto issue_pv = [&](int st, bool first, int b) {
-        uint32_t sV = sV0;
-        opaque(sV);
-        const uint32_t vb = sV + st * T::kTileBytes;
-        const uint32_t tP = tmem + (b ? C::kColS1 : C::kColS0);
+      // O_x (+)= P_x V, V in ring position pos.
+      auto issue_pv = [&](int pos, bool first) {
+        uint32_t sKV = sKV0;
+        opaque(sKV);
+        const uint32_t vb = sKV + (pos % kRingSlots) * T::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_ts(tOx, tP + kk * 8, T::mnmajor_desc(vb, kk), kIdescO, (!first || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarPVDone + b]);
-        mma_commit(&bars[kBarVEmpty + st]);
+          mma_bf16_ss(tOx, Square::kmajor_desc(sP, kk), T::mnmajor_desc(vb, kk), kIdescO,
+                      (!first || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarPVDone + x]);
+        mma_commit(&bars[kBarKVEmpty + pos % kRingSlots]);
       };
-      // S number kk may overwrite its buffer once the PV that last read it
-      // (number kk - 2 when dual, kk - 1 otherwise) has completed.
-      auto s_ready = [&](int kk) -> bool {
-        const int prev = dual ? kk - 2 : kk - 1;
-        return prev < 0 || mbar_wait(&bars[kBarPVDone + sbuf(prev)], sphase(prev), status);
-      };
-      int g = 0;   // K/V tiles of all units so far (same count as the producer's)
+      int g = 0;   // ring position of the current unit's first tile (same count as the producer's)
       int k = 0;   // S_x / P_x / PV_x issued so far (phase k & 1)
       int qn = 0;  // units whose Q_x tile was loaded so far
       bool ok = true;
@@ -408,60 +412,55 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int n_kv = max(w.cnt[0], w.cnt[1]);
         if (!w.valid || n_kv == 0) break;
         const int nx = x ? w.cnt[1] : w.cnt[0];  // (selects keep the struct in registers)
+        // Order: S(0); then per tile j: S(j+1) as soon as the softmax has
+        // read S(j) into registers, then PV(j) once P(j) is in shared memory.
+        // S(k) overwrites S_x: it waits for the softmax to have read S(k-1).
         if (nx > 0) {
           if (!(ok = mbar_wait(&bars[kBarQFull + x], qn & 1, status))) break;
           ++qn;
-        }
-        // Order: S(0); then per tile j: [dual: S(j+1)], PV(j), [else: S(j+1)].
-        if (nx > 0) {
-          const int st = g & 1;
-          if (!(ok = s_ready(k) && mbar_wait(&bars[kBarKFull + st], (g >> 1) & 1, status))) break;
+          if (!(ok = (k == 0 || mbar_wait(&bars[kBarSRead + x], (k - 1) & 1, status)) && full(g))) break;
           tc_fence_after();
-          issue_s(st, sbuf(k));
+          issue_s(g);
           if (nx == 1) mma_commit(&bars[kBarQEmpty + x]);  // last use of Q_x in this unit
         }
 #pragma unroll 1
         for (int j = 0; j < nx; ++j) {
-          const int gj = g + j, st = gj & 1, st1 = st ^ 1;
-          if (dual && j + 1 < nx) {
-            if (!(ok = s_ready(k + 1) && mbar_wait(&bars[kBarKFull + st1], ((gj + 1) >> 1) & 1, status))) break;
+          if (j + 1 < nx) {
+            const int pk = g + ring_pos_k(j + 1);
+            if (!(ok = mbar_wait2(&bars[kBarSRead + x], k & 1, &bars[kBarKVFull + pk % kRingSlots], (pk / kRingSlots) & 1, status))) break;
             tc_fence_after();
-            issue_s(st1, sbuf(k + 1));
+            issue_s(pk);
             if (j + 2 == nx) mma_commit(&bars[kBarQEmpty + x]);
           }
-          if (!(ok = mbar_wait(&bars[kBarVFull + st], (gj >> 1) & 1, status))) break;
-          // (P-full barriers are per S buffer too: with S(j+1) already issued
-          // the softmax can finish P(j+1) before this wait, and one barrier
-          // would then be two phases ahead.)
-          if (!(ok = mbar_wait(&bars[kBarPFull + sbuf(k)], sphase(k), status))) break;
+          const int pv = g + ring_pos_v(j, n_kv);
+          if (!(ok = mbar_wait2(&bars[kBarKVFull + pv % kRingSlots], (pv / kRingSlots) & 1, &bars[kBarPFull + x], k & 1, status))) break;
           tc_fence_after();
-          issue_pv(st, j == 0, sbuf(k));
+          issue_pv(pv, j == 0);
           ++k;
-          if (!dual && j + 1 < nx) {
-            // S_x(j+1) overwrites the P_x columns the PV above reads.
-            if (!(ok = s_ready(k) && mbar_wait(&bars[kBarKFull + st1], ((gj + 1) >> 1) & 1, status))) break;
-            tc_fence_after();
-            issue_s(st1, sbuf(k));
-            if (j + 2 == nx) mma_commit(&bars[kBarQEmpty + x]);
-          }
         }
         if (!ok) break;
-        // K/V tiles this query tile does not visit: release them once, in
-        // phase order (after the stage's previous use has been released).
+        // K/V tiles this query tile does not visit (those from K_nx on, all
+        // at ring positions after every tile it used except V_{nx-1}):
+        // release them in ring order, each after taking its full phase (so
+        // that this issuer's next wait on the slot is never two phases ahead
+        // of the loads; the load also implies that the slot's previous use
+        // has been released) and after the slot's previous phase is seen
+        // complete.
 #pragma unroll 1
-        for (int j = nx; j < n_kv; ++j) {
-          const int gj = g + j, st = gj & 1;
-          // Take the tile's full phases too, so that this issuer's next wait
-          // on the stage is never two phases ahead of the loads.
-          if (!(ok = mbar_wait(&bars[kBarKFull + st], (gj >> 1) & 1, status) &&
-                     mbar_wait(&bars[kBarVFull + st], (gj >> 1) & 1, status)))
-            break;
-          if (gj >= 2 && !(ok = mbar_wait(&bars[kBarKEmpty + st], ((gj >> 1) - 1) & 1, status))) break;
-          mbar_arrive(&bars[kBarKEmpty + st]);
-          if (gj >= 2 && !(ok = mbar_wait(&bars[kBarVEmpty + st], ((gj >> 1) - 1) & 1, status))) break;
-          mbar_arrive(&bars[kBarVEmpty + st]);
+        for (int pos = g + (nx == 0 ? 0 : ring_pos_k(nx)); pos < g + 2 * n_kv; ++pos) {
+          bool mine;  // is pos a tile this issuer used?
+          const int rel = pos - g;
+          if (rel == 0) mine = nx > 0;
+          else if (rel == 2 * n_kv - 1) mine = nx == n_kv;  // V_{n-1}
+          else if (rel & 1) mine = (rel + 1) / 2 < nx;      // K_{(rel+1)/2}
+          else mine = (rel - 2) / 2 < nx;                   // V_{(rel-2)/2}
+          if (mine) continue;
+          const int slot = pos % kRingSlots, use = pos / kRingSlots;
+          if (!(ok = full(pos))) break;
+          if (use >= 1 && !(ok = mbar_wait(&bars[kBarKVEmpty + slot], (use - 1) & 1, status))) break;
+          mbar_arrive(&bars[kBarKVEmpty + slot]);
         }
-        g += n_kv;
+        g += 2 * n_kv;
         } while (false);
         if (!ok) break;
         u = next_unit(bars, sched, n, true, status, ok);
@@ -475,11 +474,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int x = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (x ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_base + (x ? C::kColO1 : C::kColO0);
+    const uint32_t sP = smem_u32(smem + C::kP) + x * C::kPBytes;
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-    // S buffer / barrier phase of the tile's kk-th S (see the issuer).
-    auto sbuf = [&](int kk) { return dual ? (kk & 1) : x; };
-    auto sphase = [&](int kk) { return dual ? (kk >> 1) & 1 : kk & 1; };
     int k = 0;  // S_x tiles consumed so far
     // Softmax warps w (tile A) and w + 4 (tile B) share an SMSP and take
     // turns at the exponentials, so that the two never contend for its MUFU
@@ -510,7 +508,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!w.valid) break;
       const int nx = x ? w.cnt[1] : w.cnt[0];  // (selects keep the struct in registers)
       // Turns are taken only in units where both tiles have K/V tiles.
-      const int turns = (!dual && w.cnt[0] > 0 && w.cnt[1] > 0) ? min(w.cnt[0], w.cnt[1]) : 0;
+      const int turns = (w.cnt[0] > 0 && w.cnt[1] > 0) ? min(w.cnt[0], w.cnt[1]) : 0;
       const int q_row = w.q0 + x * kTileRows + r;              // row in the row-head
       const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
       const int imin_x = x ? w.imin[1] : w.imin[0];
@@ -519,20 +517,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float v_scale = (kF16 && p.v_scale != nullptr) ? __ldg(p.v_scale + w.rh_kv) : 1.f;
       float m = -INFINITY;  // reference max, log2 units (scores * scale * log2 e); row max - m <= slack
       float l = 0.f;        // running sum of 2^(x - m) (fp32 weights: the LSE)
-      float lo = 0.f;       // the same with each tile's largest weight as bf16 (normalises O)
+      float lo = 0.f;       // the same with each tile's largest weight as 16-bit (normalises O)
 #pragma unroll 1
       for (int j = 0; j < nx; ++j, ++k) {
-        // Without dual buffering S_x(j) was issued after O_x += P_x(j-1)
-        // V_{j-1} completed, so O_x is stable once S_x(j) has landed; with it,
-        // the O rescale below waits for that PV first.
-        const int b = sbuf(k);
-        if (!(ok = mbar_wait(&bars[kBarSFull + b], sphase(k), status))) break;
+        if (!(ok = mbar_wait(&bars[kBarSFull + x], k & 1, status))) break;
         tc_fence_after();
-        const uint32_t tS = tmem + lane_base + (b ? C::kColS1 : C::kColS0);
         float s[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + 32 * c));
         tmem_wait_ld();
+        // S_x is in registers: the issuer may compute the next S into it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarSRead + x]);
 
         const int kv0 = (w.jb + j) * kTileRows;
         if ((CAUSAL && (MODE != kSquare ? kv0 + kTileRows - 1 > imin_x + off : j == nx - 1)) || kv0 + kTileRows > Nk) {
@@ -561,18 +558,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // (no key seen yet)
         const float alpha = ex2_approx(m - m_use);
         // The tile's largest weight (computed exactly as the loop below does)
-        // and its bf16 rounding error.  With the reference max lagging the
+        // and its 16-bit rounding error.  With the reference max lagging the
         // row max, that weight is not a power of two, and the PV MMA sees it
-        // rounded to bf16; normalising O by a sum that carries the same
-        // rounding keeps O the weighted mean of V that the MMA computed.
+        // rounded; normalising O by a sum that carries the same rounding
+        // keeps O the weighted mean of V that the MMA computed.
         const float pmax = ex2_approx(fmaf(mx, scale_log2, -m_use));
         const float dpmax = (kF16 ? f16lo_to_f32(pack_f16x2(pmax, 0.f)) : unpack_bf16x2(pack_bf16x2(pmax, 0.f)).x) - pmax;
         if (j < turns && !(ok = take_turn())) break;
+        // P_x is free once PV(k-1), which reads it, has completed (that also
+        // makes O_x stable for the rescale below); at a unit's first tile,
+        // once this warp's O stores of the previous unit have read their
+        // staging rows (this warp's rows of P_x).
+        bool pv_seen = k == 0 || mbar_test_wait(&bars[kBarPVDone + x], (k - 1) & 1);
+        if (C::kTmaOut && j == 0) {
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+        }
 
         // P = 2^(s * scale_log2 - m) on packed pairs; 4 independent pair sums.
         const uint64_t negm2 = f2_pack(-m_use, -m_use);
-        // P goes to TMEM (bf16 pairs over the first 64 S columns, all of which
-        // are already in registers) 16 columns at a time.
+        // P goes to shared memory (row r of P_x) 32 columns at a time.
         uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -585,17 +590,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             acc[i & 3] = fadd2(acc[i & 3], f2_pack(p0, p1));
             pk[i] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
-          tmem_st16u(tS + 16 * c, pk);
+          if (c == 0 && !pv_seen && !(ok = mbar_wait(&bars[kBarPVDone + x], (k - 1) & 1, status))) break;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            store_square_chunk(sP, r, 4 * c + q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
+        if (!ok) break;
         const float2 a01 = f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])));
         const float rs = a01.x + a01.y;
         if (j < turns) pass_turn();
 
         if (j >= 1 && __any_sync(0xffffffffu, grow)) {
-          if (dual) {
-            if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
-            tc_fence_after();
-          }
           const uint64_t alpha2 = f2_pack(alpha, alpha);
           if constexpr (D >= 32) {
 #pragma unroll
@@ -619,11 +624,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int e = 0; e < 16; ++e) o[e] *= alpha;
             tmem_st16(tO, o);
           }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+        // P_x (shared memory, generic proxy) is read by the MMA (async proxy).
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarPFull + b]);
+        if (lane == 0) mbar_arrive(&bars[kBarPFull + x]);
         l = l * alpha + rs;
         lo = lo * alpha + (rs + dpmax);
         m = m_new;
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // unit's last PV_x has completed; the next unit's first PV_x (which
       // overwrites O_x) waits for this warp's next P_x, so the read-out cannot
       // race it.
-      if (!(ok = mbar_wait(&bars[kBarPVDone + sbuf(k - 1)], sphase(k - 1), status))) break;
+      if (!(ok = mbar_wait(&bars[kBarPVDone + x], (k - 1) & 1, status))) break;
       tc_fence_after();
       const float inv_l = lo > 0.f ? v_scale / lo : 0.f;
       // bf16 output leaves through shared memory and TMA stores, so the warp
@@ -675,16 +682,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int row_w0 = w.q0 + x * kTileRows + (warp & 3) * 32;  // this warp's first row
       const bool tma_out = C::kTmaOut && !partial && (MODE != kVarlen || row_w0 + 32 <= w.M);
       if (tma_out) {
-        const uint32_t slice = smem_u32(smem + C::kOStage + warp * 4096);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
+          // this warp's 32 rows of P_x in 64-column box h (the last PV has read them)
+          const uint32_t slice = sP + h * Square::kBoxBytes + (warp & 3) * 4096;
           float o[64];
           tmem_ld32(tO + 64 * h, *reinterpret_cast<float(*)[32]>(o));
           tmem_ld32(tO + 64 * h + 32, *reinterpret_cast<float(*)[32]>(o + 32));
           tmem_wait_ld();
-          // the slice is free once this warp's previous store has read it
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             st_shared_v4(slice + sw128_offset(lane, c), pack_bf16x2(o[8 * c + 0] * inv_l, o[8 * c + 1] * inv_l),

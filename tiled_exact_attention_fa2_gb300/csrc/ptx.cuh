@@ -93,6 +93,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t 
 // Wait until the phase with the given parity has completed.  Bounded: returns
 // false (and records kDevWaitTimeout in *status) after timeout_ns of
 // %globaltimer time (FA2_WAIT_TIMEOUT_NS unless given).
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 template <bool SLEEP = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           uint64_t timeout_ns = FA2_WAIT_TIMEOUT_NS) {
@@ -117,6 +130,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 // Sleeping variant for long, non-critical waits.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, int* status) {
   return mbar_wait<true>(bar, parity, status);
+}
+
+// Wait for two phases: both are tested at once first, so that two phases
+// that have already completed cost one test latency.
+__device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, int* status) {
+  const bool ra = mbar_test_wait(a, pa), rb = mbar_test_wait(b, pb);
+  return (ra || mbar_wait(a, pa, status)) && (rb || mbar_wait(b, pb, status));
 }
 
 // ---------------------------------------------------------------- TMA
