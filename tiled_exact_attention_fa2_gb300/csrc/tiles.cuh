@@ -11,7 +11,17 @@
 
 namespace fa2 {
 
-constexpr int kTileRows = 128;  // BLOCK_M = BLOCK_N = 128 query / key rows
+constexpr int kTileRows = 128;
+
+// The descriptor of an operand `off` bytes (a multiple of 16) past the one
+// `d` describes: only the start-address field changes, and it stays inside
+// its 14 bits for any shared-memory address, so adding to the low word is
+// exact.  Written so that the descriptor of the operand's base is built once
+// and each K step costs one 32-bit add.
+__device__ __forceinline__ uint64_t smem_desc_step(uint64_t d, uint32_t off) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (off >> 4);
+  return (d & 0xFFFFFFFF00000000ull) | lo;
+}  // BLOCK_M = BLOCK_N = 128 query / key rows
 
 template <int D>
 struct HeadDim {
@@ -28,14 +38,12 @@ struct HeadDim {
   // contraction index K ("K-major"), at contraction step kk (16 columns).
   static __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
     const int k = kk * 16;
-    const uint32_t addr = base + (k / kBoxCols) * kBoxBytes + (k % kBoxCols) * 2;
-    return make_smem_desc(addr, 16, kSBO, kSwizzle);
+    return smem_desc_step(make_smem_desc(base, 16, kSBO, kSwizzle), (k / kBoxCols) * kBoxBytes + (k % kBoxCols) * 2);
   }
   // Operand whose rows are the contraction index K and whose D columns are
   // the M (or N) index ("MN-major"), at contraction step kk (16 rows).
   static __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
-    const uint32_t addr = base + kk * 16 * kRowBytes;
-    return make_smem_desc(addr, kBoxBytes, kSBO, kSwizzle);
+    return smem_desc_step(make_smem_desc(base, kBoxBytes, kSBO, kSwizzle), kk * 16 * kRowBytes);
   }
 };
 
