@@ -102,14 +102,22 @@ def backward_roles(e, n_iter, sd, pieces, early_release=False, planted=None):
             yield "PFull", it
             mma(f"dV{it}", ("dO", ds))
             commit(*([("DoEmpty", ds)] if sd > 1 else []), "DvDone")
+            dq_done = False
             if it + 1 < n_iter:
                 yield "DvDone", it
                 yield ("QFull", (it + 1) % SQ), (it + 1) // SQ
                 mma(f"S{it + 1}", ("Q", (it + 1) % SQ))
+                # dQ(i) goes out before the last quarter of S(i+1) when dS(i)
+                # is already there (a non-blocking test in the kernel)
+                if e.bars["DsFull"].done >= it + 1:
+                    mma(f"dQ{it}", "dS")
+                    commit("DqFull")
+                    dq_done = True
                 commit("SFull")
-            yield "DsFull", it
-            mma(f"dQ{it}", "dS")
-            commit("DqFull")
+            if not dq_done:
+                yield "DsFull", it
+                mma(f"dQ{it}", "dS")
+                commit("DqFull")
             mma(f"dK{it}", "dS", ("Q", qs))
             commit(("QEmpty", qs))
         commit("AccFull", "Drain")
