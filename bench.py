@@ -50,8 +50,8 @@ KERNEL_TRAFFIC = {
     # (kernel, workload, causal): (read + write bytes, digest of the sources).
     # Capture summarised in the DRAM-traffic profile of the long causal
     # workload (dram__bytes_read.sum + dram__bytes_write.sum, one launch each).
-    ("fa2_fwd_kernel", "long", True): (405997568 + 117733632, "8c6aa5ebb913f415"),
-    ("fa2_bwd_kernel", "long", True): (836526848 + 505889792, "d91e5bdcc3a44731"),
+    ("fa2_fwd_kernel", "long", True): (405682688 + 117764352, "8c6aa5ebb913f415"),
+    ("fa2_bwd_kernel", "long", True): (836628224 + 505537536, "1517a64e2985abcf"),
 }
 
 KERNEL_SOURCES = {

@@ -140,13 +140,13 @@ def backward_roles(e, n_iter, sd, pieces, early_release=False, planted=None):
             if pieces <= 3 or early_release:
                 e.arrive("DqDrained")
             for c in range(pieces):
-                if pieces == 4 and c == 1:
-                    e.arrive("DqDrained")
                 gi = it * pieces + c
                 bsel, u = gi & 1, gi >> 1
                 if gi >= 2:
                     yield ("StageFree", bsel), u - 1
                 e.arrive(("StageFull", bsel))
+                if pieces == 4 and c == 0:  # the fourth piece is read, then the columns released
+                    e.arrive("DqDrained")
                 if w == 0:  # lane 0 of the first drain warp issues the reduce
                     yield ("StageFull", bsel), u
                     issued.append(gi)

@@ -634,8 +634,10 @@ __global__ void __launch_bounds__(512, 1)
       }
       // The first three pieces are read from TMEM at once (96 registers),
       // the fourth as soon as the first is staged, and the columns are
-      // released right after that read: dP^T(i+1) reuses them, so only one
-      // piece's staging lies between dQ landing and the release.
+      // released right after that read (before the first reduce-add is
+      // issued, which waits for the previous one to have read its source):
+      // dP^T(i+1) reuses them, so only one piece's staging lies between dQ
+      // landing and the release (+2 % over releasing after that reduce).
       constexpr int kFirst = C::kChunks < 3 ? C::kChunks : 3;
       float g[3][C::kChunk];
 #pragma unroll
@@ -654,15 +656,6 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
         const int gi = it * C::kChunks + c, bsel = gi & 1, u = gi >> 1;
-        if constexpr (C::kChunks == 4) {
-          if (c == 1) {  // piece 3 into piece 0's registers, then release
-            tmem_ld32(tmem + lane_base + C::kColDQ + 3 * 32, g[0]);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
-          }
-        }
         const int slot = c == 3 ? 0 : c;
         if (gi >= 2 && !(ok = mbar_wait_sleep(&bars[kBarStageFree + bsel], (u - 1) & 1, status))) break;
         const uint32_t sb = sStage + bsel * C::kStageBytes;
@@ -675,6 +668,15 @@ __global__ void __launch_bounds__(512, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarStageFull + bsel]);
+        if constexpr (C::kChunks == 4) {
+          if (c == 0) {  // piece 3 into piece 0's registers (just staged), then release
+            tmem_ld32(tmem + lane_base + C::kColDQ + 3 * 32, g[0]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarDqDrained]);
+          }
+        }
         if (issuer) {
           if ((ok = mbar_wait(&bars[kBarStageFull + bsel], u & 1, status))) {
             if constexpr (DQM == kDqSplit) {
