@@ -10,7 +10,9 @@ counts follow the kernel's FwdBar enum; a unit is the pair (K/V tiles of
 query tile A, K/V tiles of query tile B) that `fwd_unit` computes.  K and V
 tiles share one ring of three slots, loaded in the order K_0, (K_j, V_{j-1})
 for j = 1 .. n-1, V_{n-1}.  The scheduler barriers (one response per unit,
-read by all eleven roles) are included.
+read by all eleven roles) are included.  (The softmax warps of the two
+tiles no longer take turns at the exponentials, so the model has no token
+barriers.)
 
 Besides the barrier phases, the model tracks the data the barriers protect
 and reports a hazard when a protocol step would let one side overwrite what
@@ -35,7 +37,7 @@ def ring_pos_v(j, n):
     return 2 * j + 2 if j + 1 < n else 2 * n - 1
 
 
-def forward_roles(e, units, turns=True, planted=None):
+def forward_roles(e, units, planted=None):
     """Roles of one CTA.  ``planted`` names one deliberate protocol mistake
     (for the tests that check the model catches it)."""
     for s in range(2):
@@ -45,9 +47,6 @@ def forward_roles(e, units, turns=True, planted=None):
     for s in range(RING):
         e.bar(("KVFull", s), 1, f"KVFull[{s}]")
         e.bar(("KVEmpty", s), 2, f"KVEmpty[{s}]")
-    for w in range(4):
-        e.bar(("TokA", w), 1, f"TokA[{w}]")
-        e.bar(("TokB", w), 1, f"TokB[{w}]")
 
     reading = {sl: set() for sl in range(RING)}  # MMAs in flight that read a ring slot
     s_read = [[0] * 4 for _ in range(2)]  # S tiles each softmax warp has read, per tile
@@ -172,34 +171,19 @@ def forward_roles(e, units, turns=True, planted=None):
             e.arrive(("SchedEmpty", n & 1))
 
     def softmax(x, w):
-        k = tn = 0
-        tok_wait, tok_pass = (("TokB", w), ("TokA", w)) if x else (("TokA", w), ("TokB", w))
+        k = 0
         for n, cnt in enumerate(units):
             nx = cnt[x]
-            # turns only for the K/V tiles both query tiles visit
-            n_turns = min(cnt) if (turns and min(cnt) > 0) else 0
-            if planted == "phantom_turns_a" and x == 0 and n_turns:  # tile A also takes B's extra turns
-                n_turns = max(cnt)
-            for j in range(max(nx, n_turns)):
-                if j < nx:
-                    yield ("SFull", x), k
-                    s_read[x][w] += 1
-                    e.arrive(("SRead", x))
-                if j < n_turns:
-                    t = tn if x else tn - 1
-                    if t >= 0:
-                        yield tok_wait, t
-                if j < nx:
-                    if k >= 1 and planted != "p_before_pv_done":
-                        yield ("PVDone", x), k - 1
-                    if pv_done[x] < k:
-                        hazard(f"P_{'AB'[x]} #{k} written while P V #{k - 1} may still read P")
-                if j < n_turns:
-                    e.arrive(tok_pass)
-                    tn += 1
-                if j < nx:
-                    e.arrive(("PFull", x))
-                    k += 1
+            for j in range(nx):
+                yield ("SFull", x), k
+                s_read[x][w] += 1
+                e.arrive(("SRead", x))
+                if k >= 1 and planted != "p_before_pv_done":
+                    yield ("PVDone", x), k - 1
+                if pv_done[x] < k:
+                    hazard(f"P_{'AB'[x]} #{k} written while P V #{k - 1} may still read P")
+                e.arrive(("PFull", x))
+                k += 1
             if nx > 0:
                 yield ("PVDone", x), k - 1
             yield ("SchedFull", n & 1), n >> 1
@@ -278,9 +262,3 @@ def test_model_catches_p_written_while_the_previous_p_v_may_run():
     found = _first_failure("p_before_pv_done")
     assert found and "may still read P" in found
 
-
-def test_model_catches_turns_taken_by_one_tile_only():
-    # Tile A taking turns for the K/V tiles only tile B visits (while B
-    # takes turns only for the shared ones) puts the two token barriers out
-    # of step: a waiter ends up two phases behind or waits forever.
-    assert _first_failure("phantom_turns_a", kind="causal", seeds=2000)

@@ -43,8 +43,7 @@
 // The reference value m that the exponentials subtract is raised only when a
 // tile's row max exceeds it by more than a slack (15 or 8 log2 units), so the
 // weights stay below 2^slack and O is rescaled in TMEM (for the whole
-// warp) only on those rare tiles; softmax warps w and w + 4, which share an
-// SMSP, take turns at the exponentials.  The softmax arithmetic runs on
+// warp) only on those rare tiles.  The softmax arithmetic runs on
 // packed fp32 pairs (f32x2 FMA/ADD/MUL) and 3-input max to halve its
 // instruction count.
 #include <cuda.h>
@@ -88,9 +87,7 @@ enum FwdBar {
   kBarDrain = 18,       // +tile
   kBarSchedFull = 20,   // +slot (2): scheduler response landed (16 transaction bytes)
   kBarSchedEmpty = 22,  // +slot: every role has read the response (kSchedReaders arrivals)
-  kBarTokA = 24,        // +SMSP slot (4): softmax warp of tile A may start its exponentials
-  kBarTokB = 28,        // +SMSP slot (4): softmax warp of tile B may start its exponentials
-  kNumFwdBars = 32,
+  kNumFwdBars = 24,
 };
 
 // K and V tiles share one ring of three slots, loaded in the order the MMAs
@@ -271,10 +268,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int s = 0; s < kRingSlots; ++s) {
       mbar_init(&bars[kBarKVFull + s], 1);
       mbar_init(&bars[kBarKVEmpty + s], 2);
-    }
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(&bars[kBarTokA + s], 1);
-      mbar_init(&bars[kBarTokB + s], 1);
     }
     fence_mbar_init();
   }
@@ -479,27 +472,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t sP = smem_u32(smem + C::kP) + x * C::kPBytes;
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     int k = 0;  // S_x tiles consumed so far
-    // Softmax warps w (tile A) and w + 4 (tile B) share an SMSP and take
-    // turns at the exponentials, so that the two never contend for its MUFU
-    // and issue slots: per unit, turn j of tile A, then turn j of tile B, for
-    // every K/V tile j that both tiles visit.  A tile's K/V tiles beyond the
-    // other's (tile B's diagonal tile in a causal unit) take no turn: the
-    // other tile is then in its epilogue or starting its next unit, and
-    // need not wait for them.  Tile A's turn t waits for B's turn t - 1;
-    // B's turn t waits for A's turn t.  Each waiter is exactly one phase
-    // behind the token barrier it waits on.
-    int tn = 0;  // turns this warp has taken
-    uint64_t* tok_wait = &bars[(x ? kBarTokB : kBarTokA) + (warp & 3)];
-    uint64_t* tok_pass = &bars[(x ? kBarTokA : kBarTokB) + (warp & 3)];
-    auto take_turn = [&]() -> bool {
-      const int t = x ? tn : tn - 1;
-      return t < 0 || mbar_wait(tok_wait, t & 1, status);
-    };
-    auto pass_turn = [&]() {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tok_pass);
-      ++tn;
-    };
+    // Softmax warps w (tile A) and w + 4 (tile B) share an SMSP and its
+    // MUFU.  With P in TMEM (an earlier design) they took turns at the
+    // exponentials, passing a token per SMSP, and that was 4-11 % faster
+    // than letting the loops overlap; with P in shared memory the turns only
+    // made one tile wait for the other, and the forward is 1-3 % faster
+    // without them.
     bool ok = true;
 #pragma unroll 1
     for (int n = 0, u = static_cast<int>(blockIdx.x); ok && u >= 0; ++n) {
@@ -507,8 +485,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const FwdUnit w = fwd_unit<CAUSAL, MODE>(p, u, num_row_tiles, num_pairs, status);
       if (!w.valid) break;
       const int nx = x ? w.cnt[1] : w.cnt[0];  // (selects keep the struct in registers)
-      // Turns are taken only in units where both tiles have K/V tiles.
-      const int turns = (w.cnt[0] > 0 && w.cnt[1] > 0) ? min(w.cnt[0], w.cnt[1]) : 0;
       const int q_row = w.q0 + x * kTileRows + r;              // row in the row-head
       const int qi = MODE == kGeneral ? q_row % p.Nq : q_row;  // its query index
       const int imin_x = x ? w.imin[1] : w.imin[0];
@@ -564,7 +540,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // keeps O the weighted mean of V that the MMA computed.
         const float pmax = ex2_approx(fmaf(mx, scale_log2, -m_use));
         const float dpmax = (kF16 ? f16lo_to_f32(pack_f16x2(pmax, 0.f)) : unpack_bf16x2(pack_bf16x2(pmax, 0.f)).x) - pmax;
-        if (j < turns && !(ok = take_turn())) break;
         // P_x is free once PV(k-1), which reads it, has completed (that also
         // makes O_x stable for the rescale below); at a unit's first tile,
         // once this warp's O stores of the previous unit have read their
@@ -598,7 +573,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!ok) break;
         const float2 a01 = f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])));
         const float rs = a01.x + a01.y;
-        if (j < turns) pass_turn();
 
         if (j >= 1 && __any_sync(0xffffffffu, grow)) {
           const uint64_t alpha2 = f2_pack(alpha, alpha);
