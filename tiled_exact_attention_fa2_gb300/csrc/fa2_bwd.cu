@@ -119,6 +119,9 @@ struct BwdCfg {
 
 // ---------------------------------------------------------------- preprocess
 // D[row] = sum_c dO[row, c] * O[row, c]; also zero the dQ accumulator.
+// Blocks take rows from the end, so the rows of the first heads come last:
+// the main kernel's first CTAs visit those heads and find their dO, D and
+// zeroed dQ rows (and the forward's last O rows) still in L2.
 template <int D>
 __global__ void __launch_bounds__(256) fa2_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                                  const __nv_bfloat16* __restrict__ dO,
@@ -127,7 +130,8 @@ __global__ void __launch_bounds__(256) fa2_bwd_preprocess_kernel(const __nv_bflo
   constexpr int kTpr = D / 8;  // threads per row, 16 bytes each
   griddep_wait();
   griddep_launch_dependents();
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / kTpr;
+  const long long rb = static_cast<long long>(gridDim.x) - 1 - blockIdx.x;
+  const long long row = (rb * blockDim.x + threadIdx.x) / kTpr;
   const int sub = threadIdx.x % kTpr;
   float acc = 0.f;
   if (row < rows) {
@@ -147,14 +151,12 @@ __global__ void __launch_bounds__(256) fa2_bwd_preprocess_kernel(const __nv_bflo
   for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && sub == 0) Dvec[row] = acc;
 
-  // Zero dQacc (rows * D fp32) with 16-byte stores, grid-stride (none when
-  // dQ leaves as per-tile partials).
-  if (dq_acc == nullptr) return;
-  const long long n4 = rows * D / 4;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
-    acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // Zero this row of dQacc (D fp32 = 2 * kTpr 16-byte stores; none when dQ
+  // leaves as per-tile partials).
+  if (dq_acc == nullptr || row >= rows) return;
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc) + row * (D / 4);
+  acc4[sub] = make_float4(0.f, 0.f, 0.f, 0.f);
+  acc4[sub + kTpr] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------- dQ convert
@@ -164,7 +166,10 @@ __global__ void __launch_bounds__(256) fa2_dq_convert_kernel(const float* __rest
   griddep_wait();
   griddep_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+  // From the end: the main kernel's last CTAs reduced into the last heads'
+  // rows, which are still in L2 when this kernel starts.
+  for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < n8; j += stride) {
+    const long long i = n8 - 1 - j;
     const float4 a = __ldg(reinterpret_cast<const float4*>(dq_acc) + 2 * i);
     const float4 b = __ldg(reinterpret_cast<const float4*>(dq_acc) + 2 * i + 1);
     reinterpret_cast<uint4*>(dq)[i] =
