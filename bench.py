@@ -51,7 +51,7 @@ KERNEL_TRAFFIC = {
     # Capture summarised in the DRAM-traffic profile of the long causal
     # workload (dram__bytes_read.sum + dram__bytes_write.sum, one launch each).
     ("fa2_fwd_kernel", "long", True): (407450880 + 117617664, "3d4c11422ef5c5e3"),
-    ("fa2_bwd_kernel", "long", True): (836628224 + 505537536, "1517a64e2985abcf"),
+    ("fa2_bwd_kernel", "long", True): (836262656 + 505752832, "15c764e6e3932078"),
 }
 
 KERNEL_SOURCES = {
