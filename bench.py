@@ -653,16 +653,16 @@ def run_gpu(args, w, causal):
         host = {k: x[k].pin_memory() for k in ("q", "k", "v", "dO")}
         host.update({k: torch.empty_like(host["q"]).pin_memory() for k in ("o", "dq", "dk", "dv")})
         host["lse"] = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-        devb = dict(g, o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+        ws = torch.empty(fa2.fa2_step_from_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
         for _ in range(max(1, args.warmup)):
-            fa2.attention_step_from_host(host, devb, causal, scale, stream)
+            fa2.fa2_step_from_host(host, causal, scale, stream, workspace=ws)
         torch.cuda.synchronize()
         _barrier(world)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(args.steps):
-            fa2.attention_step_from_host(host, devb, causal, scale, stream)
+            fa2.fa2_step_from_host(host, causal, scale, stream, workspace=ws)
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = _max_over_ranks(a.elapsed_time(b), world) / args.steps

@@ -297,6 +297,51 @@ int fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, 
 /* Bytes of the fixed scratch array fa2_bwd_noalloc uses. */
 size_t fa2_noalloc_scratch_capacity(void);
 
+/*
+ * One forward and one backward pass whose tensors live in HOST memory: the
+ * end-to-end form of fa2_fwd followed by fa2_bwd on the same problem, with
+ * the same results (o, lse, dk, dv bit for bit; dq up to the order of its
+ * fp32 reduction).  Every (batch, head) is an independent problem (the
+ * article's forward-pass bullet: one work unit per batch, head and query
+ * tile), so the B*H heads run as a pipeline over groups of heads: while a
+ * group's kernels run, later groups upload and earlier ones download.
+ *   q, k, v, dO      host bf16 [B,H,N,d] inputs
+ *   o, dq, dk, dv    host bf16 [B,H,N,d] outputs; lse host fp32 [B,H,N]
+ *   group_heads      host array of num_groups head counts (>= 1, at most 64
+ *                    groups) summing to B*H, or NULL for the default plan:
+ *                    B*H/8, three groups of B*H/4 and the rest (small first
+ *                    and last groups shorten the first upload and the last
+ *                    download), or min(B*H, 4) equal groups below 8 heads
+ *   compute_streams  1 to 4: groups take turns on `stream` and up to three
+ *                    library streams, so that one group's kernels overlap
+ *                    the next group's
+ *   workspace        device scratch, 256-byte aligned, of at least
+ *                    fa2_step_from_host_workspace_bytes(...) bytes with the
+ *                    same group plan and stream count: device copies of the
+ *                    ten tensors and each compute stream's forward and
+ *                    backward scratch; owned by the caller, untouched by
+ *                    anything else until `stream` has passed this call.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to overlap the kernels; pageable memory works but serialises.
+ * Copies are plain stream-ordered copies, one per tensor and group, on two
+ * library streams (host to device, device to host); the library's streams
+ * and events are created on a device's first call and kept.  The work starts
+ * after everything enqueued on `stream` before the call, and `stream` waits
+ * for the last download: synchronise it before reading the outputs.  Calls
+ * on one device from several host threads are enqueued one at a time.
+ * Errors (checked before anything is enqueued): FA2_ERR_NULL for a NULL
+ * pointer, FA2_ERR_HEADDIM, FA2_ERR_SHAPE for sizes, an invalid group plan
+ * or stream count, FA2_ERR_SCALE, FA2_ERR_WORKSPACE; then FA2_ERR_CUDA if a
+ * copy, event or launch fails, or an error of fa2_fwd_ws / fa2_bwd_ws.
+ * The workspace size function returns 0 for invalid arguments.
+ */
+size_t fa2_step_from_host_workspace_bytes(int B, int H, int N, int d, const int* group_heads, int num_groups,
+                                          int compute_streams);
+int fa2_step_from_host(const void* q, const void* k, const void* v, const void* dO, void* o, float* lse, void* dq,
+                       void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                       const int* group_heads, int num_groups, int compute_streams, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* fa2_status_string(int status);
 

@@ -45,7 +45,7 @@ def test_status_strings(lib):
         assert fa2.fa2_status_string(s)
     assert fa2.fa2_status_string(0) == "ok"
     assert "unknown" in fa2.fa2_status_string(12345)
-    assert fa2.fa2_abi_version() == 100
+    assert fa2.fa2_abi_version() == 101
 
 
 def test_workspace_bytes(lib):
@@ -270,3 +270,34 @@ def test_bwd_deterministic_and_dq_reduce_reject_bad_arguments(lib):
     assert r(A, 2 * A, 1, 1, 256, 64, 0.125, 1, None) == 3
     assert r(A + 8, 2 * A, 1, 1, 256, 128, 0.125, 1, None) == 4
     assert r(A, A, 1, 1, 256, 128, 0.125, 1, None) == 9
+
+
+def test_step_from_host_rejects_bad_arguments_before_any_cuda_call(lib):
+    f, ws_bytes = lib.fa2_step_from_host, lib.fa2_step_from_host_workspace_bytes
+    I = ctypes.c_int
+    plan = (I * 3)(1, 2, 5)
+    need = ws_bytes(2, 4, 256, 64, None, 0, 2)
+    assert need > 8 * 2 * 4 * 256 * 64 * 2  # the ten tensors plus two streams' scratch
+    # an explicit plan: the largest group sets the per-stream scratch
+    assert ws_bytes(2, 4, 256, 64, plan, 3, 1) > 0
+    assert ws_bytes(2, 4, 256, 64, plan, 2, 1) == 0        # 1 + 2 != 8 heads
+    assert ws_bytes(2, 4, 256, 64, (I * 2)(8, 0), 2, 1) == 0  # empty group
+    assert ws_bytes(2, 4, 256, 64, None, 0, 0) == 0        # stream count
+    assert ws_bytes(2, 4, 256, 64, None, 0, 5) == 0
+    assert ws_bytes(2, 4, 256, 48, None, 0, 2) == 0
+    good = dict(B=2, H=4, N=256, d=64, scale=0.125, plan=None, n=0, streams=2, ws=A, nbytes=need)
+
+    def call(ptr=A, **kw):
+        a = dict(good, **kw)
+        return f(ptr, A, A, A, A, A, A, A, A, a["B"], a["H"], a["N"], a["d"], a["scale"], 1, a["plan"], a["n"],
+                 a["streams"], a["ws"], a["nbytes"], None)
+
+    assert call(ptr=None) == 1                       # FA2_ERR_NULL
+    assert call(d=48) == 3                           # FA2_ERR_HEADDIM
+    assert call(N=0) == 2                            # FA2_ERR_SHAPE
+    assert call(scale=float("nan")) == 5             # FA2_ERR_SCALE
+    assert call(streams=0) == 2
+    assert call(plan=plan, n=2) == 2                 # plan does not sum to B * H
+    assert call(ws=None) == 8                        # FA2_ERR_WORKSPACE
+    assert call(ws=A + 16) == 8                      # not 256-byte aligned
+    assert call(nbytes=need - 1) == 8

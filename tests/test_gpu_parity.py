@@ -129,11 +129,11 @@ def test_nonzero_stream_and_invalid_args_raise():
 
 
 def test_host_step_pipeline_matches_device_calls():
-    # attention_step_from_host pipelines host<->device copies with the
-    # kernels over groups of heads (equal groups, the default ramp, explicit
-    # groups; one to three compute streams); its results must be those of plain
-    # fa2_fwd / fa2_bwd on the same inputs (bit-identical except dQ, whose
-    # fp32 reduction order varies between runs).
+    # fa2_step_from_host (C ABI) pipelines host<->device copies with the
+    # kernels over groups of heads (equal groups, the default plan, explicit
+    # groups; one to four compute streams); its results must be those of
+    # plain fa2_fwd / fa2_bwd on the same inputs (bit-identical except dQ,
+    # whose fp32 reduction order varies between runs).
     import tiled_exact_attention_fa2_gb300 as fa2
     from parity_util import check_grad, to_np
     w = workloads.WORKLOADS["small"]
@@ -144,19 +144,24 @@ def test_host_step_pipeline_matches_device_calls():
     host = {k: x[k].pin_memory() for k in ("q", "k", "v", "dO")}
     host.update({k: torch.zeros_like(host["q"]).pin_memory() for k in ("o", "dq", "dk", "dv")})
     host["lse"] = torch.zeros((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
-    devb = {k: torch.empty_like(t) for k, t in g.items()}
-    devb.update({k: torch.empty_like(g["q"]) for k in ("o", "dq", "dk", "dv")})
-    devb["lse"] = torch.empty_like(lse)
     plans = [dict(chunks=1, compute_streams=1), dict(chunks=3), dict(),  # default: ramp of groups, 2 streams
-             dict(groups=[1, 5, 10, 10, 6], compute_streams=3)]
+             dict(groups=[1, 5, 10, 10, 6], compute_streams=3), dict(chunks=32, compute_streams=4)]
     for plan in plans:
         for name in ("o", "lse", "dq", "dk", "dv"):
             host[name].zero_()
-        fa2.attention_step_from_host(host, devb, True, None, None, **plan)
+        fa2.fa2_step_from_host(host, True, None, None, **plan)
         torch.cuda.synchronize()
         assert fa2.fa2_device_status(reset=True) == 0
         assert torch.equal(host["o"], o.cpu()) and torch.equal(host["lse"], lse.cpu())
         assert torch.equal(host["dk"], dk.cpu()) and torch.equal(host["dv"], dv.cpu())
         check_grad(to_np(host["dq"]), to_np(dq), "dQ")
+    # a caller-owned workspace, reused; a side stream as `stream`
+    ws = torch.empty(fa2.fa2_step_from_host_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=DEV)
+    side = torch.cuda.Stream()
+    for _ in range(2):
+        host["o"].zero_()
+        fa2.fa2_step_from_host(host, True, None, side, workspace=ws)
+        side.synchronize()
+        assert torch.equal(host["o"], o.cpu()) and torch.equal(host["dv"], dv.cpu())
     with pytest.raises(ValueError):
-        fa2.attention_step_from_host(host, devb, True, None, None, groups=[16, 15])
+        fa2.fa2_step_from_host(host, True, None, None, groups=[16, 15])

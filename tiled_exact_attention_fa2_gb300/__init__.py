@@ -21,7 +21,8 @@ from . import _build
 
 __all__ = [
     "FA2Error", "load_library", "fa2_fwd", "fa2_fwd_ws", "fa2_fwd_workspace_bytes", "fa2_bwd", "fa2_bwd_ws", "fa2_bwd_workspace_bytes",
-    "fa2_status_string", "fa2_device_status", "fa2_abi_version", "attention_step_from_host",
+    "fa2_status_string", "fa2_device_status", "fa2_abi_version", "fa2_step_from_host",
+    "fa2_step_from_host_workspace_bytes",
     "fa2_bwd_stages", "fa2_bwd_noalloc", "fa2_fwd_gqa", "fa2_bwd_gqa", "fa2_fwd_splitkv",
     "fa2_fwd_varlen", "fa2_bwd_varlen", "prepared_step", "FA2_OK",
 ]
@@ -57,6 +58,9 @@ _SIGNATURES = {
     "fa2_last_error_detail": (ctypes.c_char_p, []),
     "fa2_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_noalloc_scratch_capacity": (_sz, []),
+    "fa2_step_from_host_workspace_bytes": (_sz, [_i, _i, _i, _i, ctypes.POINTER(_i), _i, _i]),
+    "fa2_step_from_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
+                                ctypes.POINTER(_i), _i, _i, _vp, _sz, _vp]),
     "fa2_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa2_bwd_gqa_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
@@ -500,123 +504,69 @@ def fa2_bwd_stages(q, k, v, o, dO, lse, Dvec, dq_acc, dq, dk, dv, scale: Optiona
     return dq, dk, dv
 
 
-_COPY_STREAMS = {}
-
-
-def _copy_streams(device):
-    """Two side streams per device: host->device and device->host copies."""
-    key = torch.device(device).index
-    if key not in _COPY_STREAMS:
-        _COPY_STREAMS[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
-    return _COPY_STREAMS[key]
-
-
-_COMPUTE_STREAMS = {}
-
-
-def _compute_streams(device, n):
-    """n extra compute streams per device, created once."""
-    if n <= 0:
-        return ()
-    key = (str(device), n)
-    if key not in _COMPUTE_STREAMS:
-        _COMPUTE_STREAMS[key] = tuple(torch.cuda.Stream(device=device) for _ in range(n))
-    return _COMPUTE_STREAMS[key]
-
-
-def attention_step_from_host(host: dict, dev: dict, causal: bool = True, scale: Optional[float] = None,
-                             stream=None, chunks: Optional[int] = None, groups=None,
-                             compute_streams: int = 2) -> dict:
-    """One forward + backward pass starting from pinned host tensors.
-
-    ``host`` holds pinned CPU bf16 tensors q, k, v, dO and pinned outputs
-    o, lse, dq, dk, dv; ``dev`` holds device buffers of the same names
-    ([B, H, N, d]; lse [B, H, N]).  Every (batch, head) is an independent
-    problem, so the B * H heads are processed in groups as a pipeline: the
-    host->device copy of a later group and the device->host copy of an
-    earlier one run while fa2_fwd and fa2_bwd of the current group run (a
-    group's forward starts once its q, k, v have arrived, and its O and LSE
-    go back while its backward runs).
-    Groups: ``groups`` (head counts summing to B * H), else ``chunks`` equal
-    groups, else by default a ramp of B*H/8, three of B*H/4 and the rest
-    (small first and last groups shorten the first upload and the last
-    download; the large middle ones keep the kernels efficient).  The groups
-    take turns on ``compute_streams`` streams (``stream`` and extra ones), so
-    one group's causal tail overlaps the next group's start.  Everything is
-    enqueued asynchronously and ``stream`` waits for the last copy:
-    synchronise it before reading ``host``.
-    """
-    s = torch.cuda.current_stream() if stream is None else stream
-    device = dev["q"].device
-    B, H, N, d = dev["q"].shape
-    BH = B * H
+def _group_plan(BH: int, chunks: Optional[int], groups):
+    """Head counts per group for fa2_step_from_host: `groups` as given,
+    `chunks` equal groups, or None for the library's default plan."""
     if groups is not None:
-        if sum(groups) != BH or min(groups) < 1:
+        sizes = [int(x) for x in groups]
+        if sum(sizes) != BH or min(sizes) < 1:
             raise ValueError(f"groups must be positive head counts summing to B * H = {BH}")
-        bounds = [0]
-        for size in groups:
-            bounds.append(bounds[-1] + int(size))
-        n = len(groups)
-    elif chunks is not None or BH < 8:
-        n = max(1, min(BH, chunks if chunks is not None else 4))
-        bounds = [BH * i // n for i in range(n + 1)]
-    else:
-        sizes = [BH // 8, BH // 4, BH // 4, BH // 4]
-        sizes.append(BH - sum(sizes))
-        bounds = [0]
-        for size in sizes:
-            bounds.append(bounds[-1] + size)
-        n = len(sizes)
-    cin, cout = _copy_streams(device)
-    flat = {k: (t.view(BH, N, d) if k != "lse" else t.view(BH, N)) for k, t in dev.items()}
-    hflat = {k: (t.view(BH, N, d) if k != "lse" else t.view(BH, N)) for k, t in host.items()}
-    start = torch.cuda.Event()
-    start.record(s)
-    cin.wait_event(start)  # the device buffers are free once earlier work on `stream` is done
-    def copies(stream, names, a, b, to_host):
-        with torch.cuda.stream(stream):
-            for name in names:
-                if to_host:
-                    hflat[name][a:b].copy_(flat[name][a:b], non_blocking=True)
-                else:
-                    flat[name][a:b].copy_(hflat[name][a:b], non_blocking=True)
-            e = torch.cuda.Event()
-            e.record(stream)
-        return e
+        return sizes
+    if chunks is not None:
+        n = max(1, min(BH, int(chunks)))
+        return [BH * (i + 1) // n - BH * i // n for i in range(n)]
+    return None
 
-    # Uploads: a group's q, k, v (all its forward needs), then its dO.
-    qkv_in, do_in = [], []
-    for c in range(n):
-        qkv_in.append(copies(cin, ("q", "k", "v"), bounds[c], bounds[c + 1], False))
-        do_in.append(copies(cin, ("dO",), bounds[c], bounds[c + 1], False))
-    comp = [s] + list(_compute_streams(device, compute_streams - 1))
-    for extra in comp[1:]:
-        extra.wait_event(start)
-    fwd_done, bwd_done = [], []
-    for c in range(n):
-        a, b = bounds[c], bounds[c + 1]
-        cs = comp[c % len(comp)]
-        view = {k: flat[k][a:b].unsqueeze(0) for k in flat}
-        cs.wait_event(qkv_in[c])
-        fa2_fwd(view["q"], view["k"], view["v"], view["o"], view["lse"], scale, causal, cs)
-        e = torch.cuda.Event()
-        e.record(cs)
-        fwd_done.append(e)
-        cs.wait_event(do_in[c])
-        fa2_bwd(view["q"], view["k"], view["v"], view["o"], view["dO"], view["lse"], view["dq"], view["dk"],
-                view["dv"], scale, causal, cs)
-        e = torch.cuda.Event()
-        e.record(cs)
-        bwd_done.append(e)
-    # Downloads: a group's O and LSE as soon as its forward is done, its
-    # gradients after its backward.
-    for c in range(n):
-        a, b = bounds[c], bounds[c + 1]
-        cout.wait_event(fwd_done[c])
-        copies(cout, ("o", "lse"), a, b, True)
-        cout.wait_event(bwd_done[c])
-        copies(cout, ("dq", "dk", "dv"), a, b, True)
-    done = torch.cuda.Event()
-    done.record(cout)
-    s.wait_event(done)
+
+def fa2_step_from_host_workspace_bytes(B: int, H: int, N: int, d: int, groups=None, compute_streams: int = 2) -> int:
+    arr, n = _int_array(groups)
+    return load_library().fa2_step_from_host_workspace_bytes(B, H, N, d, arr, n, compute_streams)
+
+
+def _int_array(values):
+    if values is None:
+        return None, 0
+    return (ctypes.c_int * len(values))(*values), len(values)
+
+
+def fa2_step_from_host(host: dict, causal: bool = True, scale: Optional[float] = None, stream=None,
+                       chunks: Optional[int] = None, groups=None, compute_streams: int = 2,
+                       workspace: Optional[torch.Tensor] = None) -> dict:
+    """One forward + backward pass on host tensors (C ABI fa2_step_from_host).
+
+    ``host`` holds CPU tensors (page-locked for overlap): bf16 q, k, v, dO
+    [B, H, N, d] and outputs o, dq, dk, dv (bf16, same shape) and lse (fp32
+    [B, H, N]).  The library pipelines the copies and kernels over groups of
+    heads (``groups`` head counts, ``chunks`` equal groups, or its default
+    plan) on ``compute_streams`` compute streams.  ``workspace`` is a CUDA
+    uint8 tensor of at least fa2_step_from_host_workspace_bytes(...) bytes
+    (allocated here when omitted).  Everything is enqueued on ``stream``
+    (default: the current stream); synchronise it before reading ``host``.
+    """
+    q = host["q"]
+    if q.dim() != 4 or q.dtype != torch.bfloat16 or q.is_cuda:
+        raise ValueError("host['q'] must be a CPU bfloat16 [B, H, N, d] tensor")
+    B, H, N, d = q.shape
+    for name in ("k", "v", "dO", "o", "dq", "dk", "dv"):
+        t = host[name]
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"host['{name}'] must be a contiguous CPU bfloat16 tensor shaped like q")
+    lse = host["lse"]
+    if tuple(lse.shape) != (B, H, N) or lse.dtype != torch.float32 or lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("host['lse'] must be a contiguous CPU float32 [B, H, N] tensor")
+    plan = _group_plan(B * H, chunks, groups)
+    arr, n = _int_array(plan)
+    lib = load_library()
+    need = lib.fa2_step_from_host_workspace_bytes(B, H, N, d, arr, n, compute_streams)
+    if need == 0:
+        raise FA2Error("fa2_step_from_host_workspace_bytes", 2)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=torch.cuda.current_device())
+    st = _stream(stream, workspace.device)
+    rc = lib.fa2_step_from_host(q.data_ptr(), host["k"].data_ptr(), host["v"].data_ptr(), host["dO"].data_ptr(),
+                                host["o"].data_ptr(), lse.data_ptr(), host["dq"].data_ptr(), host["dk"].data_ptr(),
+                                host["dv"].data_ptr(), B, H, N, d, _scale(scale, d), 1 if causal else 0, arr, n,
+                                compute_streams, workspace.data_ptr(), workspace.numel(), st)
+    if rc != FA2_OK:
+        raise FA2Error("fa2_step_from_host", rc)
     return host

@@ -910,7 +910,7 @@ int fa2_device_status(int* value, int reset) {
   return FA2_OK;
 }
 
-int fa2_abi_version(void) { return 100; }
+int fa2_abi_version(void) { return 101; }
 
 const char* fa2_last_error_detail(void) { return g_last_error; }
 
