@@ -669,7 +669,8 @@ def run_gpu(args, w, causal):
         h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "dO"))
         d2h = sum(host[k].numel() * host[k].element_size() for k in ("o", "lse", "dq", "dk", "dv"))
         e2e = {"value": job_tflops(world, fwd_flops + bwd_flops, e2e_ms), "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "api": "fa2_step_from_host (C ABI, pinned host buffers)"}
 
     peaks = _peaks()
     value = job_tflops(world, fwd_flops + bwd_flops, ms_step)
