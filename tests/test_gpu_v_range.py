@@ -41,10 +41,14 @@ def _check_scaled(o, lse, e, h, what):
     assert torch.equal(lse.select(1, h), lse.select(1, 0)), f"{what}: LSE differs"
 
 
-@pytest.mark.parametrize("exps", [(20,), (14,)], ids=["2^20", "2^14"])
-def test_heads_beyond_fp16_range_forward_and_backward(exps):
-    # 2^20: values up to about 4e6; 2^14: up to about 65536 (the range's edge)
-    B, N, d = 1, 300, 64
+@pytest.mark.parametrize("exps,N,d", [((20,), 300, 64), ((14,), 300, 64), ((20,), 1100, 128)],
+                         ids=["2^20", "2^14", "2^20_large_head"])
+def test_heads_beyond_fp16_range_forward_and_backward(exps, N, d):
+    # 2^20: values up to about 4e6; 2^14: up to about 65536 (the range's
+    # edge).  Heads of at most 64K elements are copied to fp16 and rescaled by
+    # one kernel, larger ones (1100 x 128) by the grid-wide copy and the
+    # per-head rescale.
+    B = 1
     x = _scaled_copies(workloads.make_inputs(B, 1, N, d, seed=31), exps)
     assert float(x["v"][0, 1].float().abs().max()) > 65504.0
     g = {k: t.to(DEV) for k, t in x.items()}

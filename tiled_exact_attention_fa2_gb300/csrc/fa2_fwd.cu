@@ -828,6 +828,64 @@ __global__ void __launch_bounds__(256) fa2_v_scale_kernel(const __nv_bfloat16* _
   if (threadIdx.x == 0) scales[h] = ldexpf(1.f, k);
 }
 
+// Small heads (rows * d <= kVHeadSmall): both steps above in one kernel, one
+// CTA per K/V head (copy, then rescale the head if it held a value beyond
+// the fp16 range), saving a launch where launches dominate.
+constexpr long long kVHeadSmall = 64 * 1024;
+__global__ void __launch_bounds__(256) fa2_v_to_f16_head_kernel(const __nv_bfloat16* __restrict__ v,
+                                                               __half* __restrict__ v16,
+                                                               float* __restrict__ scales, long long rows, int d,
+                                                               long long row_stride, long long head_stride) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int h = blockIdx.x;
+  const int per_row = d / 8;
+  const long long n8 = rows * per_row;
+  const long long base = static_cast<long long>(h) * head_stride;
+  auto at8 = [&](long long e8) { return base + (e8 / per_row) * row_stride + (e8 % per_row) * 8; };
+  bool big = false;
+  for (long long e8 = threadIdx.x; e8 < n8; e8 += blockDim.x) {
+    const long long i = at8(e8);
+    const uint4 a = *reinterpret_cast<const uint4*>(v + i);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t hv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+      big |= (fabsf(lo) > 65504.f && fabsf(lo) < INFINITY) || (fabsf(hi) > 65504.f && fabsf(hi) < INFINITY);
+      hv[e] = pack_f16x2(lo, hi);
+    }
+    *reinterpret_cast<uint4*>(v16 + i) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+  }
+  if (!__syncthreads_or(big)) {
+    if (threadIdx.x == 0) scales[h] = 1.f;
+    return;
+  }
+  // the rare head: the same rescaling as fa2_v_scale_kernel
+  const long long n = rows * d;
+  auto at = [&](long long e) { return base + (e / d) * row_stride + e % d; };
+  float mx = 0.f;
+  for (long long e = threadIdx.x; e < n; e += blockDim.x) {
+    const float a = fabsf(__bfloat162float(v[at(e)]));
+    if (a < INFINITY) mx = fmaxf(mx, a);
+  }
+  __shared__ float red[32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = 0.f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) mx = fmaxf(mx, red[i]);
+  int k = 0;
+  while (ldexpf(mx, -k) > 32768.f) ++k;
+  const float inv = ldexpf(1.f, -k);
+  for (long long e = threadIdx.x; e < n; e += blockDim.x) {
+    const long long i = at(e);
+    v16[i] = __float2half_rn(__bfloat162float(v[i]) * inv);
+  }
+  if (threadIdx.x == 0) scales[h] = ldexpf(1.f, k);
+}
+
 // Merge per-split results: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
 // One warp per row; lane l holds columns [l * D / 32, (l + 1) * D / 32).  The
 // split LSEs are read by the lanes in parallel (lane l: splits l, l + 32, ...)
@@ -898,6 +956,10 @@ int launch_fwd(const TmapSet& tm, const FwdProblem& p, int d, float scale, bool 
 int launch_v_to_f16(const void* v, void* v16, unsigned long long* v_flags, float* v_scale, unsigned long long call,
                     int heads, long long rows, int d, long long row_stride, long long head_stride, bool packed,
                     cudaStream_t stream) {
+  if (rows * d <= kVHeadSmall)
+    return launch_pdl(fa2_v_to_f16_head_kernel, dim3(static_cast<unsigned>(heads)), dim3(256), 0, stream,
+                      static_cast<const __nv_bfloat16*>(v), static_cast<__half*>(v16), v_scale, rows, d, row_stride,
+                      head_stride);
   const long long n8 = static_cast<long long>(heads) * rows * d / 8;
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;

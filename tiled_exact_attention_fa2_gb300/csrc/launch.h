@@ -98,7 +98,9 @@ int launch_fwd(const TmapSet& tm, const FwdProblem& p, int d, float scale, bool 
 // head, the power of two 2^k that brings its largest finite magnitude into
 // the fp16 range and rewrites the head's copy as fp16(v / 2^k).  Element
 // (row r, column c) of head h is v[r * row_stride + h * head_stride + c],
-// r < rows.  Flags holding another call's number count as clear.
+// r < rows.  Flags holding another call's number count as clear.  Heads of
+// at most 64K elements (rows * d) take one kernel instead: one CTA per head
+// copies it and, if it holds such a value, rescales it and sets v_scale[h].
 int launch_v_to_f16(const void* v, void* v16, unsigned long long* v_flags, float* v_scale, unsigned long long call,
                     int heads, long long rows, int d, long long row_stride, long long head_stride, bool packed,
                     cudaStream_t stream);
