@@ -325,7 +325,8 @@ size_t fa2_noalloc_scratch_capacity(void);
  * the copies to overlap the kernels; pageable memory works but serialises.
  * Copies are plain stream-ordered copies, one per tensor and group, on two
  * library streams (host to device, device to host); the library's streams
- * and events are created on a device's first call and kept.  The work starts
+ * and events are created on a device's first call and kept (created again
+ * after cudaDeviceReset, which gives the device a new context).  The work starts
  * after everything enqueued on `stream` before the call, and `stream` waits
  * for the last download: synchronise it before reading the outputs.  Calls
  * on one device from several host threads are enqueued one at a time.

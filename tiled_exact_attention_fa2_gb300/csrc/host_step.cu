@@ -77,11 +77,14 @@ Layout layout_of(int B, int H, int N, int d, int max_group, int compute_streams)
 }
 
 // Side streams (upload, download, extra compute) and the events that link
-// the stages, created once per device.  The mutex serialises the enqueue of
-// concurrent calls on one device, which share these.
+// the stages, created once per device and CUDA context (again after a device
+// reset, which changes the context id; kept when the id cannot be read).  The
+// mutex serialises the enqueue of concurrent calls on one device, which share
+// these.
 struct DeviceState {
   std::mutex mu;
   bool ready = false;
+  unsigned long long ctx_id = 0;
   cudaStream_t up = nullptr, down = nullptr;
   cudaStream_t comp[kMaxComputeStreams - 1] = {};
   cudaEvent_t start = nullptr, done = nullptr;
@@ -91,7 +94,11 @@ struct DeviceState {
 DeviceState g_state[kMaxDevices];
 
 int init_state(DeviceState& s) {
-  if (s.ready) return FA2_OK;
+  const unsigned long long ctx = fa2::current_context_id();
+  if (s.ready && (ctx == 0 || ctx == s.ctx_id)) return FA2_OK;
+  // (handles of an earlier context are invalid now; they are dropped)
+  s.ready = false;
+  s.ctx_id = ctx;
   cudaError_t e = cudaStreamCreateWithFlags(&s.up, cudaStreamNonBlocking);
   if (!e) e = cudaStreamCreateWithFlags(&s.down, cudaStreamNonBlocking);
   for (int i = 0; !e && i < kMaxComputeStreams - 1; ++i) e = cudaStreamCreateWithFlags(&s.comp[i], cudaStreamNonBlocking);

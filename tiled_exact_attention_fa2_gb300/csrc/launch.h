@@ -157,6 +157,9 @@ int validate_bwd_args(const void* q, const void* k, const void* v, const void* o
                       void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, float scale);
 // Record a CUDA failure for fa2_last_error_detail; returns FA2_ERR_CUDA.
 int record_cuda_failure(int cuda_code, const char* where);
+// Unique id of the calling thread's current CUDA context, 0 if none or
+// unreadable (changes after cudaDeviceReset).
+unsigned long long current_context_id();
 int read_bwd_status(int* value, bool reset);
 
 }  // namespace fa2

@@ -44,6 +44,10 @@ namespace {
 using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
+}  // namespace
+
+namespace fa2 {
+
 // Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
 // through the runtime so the library needs no link-time libcuda), or 0 when
 // there is none or it cannot be read.
@@ -67,6 +71,12 @@ unsigned long long current_context_id() {
     return 0;
   return id;
 }
+
+}  // namespace fa2
+
+namespace {
+
+using fa2::current_context_id;
 
 struct ScratchSlot {
   void* ptr;                 // device address of the array in context ctx_id
