@@ -163,5 +163,15 @@ def test_host_step_pipeline_matches_device_calls():
         fa2.fa2_step_from_host(host, True, None, side, workspace=ws)
         side.synchronize()
         assert torch.equal(host["o"], o.cpu()) and torch.equal(host["dv"], dv.cpu())
+    # pageable (not page-locked) host memory: slower, same results
+    pageable = {k: t.clone() for k, t in host.items()}
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        pageable[name].zero_()
+    assert not pageable["q"].is_pinned()
+    fa2.fa2_step_from_host(pageable, True, None, None, chunks=2)
+    torch.cuda.synchronize()
+    assert torch.equal(pageable["o"], o.cpu()) and torch.equal(pageable["lse"], lse.cpu())
+    assert torch.equal(pageable["dk"], dk.cpu()) and torch.equal(pageable["dv"], dv.cpu())
+    check_grad(to_np(pageable["dq"]), to_np(dq), "dQ (pageable)")
     with pytest.raises(ValueError):
         fa2.fa2_step_from_host(host, True, None, None, groups=[16, 15])
